@@ -1,0 +1,174 @@
+/*
+ * mma_gb300.h -- C ABI of the GB300 (sm_103a) dense multiply-accumulate
+ * library  D = A * B + C.
+ *
+ * Operation (page "CDNA2 dense MFMA builtins", section "Naming convention"):
+ * one matrix instruction adds the contribution of an M x K panel of A and a
+ * K x N panel of B to an M x N output tile, and the caller loops over K to
+ * accumulate the full product.  Each call here performs that whole K loop:
+ *
+ *     D[i][j] = C[i][j] + sum_{k < K} A[i][k] * B[k][j]
+ *
+ * with the input/accumulator pairs of the pages' builtin lists ("CDNA2 dense
+ * MFMA builtins", section "Builtin reference"; "RDNA3 dense WMMA builtins",
+ * section "Builtin reference", which defines every builtin's result as
+ * srcA x srcB + srcC):
+ *
+ *     dtype_in  dtype_acc   A, B element     C, D element
+ *     MMA_F16   MMA_F32     IEEE binary16    float
+ *     MMA_BF16  MMA_F32     bfloat16 bits    float
+ *     MMA_I8    MMA_I32     signed int8      int32_t  (exact; wraps mod 2^32)
+ *     MMA_F64   MMA_F64     double           double
+ *
+ * Any other pair returns MMA_ERR_UNSUPPORTED.
+ *
+ * Layouts (elements, not bytes; "RDNA3 dense WMMA builtins", section
+ * "Using WMMA builtins as a compute policy": A rows and B columns are read
+ * K-contiguous, the output is written row-major):
+ *   A  M x K row-major:     A[i][k] at A[i*lda + k],  lda >= K
+ *   B  column-major:        B[k][j] at B[j*ldb + k],  ldb >= K   (mma_gemm)
+ *      or row-major:        B[k][j] at B[k*ldb + j],  ldb >= N   (mma_gemm_ex)
+ *   C, D  M x N row-major:  C[i][j] at C[i*ldc + j],  ldc, ldd >= N
+ *
+ * Pointers and ownership: A, B, C and D are device pointers owned by the
+ * caller; the library keeps no reference to them after the call returns and
+ * allocates no memory per call.  C may be NULL (read as zero).  C may equal D
+ * (in place) only when ldc == ldd; any other overlap between D and an input
+ * is undefined.
+ *
+ * Alignment: every non-NULL base pointer must be 16-byte aligned and every
+ * leading dimension times the element size must be a multiple of 16 bytes
+ * (the tensor-memory-access engine's rule); otherwise MMA_ERR_MISALIGNED.
+ * M, N and K themselves are arbitrary (>= 0): ragged edges are handled
+ * inside the kernels.  M == 0 or N == 0 is a no-op; K == 0 gives D = C.
+ *
+ * Streams and errors: `stream` is a cudaStream_t (NULL = the legacy default
+ * stream).  Work is enqueued on it and the call returns without
+ * synchronising.  Argument errors are detected before anything is launched
+ * and reported by the return value; a failed launch returns MMA_ERR_LAUNCH.
+ * No C++ exception crosses this interface.  Every pipeline wait inside the
+ * kernels is bounded; a wait that runs out records MMA_ERR_TIMEOUT in a
+ * device-side status word that mma_device_status() reads back.  Calls on
+ * different streams may run concurrently; the library holds no per-call
+ * state.
+ */
+#ifndef MMA_GB300_H
+#define MMA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MMA_F16 = 1,
+  MMA_BF16 = 2,
+  MMA_I8 = 3,
+  MMA_F64 = 4,
+  MMA_F32 = 5,
+  MMA_I32 = 6
+} mma_dtype_t;
+
+typedef enum { MMA_COL_MAJOR = 0, MMA_ROW_MAJOR = 1 } mma_layout_t;
+
+typedef enum {
+  MMA_OK = 0,
+  MMA_ERR_INVALID_ARG = 1, /* negative size, short leading dimension, NULL
+                              operand, bad broadcast group/id            */
+  MMA_ERR_UNSUPPORTED = 2, /* dtype pair or batched shape not provided    */
+  MMA_ERR_MISALIGNED = 3,  /* pointer or leading dimension not 16 B       */
+  MMA_ERR_LAUNCH = 4,      /* CUDA reported an error at launch            */
+  MMA_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out            */
+  MMA_ERR_NO_DEVICE = 6    /* no usable sm_103 device is current          */
+} mma_status_t;
+
+/*
+ * mma_gemm -- D = A * B + C with column-major B.
+ *
+ * Passage: "CDNA2 dense MFMA builtins", sections "Naming convention" (the
+ * K-loop contract) and "Builtin reference" (FP16/BF16 -> FP32, INT8 ->
+ * INT32, FP64 -> FP64 with round-to-nearest-even); "RDNA3 dense WMMA
+ * builtins", section "Builtin reference" (srcA x srcB + srcC; signed int8).
+ *
+ * dtype_in, dtype_acc : one of the four pairs in the table above.
+ * M, N, K             : problem size, each >= 0.
+ * A, lda              : M x K row-major input, lda >= K.
+ * B, ldb              : K x N column-major input (stored as N rows of K
+ *                       contiguous elements), ldb >= K.
+ * C, ldc              : M x N row-major addend of type dtype_acc, or NULL.
+ * D, ldd              : M x N row-major output of type dtype_acc.
+ * stream              : cudaStream_t to enqueue on.
+ * Returns MMA_OK or an error code; see the header comment for each case.
+ */
+mma_status_t mma_gemm(int dtype_in, int dtype_acc, int64_t M, int64_t N,
+                      int64_t K, const void *A, int64_t lda, const void *B,
+                      int64_t ldb, const void *C, int64_t ldc, void *D,
+                      int64_t ldd, void *stream);
+
+/*
+ * mma_gemm_ex -- as mma_gemm, with the layout of B chosen by `layout_b`:
+ * MMA_COL_MAJOR (same as mma_gemm) or MMA_ROW_MAJOR (B[k][j] at
+ * B[k*ldb + j], ldb >= N).  Same passages as mma_gemm; the row-major form
+ * is the plain storage of a K x N matrix.
+ */
+mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M, int64_t N,
+                         int64_t K, const void *A, int64_t lda, const void *B,
+                         int64_t ldb, int layout_b, const void *C, int64_t ldc,
+                         void *D, int64_t ldd, void *stream);
+
+/*
+ * mma_gemm_batched -- `batch` independent M x N x K products with A-block
+ * broadcast:
+ *
+ *     for b in [0, batch):  D_b = A_{src(b)} * B_b + C_b,
+ *                           src(b) = (b / G) * G + a_broadcast_id
+ *
+ * Passage: "Common MFMA parameters", section "Shared parameters" (cbsz:
+ * one chosen input block of A is broadcast to the 2^cbsz - 1 neighbouring
+ * blocks of its group; abid: which block of each group is the source;
+ * worked example cbsz = 2, abid = 1: block 1's A goes to blocks 0, 2, 3 and
+ * block 5's to 4, 6, 7), and "CDNA2 dense MFMA builtins", section
+ * "Accumulator layout" (one instruction computes several independent
+ * blocks, each with its own A, B, C and D).  Here a batch entry plays the
+ * role of a block and G = a_broadcast_group = 2^cbsz.
+ *
+ * Storage: tiles are contiguous, tile b of A at A + b*M*lda, of B at
+ * B + b*N*ldb (column-major tiles), of C and D at b*M*ldc and b*M*ldd
+ * (elements).  A holds `batch` tiles; only tile src(b) is read for entry b.
+ * B, C and D are never broadcast.
+ * Constraints: a_broadcast_group in {1, 2, 4, 8, 16}; 0 <= a_broadcast_id
+ * < a_broadcast_group; batch % a_broadcast_group == 0 (else
+ * MMA_ERR_INVALID_ARG).  Provided shapes: M = N = K = 16 with
+ * (MMA_F16 | MMA_BF16, MMA_F32) and lda = ldb = ldc = ldd = 16; other
+ * shapes or pairs return MMA_ERR_UNSUPPORTED.
+ */
+mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc, int64_t M,
+                              int64_t N, int64_t K, const void *A, int64_t lda,
+                              const void *B, int64_t ldb, const void *C,
+                              int64_t ldc, void *D, int64_t ldd, int64_t batch,
+                              int a_broadcast_group, int a_broadcast_id,
+                              void *stream);
+
+/*
+ * mma_device_status -- synchronise `stream`, then read and clear the
+ * library's device-side status word on the current device.  Returns MMA_OK
+ * when no in-kernel wait has run out since the last call, MMA_ERR_TIMEOUT
+ * otherwise, or MMA_ERR_LAUNCH if the synchronisation itself failed.
+ * (The pages check errors after every launch: "RDNA3 dense WMMA builtins",
+ * section "Instantiating the kernel"; this is the matching device-side
+ * check.)
+ */
+mma_status_t mma_device_status(void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mma_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int mma_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MMA_GB300_H */

@@ -1,0 +1,210 @@
+"""Thin ctypes binding over the C ABI in ``include/mma_gb300.h``.
+
+Argument marshalling only: every step of D = A*B + C runs in the CUDA
+library ``libmma_gb300.so`` built in-tree from ``csrc/``.  PyTorch supplies
+device memory and the current stream.  If the library is missing, or no
+CUDA device is present, calls raise; nothing here computes on the CPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIBNAME = "libmma_gb300.so"
+
+MMA_F16, MMA_BF16, MMA_I8, MMA_F64, MMA_F32, MMA_I32 = 1, 2, 3, 4, 5, 6
+MMA_COL_MAJOR, MMA_ROW_MAJOR = 0, 1
+STATUS = {0: "MMA_OK", 1: "MMA_ERR_INVALID_ARG", 2: "MMA_ERR_UNSUPPORTED",
+          3: "MMA_ERR_MISALIGNED", 4: "MMA_ERR_LAUNCH", 5: "MMA_ERR_TIMEOUT",
+          6: "MMA_ERR_NO_DEVICE"}
+
+# The exported entry points and their ctypes signatures (kept in step with
+# include/mma_gb300.h; tests check both lists against the header).
+_p, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+SIGNATURES = {
+    "mma_gemm": (_int, [_int, _int, _i64, _i64, _i64, _p, _i64, _p, _i64, _p,
+                        _i64, _p, _i64, _p]),
+    "mma_gemm_ex": (_int, [_int, _int, _i64, _i64, _i64, _p, _i64, _p, _i64,
+                           _int, _p, _i64, _p, _i64, _p]),
+    "mma_gemm_batched": (_int, [_int, _int, _i64, _i64, _i64, _p, _i64, _p,
+                                _i64, _p, _i64, _p, _i64, _i64, _int, _int,
+                                _p]),
+    "mma_device_status": (_int, [_p]),
+    "mma_status_string": (ctypes.c_char_p, [_int]),
+    "mma_version": (_int, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MMAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIBNAME)
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{_LIBNAME} is not built (expected at {path}); run "
+                    "`python -m mixed_precision_dense_02_gb300.build`")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MMAError(fn, status)
+
+
+# --------------------------------------------------------------------------
+# raw-pointer entry points (same names as the C ABI)
+
+def mma_gemm(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C, ldc, D, ldd,
+             stream) -> int:
+    return load().mma_gemm(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C,
+                           ldc, D, ldd, stream)
+
+
+def mma_gemm_ex(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, layout_b, C,
+                ldc, D, ldd, stream) -> int:
+    return load().mma_gemm_ex(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb,
+                              layout_b, C, ldc, D, ldd, stream)
+
+
+def mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C, ldc, D,
+                     ldd, batch, group, abid, stream) -> int:
+    return load().mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B,
+                                   ldb, C, ldc, D, ldd, batch, group, abid,
+                                   stream)
+
+
+def mma_device_status(stream) -> int:
+    return load().mma_device_status(stream)
+
+
+def mma_status_string(status: int) -> str:
+    return load().mma_status_string(status).decode()
+
+
+# --------------------------------------------------------------------------
+# torch-tensor convenience layer (still marshalling only)
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtypes(t):
+    torch = _torch()
+    m = {torch.float16: (MMA_F16, MMA_F32, torch.float32),
+         torch.bfloat16: (MMA_BF16, MMA_F32, torch.float32),
+         torch.int8: (MMA_I8, MMA_I32, torch.int32),
+         torch.float64: (MMA_F64, MMA_F64, torch.float64)}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported input dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _ld(t) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("2-D tensors with unit inner stride are required")
+    return t.stride(0)
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def gemm_ex(A, B, C=None, D=None, *, b_layout: str = "col", stream=None):
+    """D = A @ B + C on the GPU.
+
+    ``A``: (M, K) row-major; ``B`` as stored: (N, K) for column-major B
+    (``b_layout="col"``) or (K, N) for row-major B; ``C``/``D``: (M, N).
+    Input dtype float16/bfloat16 -> float32 output, int8 -> int32,
+    float64 -> float64.  ``D`` is allocated when not given.  Returns D.
+    """
+    torch = _torch()
+    dt_in, dt_acc, out_dtype = _dtypes(A)
+    if B.dtype != A.dtype:
+        raise TypeError("A and B must have the same dtype")
+    M, K = A.shape
+    if b_layout == "col":
+        N, Kb = B.shape
+        layout = MMA_COL_MAJOR
+    elif b_layout == "row":
+        Kb, N = B.shape
+        layout = MMA_ROW_MAJOR
+    else:
+        raise ValueError(b_layout)
+    if Kb != K:
+        raise ValueError(f"K mismatch: {K} vs {Kb}")
+    if D is None:
+        D = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    for t in (C, D):
+        if t is not None and (t.dtype != out_dtype or tuple(t.shape) != (M, N)):
+            raise ValueError("C/D must be (M, N) of the accumulator dtype")
+    st = mma_gemm_ex(dt_in, dt_acc, M, N, K, A.data_ptr(), _ld(A),
+                     B.data_ptr(), _ld(B), layout,
+                     None if C is None else C.data_ptr(),
+                     0 if C is None else _ld(C), D.data_ptr(), _ld(D),
+                     _stream(stream))
+    _check("mma_gemm_ex", st)
+    return D
+
+
+def gemm(A, B, C=None, D=None, *, stream=None):
+    """D = A @ B + C with B given column-major as an (N, K) tensor."""
+    return gemm_ex(A, B, C, D, b_layout="col", stream=stream)
+
+
+def gemm_batched(A, B, C=None, D=None, *, group: int = 1, abid: int = 0,
+                 stream=None):
+    """Batched D_b = A_{(b//group)*group + abid} @ B_b + C_b.
+
+    ``A``: (batch, M, K); ``B``: (batch, N, K) column-major tiles;
+    ``C``/``D``: (batch, M, N); all contiguous.
+    """
+    torch = _torch()
+    dt_in, dt_acc, out_dtype = _dtypes(A)
+    batch, M, K = A.shape
+    _, N, Kb = B.shape
+    if Kb != K or B.shape[0] != batch:
+        raise ValueError("shape mismatch")
+    for t in (A, B, C, D):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("batched operands must be contiguous")
+    if D is None:
+        D = torch.empty((batch, M, N), dtype=out_dtype, device=A.device)
+    st = mma_gemm_batched(dt_in, dt_acc, M, N, K, A.data_ptr(), K,
+                          B.data_ptr(), K, None if C is None else C.data_ptr(),
+                          N, D.data_ptr(), N, batch, group, abid,
+                          _stream(stream))
+    _check("mma_gemm_batched", st)
+    return D
+
+
+def device_status(stream=None) -> None:
+    """Raise MMAError if an in-kernel wait has run out since the last check."""
+    _check("mma_device_status", mma_device_status(_stream(stream)))

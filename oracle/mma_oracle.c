@@ -1,0 +1,280 @@
+/*
+ * CPU oracle for the dense multiply-accumulate D = A*B + C.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * definition that the CUDA library is checked against.  It shares no code,
+ * header, table or helper with the CUDA path, and the product path never
+ * loads it: only the test suite, the smoke check and the bench's CPU-baseline
+ * leg call into it.
+ *
+ * What it follows (page title -- section):
+ *   - "CDNA2 dense MFMA builtins" -- Naming convention: one instruction adds
+ *     the contribution of an M x K panel of A and a K x N panel of B to an
+ *     M x N tile; the caller loops over K for the full product.  Here the
+ *     whole K loop is written out, so the result is the plain definition
+ *       D[i][j] = C[i][j] + sum_k A[i][k] * B[k][j].
+ *   - "CDNA2 dense MFMA builtins" -- Builtin reference: FP16/BF16 inputs
+ *     accumulate in FP32, INT8 inputs in INT32, FP64 in FP64 with
+ *     round-to-nearest-even.
+ *   - "RDNA3 dense WMMA builtins" -- Builtin reference: each builtin returns
+ *     srcA x srcB + srcC; INT8 inputs are signed (a_neg/b_neg select signed).
+ *   - "Common MFMA parameters" -- Shared parameters (cbsz, abid): with a
+ *     group of G = 2^cbsz neighbouring blocks, every block of the group uses
+ *     the A values of block abid of that group.
+ *
+ * Precision of the oracle itself:
+ *   - FP16/BF16 -> FP32: operands are decoded exactly to double; each product
+ *     is exact in double (at most 11 x 11 significant bits); the K products
+ *     are summed in double in sequential k order; C is added in double and
+ *     the sum is rounded once to FP32 (round to nearest even).
+ *   - INT8 -> INT32: exact 64-bit integer sum, plus C; results that do not
+ *     fit in INT32 are counted (overflow is never silent) and wrap in two's
+ *     complement.
+ *   - FP64: Ogita-Rump-Oishi compensated dot product "Dot2" (TwoProduct by
+ *     fma, TwoSum by Knuth), with C as one more term, so the oracle's error
+ *     is about eps^2 relative to sum |a*b| plus one final rounding.
+ *
+ * Build: plain C11, -O2 -fopenmp -ffp-contract=off (no contraction, no
+ * reassociation, no fast-math); only the loop over output rows is parallel.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* dtype codes, matching the numeric values of the public enum */
+enum { OR_F16 = 1, OR_BF16 = 2, OR_I8 = 3, OR_F64 = 4, OR_F32 = 5, OR_I32 = 6 };
+/* B layouts: column-major (B[k][j] at B[j*ldb + k]) or row-major */
+enum { OR_B_COL = 0, OR_B_ROW = 1 };
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ---- c1: exact decode of 16-bit float bit patterns -------------------- */
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double oracle_f16_to_double(uint16_t h) {
+  const int neg = (h >> 15) & 1;
+  const int e = (h >> 10) & 0x1f;
+  const int f = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -24); /* subnormal: f * 2^(1-15-10) */
+  else if (e == 31)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp((double)(f | 0x400), e - 25); /* (2^10 + f) * 2^(e-15-10) */
+  return neg ? -v : v;
+}
+
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits. */
+double oracle_bf16_to_double(uint16_t h) {
+  const int neg = (h >> 15) & 1;
+  const int e = (h >> 7) & 0xff;
+  const int f = h & 0x7f;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -133); /* subnormal: f * 2^(1-127-7) */
+  else if (e == 255)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp((double)(f | 0x80), e - 134); /* (2^7 + f) * 2^(e-127-7) */
+  return neg ? -v : v;
+}
+
+static double *decode_table(int kind) {
+  double *t = (double *)malloc(65536 * sizeof(double));
+  if (!t) return NULL;
+  for (int b = 0; b < 65536; ++b)
+    t[b] = kind == OR_F16 ? oracle_f16_to_double((uint16_t)b)
+                          : oracle_bf16_to_double((uint16_t)b);
+  return t;
+}
+
+static inline int64_t b_index(int b_layout, int64_t k, int64_t j, int64_t ldb) {
+  return b_layout == OR_B_COL ? j * ldb + k : k * ldb + j;
+}
+
+/* ---- c2: FP16/BF16 inputs, FP32 accumulate ---------------------------- *
+ * A: M x K row-major (A[i][k] at A[i*lda + k]); B per b_layout; C, D: M x N
+ * row-major.  C may be NULL (C = 0).  If absab is not NULL it receives
+ * (|A|*|B|)[i][j] in double (the scale of the parity tolerance).        */
+static void f16_row(const double *tab, int64_t i, int64_t N, int64_t K,
+                    const uint16_t *A, int64_t lda, const uint16_t *B,
+                    int64_t ldb, int b_layout, const float *C, int64_t ldc,
+                    float *D, int64_t ldd, double *absab, int64_t ldabs) {
+  for (int64_t j = 0; j < N; ++j) {
+    double s = 0.0, sa = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = tab[A[i * lda + k]];
+      const double b = tab[B[b_index(b_layout, k, j, ldb)]];
+      s += a * b;
+      if (absab) sa += fabs(a) * fabs(b);
+    }
+    const double c = C ? (double)C[i * ldc + j] : 0.0;
+    D[i * ldd + j] = (float)(s + c);
+    if (absab) absab[i * ldabs + j] = sa;
+  }
+}
+
+/* Returns 0, or -1 on bad arguments / allocation failure. */
+int oracle_gemm_f16f32(int in_kind, int64_t M, int64_t N, int64_t K,
+                       const uint16_t *A, int64_t lda, const uint16_t *B,
+                       int64_t ldb, int b_layout, const float *C, int64_t ldc,
+                       float *D, int64_t ldd, double *absab, int64_t ldabs) {
+  if (in_kind != OR_F16 && in_kind != OR_BF16) return -1;
+  if (M < 0 || N < 0 || K < 0) return -1;
+  double *tab = decode_table(in_kind);
+  if (!tab) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < M; ++i)
+    f16_row(tab, i, N, K, A, lda, B, ldb, b_layout, C, ldc, D, ldd, absab,
+            ldabs);
+  free(tab);
+  return 0;
+}
+
+/* ---- c3: INT8 inputs, INT32 accumulate -------------------------------- *
+ * Exact int64 sum.  Outputs that do not fit in INT32 wrap in two's
+ * complement and are counted.                                           */
+static int64_t i8_row(int64_t i, int64_t N, int64_t K, const int8_t *A,
+                      int64_t lda, const int8_t *B, int64_t ldb, int b_layout,
+                      const int32_t *C, int64_t ldc, int32_t *D, int64_t ldd) {
+  int64_t overflow = 0;
+  for (int64_t j = 0; j < N; ++j) {
+    int64_t s = 0;
+    for (int64_t k = 0; k < K; ++k)
+      s += (int64_t)A[i * lda + k] * (int64_t)B[b_index(b_layout, k, j, ldb)];
+    const int64_t d = s + (C ? (int64_t)C[i * ldc + j] : 0);
+    if (d < INT32_MIN || d > INT32_MAX) ++overflow;
+    D[i * ldd + j] = (int32_t)(uint32_t)(uint64_t)d;
+  }
+  return overflow;
+}
+
+/* Returns the number of outputs that overflowed INT32, or -1. */
+int64_t oracle_gemm_i8i32(int64_t M, int64_t N, int64_t K, const int8_t *A,
+                          int64_t lda, const int8_t *B, int64_t ldb,
+                          int b_layout, const int32_t *C, int64_t ldc,
+                          int32_t *D, int64_t ldd) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  int64_t overflow = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : overflow)
+  for (int64_t i = 0; i < M; ++i)
+    overflow += i8_row(i, N, K, A, lda, B, ldb, b_layout, C, ldc, D, ldd);
+  return overflow;
+}
+
+/* ---- c4: FP64, compensated dot product (Dot2) ------------------------- */
+
+/* Knuth's TwoSum: s + e == a + b exactly, s = fl(a + b). */
+static inline void two_sum(double a, double b, double *s, double *e) {
+  const double x = a + b;
+  const double z = x - a;
+  *e = (a - (x - z)) + (b - z);
+  *s = x;
+}
+
+/* TwoProduct with a fused multiply-add: p + e == a * b exactly. */
+static inline void two_prod(double a, double b, double *p, double *e) {
+  const double x = a * b;
+  *e = fma(a, b, -x);
+  *p = x;
+}
+
+static void f64_row(int64_t i, int64_t N, int64_t K, const double *A,
+                    int64_t lda, const double *B, int64_t ldb, int b_layout,
+                    const double *C, int64_t ldc, double *D, int64_t ldd,
+                    double *absab, int64_t ldabs) {
+  for (int64_t j = 0; j < N; ++j) {
+    double p = 0.0, s = 0.0, sa = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = A[i * lda + k];
+      const double b = B[b_index(b_layout, k, j, ldb)];
+      double h, r, q;
+      two_prod(a, b, &h, &r);
+      two_sum(p, h, &p, &q);
+      s += q + r;
+      if (absab) sa += fabs(a) * fabs(b);
+    }
+    if (C) {
+      double q;
+      two_sum(p, C[i * ldc + j], &p, &q);
+      s += q;
+    }
+    D[i * ldd + j] = p + s;
+    if (absab) absab[i * ldabs + j] = sa;
+  }
+}
+
+int oracle_gemm_f64(int64_t M, int64_t N, int64_t K, const double *A,
+                    int64_t lda, const double *B, int64_t ldb, int b_layout,
+                    const double *C, int64_t ldc, double *D, int64_t ldd,
+                    double *absab, int64_t ldabs) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < M; ++i)
+    f64_row(i, N, K, A, lda, B, ldb, b_layout, C, ldc, D, ldd, absab, ldabs);
+  return 0;
+}
+
+/* ---- c5: batched tiles with A-block broadcast ------------------------- *
+ * Tile b of each operand is stored contiguously: A tile t at A + t*M*lda,
+ * B tile b at B + b*N*ldb (column-major B) or B + b*K*ldb (row-major B),
+ * C and D tile b at b*M*ldc and b*M*ldd.  With a broadcast group of G
+ * entries and source index abid, entry b reads A tile
+ *     src(b) = (b / G) * G + abid,
+ * while B, C and D are never broadcast.  G is 1, 2, 4, 8 or 16, G must
+ * divide batch and 0 <= abid < G.  Returns 0 (or the INT8 overflow count), -1 on bad
+ * arguments.                                                            */
+int64_t oracle_gemm_batched(int dtype_in, int64_t M, int64_t N, int64_t K,
+                            const void *A, int64_t lda, const void *B,
+                            int64_t ldb, int b_layout, const void *C,
+                            int64_t ldc, void *D, int64_t ldd, int64_t batch,
+                            int64_t G, int64_t abid) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  /* G = 2^cbsz with cbsz in 0..4 ("Common MFMA parameters", cbsz row) */
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return -1;
+  if (batch < 0 || abid < 0 || abid >= G || batch % G != 0) return -1;
+  if (dtype_in != OR_F16 && dtype_in != OR_BF16 && dtype_in != OR_I8 &&
+      dtype_in != OR_F64)
+    return -1;
+  double *tab = NULL;
+  if (dtype_in == OR_F16 || dtype_in == OR_BF16) {
+    tab = decode_table(dtype_in);
+    if (!tab) return -1;
+  }
+  const int64_t b_tile = (b_layout == OR_B_COL ? N : K) * ldb;
+  int64_t overflow = 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(+ : overflow)
+  for (int64_t b = 0; b < batch; ++b) {
+    const int64_t src = (b / G) * G + abid;
+    for (int64_t i = 0; i < M; ++i) {
+      if (dtype_in == OR_I8)
+        overflow += i8_row(i, N, K, (const int8_t *)A + src * M * lda, lda,
+                           (const int8_t *)B + b * b_tile, ldb, b_layout,
+                           C ? (const int32_t *)C + b * M * ldc : NULL, ldc,
+                           (int32_t *)D + b * M * ldd, ldd);
+      else if (dtype_in == OR_F64)
+        f64_row(i, N, K, (const double *)A + src * M * lda, lda,
+                (const double *)B + b * b_tile, ldb, b_layout,
+                C ? (const double *)C + b * M * ldc : NULL, ldc,
+                (double *)D + b * M * ldd, ldd, NULL, 0);
+      else
+        f16_row(tab, i, N, K, (const uint16_t *)A + src * M * lda, lda,
+                (const uint16_t *)B + b * b_tile, ldb, b_layout,
+                C ? (const float *)C + b * M * ldc : NULL, ldc,
+                (float *)D + b * M * ldd, ldd, NULL, 0);
+    }
+  }
+  free(tab);
+  return overflow;
+}

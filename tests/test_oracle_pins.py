@@ -1,0 +1,368 @@
+"""Pins of the CPU oracle to facts fixed outside itself.
+
+Each test checks the oracle against something other than its own code:
+exact rational arithmetic (Python ``fractions``/ints) on small inputs, closed
+forms (identity, all-ones), invariants (transpose), library conversions of
+the 16-bit formats, and the worked broadcast example printed on the page
+"Common MFMA parameters" (section "Shared parameters").  A dropped term,
+wrong sign, swapped index or transposed operand in the oracle fails at
+least one of them.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from mixed_precision_dense_02_gb300 import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ---------------------------------------------------------------- helpers
+
+def frac_of_f16(bits):
+    return Fraction(float(np.uint16(bits).view(np.float16)))
+
+
+def frac_of_bf16(bits):
+    return Fraction(float(np.array([np.uint32(bits) << np.uint32(16)],
+                                   np.uint32).view(np.float32)[0]))
+
+
+def round_fraction_f32(q: Fraction) -> np.float32:
+    """Round an exact rational to float32, nearest with ties to even."""
+    if q == 0:
+        return np.float32(0.0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length() - 24
+    while a / Fraction(2) ** e >= 2 ** 24:
+        e += 1
+    while a / Fraction(2) ** e < 2 ** 23:
+        e -= 1
+    e = max(e, -149)
+    scaled = a / Fraction(2) ** e
+    m = math.floor(scaled)
+    rem = scaled - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    return np.float32(sign * float(m * Fraction(2) ** e))
+
+
+def exact_gemm(A, Bcol, C, dec):
+    """Exact rational D = A*B + C, B given column-major (N x K)."""
+    M, K = A.shape
+    N = Bcol.shape[0]
+    out = [[None] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = Fraction(0)
+            for k in range(K):
+                s += dec(A[i, k]) * dec(Bcol[j, k])
+            out[i][j] = s + (Fraction(float(C[i, j])) if C is not None else 0)
+    return out
+
+
+def f16_grid(rng, shape, dtype_in):
+    """Values on the 2^-10 grid in [-1, 1): sums stay exact in double."""
+    v = rng.integers(-1024, 1024, size=shape) / 1024.0
+    return (synth.round_f16_bits(v) if dtype_in == "f16"
+            else synth.round_bf16_bits(np.round(v * 128) / 128))
+
+
+# ------------------------------------------------------ c1 decode pins
+
+def test_f16_decode_matches_numpy_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle_mod.f16_to_double(int(b)) for b in bits])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_bf16_decode_matches_float32_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (bits << np.uint32(16)).view(np.float32).astype(np.float64)
+    got = np.array([oracle_mod.bf16_to_double(int(b)) for b in bits])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+# ------------------------------------------- c2 FP16/BF16 -> FP32 pins
+
+SMALL = [(1, 1, 1), (2, 3, 5), (3, 2, 1), (5, 5, 16), (16, 17, 3),
+         (17, 16, 17), (1, 17, 16)]
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_f16_exact_bruteforce_on_grid(oracle_mod, dtype_in, M, N, K):
+    """On grid inputs the double sum is exact, so the oracle must equal the
+    exact rational result rounded once to FP32."""
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    A = f16_grid(rng, (M, K), dtype_in)
+    B = f16_grid(rng, (N, K), dtype_in)
+    C = rng.standard_normal((M, N)).astype(np.float32)
+    D = oracle_mod.gemm(dtype_in, A, B, C)
+    dec = frac_of_f16 if dtype_in == "f16" else frac_of_bf16
+    ex = exact_gemm(A, B, C, dec)
+    want = np.array([[round_fraction_f32(q) for q in row] for row in ex],
+                    np.float32)
+    assert np.array_equal(D.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+def test_f16_bruteforce_general_inputs_within_one_rounding(oracle_mod, dtype_in):
+    """Any fp16/bf16 inputs (subnormals included): at most one FP32 rounding
+    away from the exact value (plus a double-precision term)."""
+    rng = np.random.default_rng(7)
+    M, N, K = 6, 5, 17
+    rnd = synth.round_f16_bits if dtype_in == "f16" else synth.round_bf16_bits
+    A = rnd(rng.standard_normal((M, K)) * np.exp2(rng.integers(-20, 5, (M, K))))
+    B = rnd(rng.standard_normal((N, K)) * np.exp2(rng.integers(-20, 5, (N, K))))
+    C = rng.standard_normal((M, N)).astype(np.float32)
+    D = oracle_mod.gemm(dtype_in, A, B, C)
+    dec = frac_of_f16 if dtype_in == "f16" else frac_of_bf16
+    ex = exact_gemm(A, B, C, dec)
+    for i in range(M):
+        for j in range(N):
+            q = ex[i][j]
+            err = abs(Fraction(float(D[i, j])) - q)
+            assert err <= abs(q) * Fraction(1, 2 ** 24) + Fraction(1, 2 ** 60)
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+def test_f16_all_ones_closed_form(oracle_mod, dtype_in):
+    M, N, K = 7, 9, 300
+    one = 0x3C00 if dtype_in == "f16" else 0x3F80
+    A = np.full((M, K), one, np.uint16)
+    B = np.full((N, K), one, np.uint16)
+    C = np.random.default_rng(0).standard_normal((M, N)).astype(np.float32)
+    D = oracle_mod.gemm(dtype_in, A, B, C)
+    want = (np.float64(K) + C.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(D, want)
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+def test_f16_identity_closed_forms(oracle_mod, dtype_in):
+    """B = I gives D = A + C; A = I gives D = B + C (B read as K x N)."""
+    rng = np.random.default_rng(1)
+    n = 24
+    rnd = synth.round_f16_bits if dtype_in == "f16" else synth.round_bf16_bits
+    to32 = synth.f16_bits_to_f32 if dtype_in == "f16" else synth.bf16_bits_to_f32
+    one = 0x3C00 if dtype_in == "f16" else 0x3F80
+    eye = np.where(np.eye(n, dtype=bool), one, 0).astype(np.uint16)
+    X = rnd(rng.uniform(-1, 1, (n, n)))          # not symmetric
+    C = rng.standard_normal((n, n)).astype(np.float32)
+    # B = I (column-major storage of I is I)
+    D = oracle_mod.gemm(dtype_in, X, eye, C)
+    assert np.array_equal(D, (to32(X).astype(np.float64) + C).astype(np.float32))
+    # A = I, B column-major stored as X (N x K): B[k][j] = X[j][k]
+    D2 = oracle_mod.gemm(dtype_in, eye, X, C)
+    assert np.array_equal(D2, (to32(X).T.astype(np.float64) + C).astype(np.float32))
+    # A = I, B row-major stored as X (K x N): B[k][j] = X[k][j]
+    D3 = oracle_mod.gemm(dtype_in, eye, X, C, b_layout="row")
+    assert np.array_equal(D3, (to32(X).astype(np.float64) + C).astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8", "f64"])
+def test_transpose_invariance(oracle_mod, dtype_in):
+    """(A*B + C)^T == B^T * A^T + C^T.  With A row-major and B column-major,
+    the operand buffers swap roles unchanged, so the oracle must agree with
+    itself bit for bit (it sums in the same k order)."""
+    M, N, K = 13, 21, 37
+    g = synth.gemm_inputs("transpose_pin", dtype_in, M, N, K, dist="uniform")
+    D = oracle_mod.gemm(dtype_in, g.A, g.B, g.C)
+    DT = oracle_mod.gemm(dtype_in, g.B, g.A, np.ascontiguousarray(g.C.T))
+    assert np.array_equal(D.T, DT)
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8", "f64"])
+def test_layout_and_padding_invariance(oracle_mod, dtype_in):
+    """Row-major B == column-major B transposed; padded leading dimensions
+    (garbage in the padding) do not change the result; C=None == C=0."""
+    M, N, K = 9, 11, 19
+    g = synth.gemm_inputs("layout_pin", dtype_in, M, N, K, dist="uniform")
+    D = oracle_mod.gemm(dtype_in, g.A, g.B, g.C)
+    Brow = np.ascontiguousarray(g.B.T)
+    assert np.array_equal(D, oracle_mod.gemm(dtype_in, g.A, Brow, g.C, b_layout="row"))
+
+    def pad(x, extra):
+        big = np.empty((x.shape[0], x.shape[1] + extra), x.dtype)
+        big.view(np.uint8)[:] = 0xA5
+        big[:, : x.shape[1]] = x
+        return big[:, : x.shape[1]]
+
+    Dp = oracle_mod.gemm(dtype_in, pad(g.A, 7), pad(g.B, 3), pad(g.C, 5))
+    assert np.array_equal(D, Dp)
+    Z = np.zeros_like(g.C)
+    assert np.array_equal(oracle_mod.gemm(dtype_in, g.A, g.B, None),
+                          oracle_mod.gemm(dtype_in, g.A, g.B, Z))
+
+
+def test_absab_is_sum_of_absolute_products(oracle_mod):
+    rng = np.random.default_rng(3)
+    A = synth.round_bf16_bits(rng.standard_normal((4, 9)))
+    B = synth.round_bf16_bits(rng.standard_normal((5, 9)))
+    _, ab = oracle_mod.gemm("bf16", A, B, None, want_absab=True)
+    a = synth.bf16_bits_to_f32(A).astype(np.float64)
+    b = synth.bf16_bits_to_f32(B).astype(np.float64)
+    for i in range(4):
+        for j in range(5):
+            ex = sum(Fraction(abs(a[i, k])) * Fraction(abs(b[j, k])) for k in range(9))
+            assert abs(Fraction(ab[i, j]) - ex) <= ex * Fraction(1, 2 ** 50)
+
+
+# ----------------------------------------------------- c3 INT8 pins
+
+@pytest.mark.parametrize("M,N,K", SMALL + [(8, 8, 64)])
+def test_i8_exact_bruteforce(oracle_mod, M, N, K):
+    g = synth.gemm_inputs(f"i8_pin_{M}_{N}_{K}", "i8", M, N, K)
+    D = oracle_mod.gemm("i8", g.A, g.B, g.C)
+    for i in range(M):
+        for j in range(N):
+            s = sum(int(g.A[i, k]) * int(g.B[j, k]) for k in range(K)) + int(g.C[i, j])
+            assert int(D[i, j]) == s
+
+
+def test_i8_closed_forms(oracle_mod):
+    M, N, K = 5, 6, 4096
+    C = synth.int_uniform(0, 99, M * N, -(1 << 20), 1 << 20).astype(np.int32).reshape(M, N)
+    ones = np.ones((M, K), np.int8)
+    D = oracle_mod.gemm("i8", ones, np.ones((N, K), np.int8), C)
+    assert np.array_equal(D, K + C)
+    # the largest product magnitude everywhere: (-128) * (-128) = 2^14
+    neg = np.full((M, K), -128, np.int8)
+    D = oracle_mod.gemm("i8", neg, np.full((N, K), -128, np.int8), C)
+    assert np.array_equal(D.astype(np.int64), K * 16384 + C.astype(np.int64))
+    # mixed signs: (-128) * 127
+    D = oracle_mod.gemm("i8", neg, np.full((N, K), 127, np.int8), C)
+    assert np.array_equal(D.astype(np.int64), -K * 16256 + C.astype(np.int64))
+
+
+def test_i8_overflow_is_reported(oracle_mod):
+    K = 1 << 17  # 2^17 * 2^14 = 2^31 does not fit in int32
+    A = np.full((1, K), -128, np.int8)
+    B = np.full((1, K), -128, np.int8)
+    with pytest.raises(OverflowError):
+        oracle_mod.gemm("i8", A, B, None)
+
+
+# ----------------------------------------------------- c4 FP64 pins
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_f64_bruteforce_one_rounding(oracle_mod, M, N, K):
+    """Dot2 plus C: within one rounding of the exact rational result, up to
+    an eps^2-sized term (Ogita, Rump, Oishi 2005, Prop. 5.5)."""
+    g = synth.gemm_inputs(f"f64_pin_{M}_{N}_{K}", "f64", M, N, K)
+    D = oracle_mod.gemm("f64", g.A, g.B, g.C)
+    for i in range(M):
+        for j in range(N):
+            q = sum(Fraction(g.A[i, k]) * Fraction(g.B[j, k]) for k in range(K))
+            sab = sum(abs(Fraction(g.A[i, k]) * Fraction(g.B[j, k])) for k in range(K))
+            q += Fraction(g.C[i, j])
+            err = abs(Fraction(D[i, j]) - q)
+            assert err <= abs(q) * Fraction(1, 2 ** 53) + sab * Fraction(1, 2 ** 90)
+
+
+def test_f64_compensation_recovers_cancelled_terms(oracle_mod):
+    """Naive summation loses the small terms here; the exact answer is 2.5."""
+    A = np.array([[1e16, 1.0, -1e16, 1.5, 3e20, -3e20]])
+    B = np.ones((1, 6))
+    assert oracle_mod.gemm("f64", A, B, None)[0, 0] == 2.5
+    # the product error term: (1 + 2^-30)^2 = 1 + 2^-29 + 2^-60, minus 1 + 2^-29
+    a = 1.0 + 2.0 ** -30
+    A = np.array([[a, -1.0, -(2.0 ** -29)]])
+    B = np.array([[a, 1.0, 1.0]])
+    assert oracle_mod.gemm("f64", A, B, None)[0, 0] == 2.0 ** -60
+
+
+def test_f64_closed_forms(oracle_mod):
+    n = 32
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((n, n))
+    C = rng.standard_normal((n, n))
+    I = np.eye(n)
+    assert np.array_equal(oracle_mod.gemm("f64", X, I, C), X + C)
+    assert np.array_equal(oracle_mod.gemm("f64", I, X, C, b_layout="row"), X + C)
+    D = oracle_mod.gemm("f64", np.ones((3, 1000)), np.ones((4, 1000)), C[:3, :4].copy())
+    assert np.array_equal(D, 1000.0 + C[:3, :4])
+
+
+# ------------------------------------------------- c5 broadcast pins
+
+def _golden_broadcast():
+    rows = []
+    with open(os.path.join(HERE, "golden", "broadcast_worked_example.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if line:
+                rows.append(line)
+    return rows
+
+
+def _tagged_tiles(batch, n=16):
+    """A tile t = (t+1) * I (exact in bf16 for t < 256), B_b = I, C = 0:
+    D_b = (src(b) + 1) * I, so the source index is read off D."""
+    one = 0x3F80
+    A = np.zeros((batch, n, n), np.uint16)
+    for t in range(batch):
+        A[t] = np.where(np.eye(n, dtype=bool),
+                        synth.round_bf16_bits(np.array([t + 1.0]))[0], 0)
+    B = np.broadcast_to(np.where(np.eye(n, dtype=bool), one, 0).astype(np.uint16),
+                        (batch, n, n)).copy()
+    C = np.zeros((batch, n, n), np.float32)
+    return A, B, C
+
+
+def test_broadcast_worked_example(oracle_mod):
+    rows = _golden_broadcast()
+    assert rows, "golden fixture is empty"
+    batch = 16
+    A, B, C = _tagged_tiles(batch)
+    for r in rows:
+        if r[0] == "src":
+            G, abid, block, source = map(int, r[1:])
+            D = oracle_mod.gemm_batched("bf16", A, B, C, group=G, abid=abid)
+            assert D[block, 0, 0] == source + 1
+            assert D[block, 3, 3] == source + 1 and D[block, 0, 1] == 0
+        elif r[0] == "same":
+            G = int(r[1])
+            blocks = list(map(int, r[2:]))
+            for abid in range(G):
+                D = oracle_mod.gemm_batched("bf16", A, B, C, group=G, abid=abid)
+                for b in blocks[1:]:
+                    assert np.array_equal(D[b], D[blocks[0]])
+                # and a different group sees different A
+                other = (blocks[0] + G) % batch
+                assert not np.array_equal(D[other], D[blocks[0]])
+
+
+@pytest.mark.parametrize("G,abid", [(1, 0), (2, 1), (4, 1), (4, 3), (8, 0), (16, 15)])
+def test_broadcast_equals_replicated_a(oracle_mod, G, abid):
+    batch = 32
+    bi = synth.batched_inputs("bcast_pin", "bf16", batch, group=G, abid=abid)
+    D = oracle_mod.gemm_batched("bf16", bi.A, bi.B, bi.C, group=G, abid=abid)
+    src = (np.arange(batch) // G) * G + abid
+    Arep = np.ascontiguousarray(bi.A[src])
+    D1 = oracle_mod.gemm_batched("bf16", Arep, bi.B, bi.C, group=1, abid=0)
+    assert np.array_equal(D, D1)
+    # G = 1 is a plain batch of independent products
+    for b in (0, batch - 1):
+        assert np.array_equal(D1[b], oracle_mod.gemm("bf16", Arep[b], bi.B[b], bi.C[b]))
+
+
+@pytest.mark.parametrize("G,abid,batch", [(4, 4, 8), (4, -1, 8), (3, 0, 9), (4, 0, 6), (0, 0, 4)])
+def test_broadcast_rejects_bad_groups(oracle_mod, G, abid, batch):
+    A = np.zeros((batch, 16, 16), np.uint16)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_batched("bf16", A, A.copy(), None, group=G, abid=abid)
