@@ -1,0 +1,259 @@
+// C ABI of the library (declared in include/mma_gb300.h): argument
+// validation, per-device set-up and dispatch to the kernels.  Nothing here
+// computes any part of D = A * B + C; every arithmetic step runs on the GPU.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+namespace mmagb {
+
+// Device-side status word: bounded pipeline waits OR their error bits in.
+__device__ unsigned g_mma_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool usable = false;
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Per-device set-up, once, with that device current: SM count, the
+// architecture check and the device address of the status word.
+const DeviceInfo* device_info(int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    d.ready = true;
+    int major = 0, minor = 0, sms = 0;
+    void* p = nullptr;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor,
+                               dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor,
+                               dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
+            cudaSuccess &&
+        major == 10 && minor == 3 &&
+        cudaGetSymbolAddress(&p, g_mma_status) == cudaSuccess) {
+      d.usable = true;
+      d.num_sms = sms;
+      d.status = static_cast<unsigned*>(p);
+    } else {
+      cudaGetLastError();
+    }
+  }
+  return d.usable ? &d : nullptr;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool ld_ok(int64_t ld, int64_t elem) { return ((ld * elem) & 15) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+__global__ void copy_c_kernel(const uint8_t* __restrict__ C, int64_t ldc_b,
+                              uint8_t* __restrict__ D, int64_t ldd_b,
+                              int64_t M, int64_t N, int elem) {
+  const int64_t total = M * N;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N, c = i % N;
+    if (elem == 8) {
+      const uint64_t v =
+          C ? *reinterpret_cast<const uint64_t*>(C + r * ldc_b + c * 8) : 0ull;
+      *reinterpret_cast<uint64_t*>(D + r * ldd_b + c * 8) = v;
+    } else {
+      const uint32_t v =
+          C ? *reinterpret_cast<const uint32_t*>(C + r * ldc_b + c * 4) : 0u;
+      *reinterpret_cast<uint32_t*>(D + r * ldd_b + c * 4) = v;
+    }
+  }
+}
+
+}  // namespace
+
+mma_status_t launch_copy_c(const Ctx& ctx, int64_t M, int64_t N,
+                           int elem_bytes, const void* C, int64_t ldc, void* D,
+                           int64_t ldd) {
+  int64_t blocks = (M * N + 255) / 256;
+  if (blocks > int64_t(ctx.num_sms) * 16) blocks = int64_t(ctx.num_sms) * 16;
+  copy_c_kernel<<<int(blocks), 256, 0, ctx.stream>>>(
+      static_cast<const uint8_t*>(C), ldc * elem_bytes,
+      static_cast<uint8_t*>(D), ldd * elem_bytes, M, N, elem_bytes);
+  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}
+
+}  // namespace mmagb
+
+using namespace mmagb;
+
+namespace {
+
+// Element sizes of a supported (dtype_in, dtype_acc) pair, or false.
+bool pair_sizes(int in, int acc, int64_t* in_b, int64_t* acc_b) {
+  if ((in == MMA_F16 || in == MMA_BF16) && acc == MMA_F32) {
+    *in_b = 2;
+    *acc_b = 4;
+    return true;
+  }
+  if (in == MMA_I8 && acc == MMA_I32) {
+    *in_b = 1;
+    *acc_b = 4;
+    return true;
+  }
+  if (in == MMA_F64 && acc == MMA_F64) {
+    *in_b = 8;
+    *acc_b = 8;
+    return true;
+  }
+  return false;
+}
+
+}  // namespace
+
+extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
+                                    int64_t N, int64_t K, const void* A,
+                                    int64_t lda, const void* B, int64_t ldb,
+                                    int layout_b, const void* C, int64_t ldc,
+                                    void* D, int64_t ldd, void* stream) {
+  int64_t eb = 0, ea = 0;
+  if (!pair_sizes(dtype_in, dtype_acc, &eb, &ea)) return MMA_ERR_UNSUPPORTED;
+  if (layout_b != MMA_COL_MAJOR && layout_b != MMA_ROW_MAJOR)
+    return MMA_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MMA_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MMA_OK;
+  const bool b_row = layout_b == MMA_ROW_MAJOR;
+  if (D == nullptr || ldd < N) return MMA_ERR_INVALID_ARG;
+  if (C != nullptr && ldc < N) return MMA_ERR_INVALID_ARG;
+  if (C != nullptr && C == D && ldc != ldd) return MMA_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (A == nullptr || B == nullptr) return MMA_ERR_INVALID_ARG;
+    if (lda < K || ldb < (b_row ? N : K)) return MMA_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !ld_ok(lda, eb) || !ld_ok(ldb, eb))
+      return MMA_ERR_MISALIGNED;
+  }
+  if (!aligned16(D) || !ld_ok(ldd, ea)) return MMA_ERR_MISALIGNED;
+  if (C != nullptr && (!aligned16(C) || !ld_ok(ldc, ea)))
+    return MMA_ERR_MISALIGNED;
+  if (b_row && dtype_in != MMA_F64) return MMA_ERR_UNSUPPORTED;
+
+  int dev = -1;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info) return MMA_ERR_NO_DEVICE;
+  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+
+  if (K == 0) return launch_copy_c(ctx, M, N, int(ea), C, ldc, D, ldd);
+  switch (dtype_in) {
+    case MMA_F16:
+    case MMA_BF16:
+      return launch_gemm_tc_f16(ctx, dtype_in == MMA_BF16, M, N, K, A, lda, B,
+                                ldb, static_cast<const float*>(C), ldc,
+                                static_cast<float*>(D), ldd);
+    case MMA_I8:
+      return launch_gemm_i8_imma(ctx, M, N, K, static_cast<const int8_t*>(A),
+                                 lda, static_cast<const int8_t*>(B), ldb,
+                                 static_cast<const int32_t*>(C), ldc,
+                                 static_cast<int32_t*>(D), ldd);
+    case MMA_F64:
+      return launch_gemm_f64(ctx, M, N, K, static_cast<const double*>(A), lda,
+                             static_cast<const double*>(B), ldb, b_row,
+                             static_cast<const double*>(C), ldc,
+                             static_cast<double*>(D), ldd);
+    default:
+      return MMA_ERR_UNSUPPORTED;
+  }
+}
+
+extern "C" mma_status_t mma_gemm(int dtype_in, int dtype_acc, int64_t M,
+                                 int64_t N, int64_t K, const void* A,
+                                 int64_t lda, const void* B, int64_t ldb,
+                                 const void* C, int64_t ldc, void* D,
+                                 int64_t ldd, void* stream) {
+  return mma_gemm_ex(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb,
+                     MMA_COL_MAJOR, C, ldc, D, ldd, stream);
+}
+
+extern "C" mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc,
+                                         int64_t M, int64_t N, int64_t K,
+                                         const void* A, int64_t lda,
+                                         const void* B, int64_t ldb,
+                                         const void* C, int64_t ldc, void* D,
+                                         int64_t ldd, int64_t batch,
+                                         int a_broadcast_group,
+                                         int a_broadcast_id, void* stream) {
+  int64_t eb = 0, ea = 0;
+  if (!pair_sizes(dtype_in, dtype_acc, &eb, &ea)) return MMA_ERR_UNSUPPORTED;
+  const int G = a_broadcast_group;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return MMA_ERR_INVALID_ARG;
+  if (a_broadcast_id < 0 || a_broadcast_id >= G) return MMA_ERR_INVALID_ARG;
+  if (batch < 0 || M < 0 || N < 0 || K < 0) return MMA_ERR_INVALID_ARG;
+  if (batch % G != 0) return MMA_ERR_INVALID_ARG;
+  if (!(M == 16 && N == 16 && K == 16)) return MMA_ERR_UNSUPPORTED;
+  if (dtype_in != MMA_F16 && dtype_in != MMA_BF16) return MMA_ERR_UNSUPPORTED;
+  if (lda != 16 || ldb != 16 || ldd != 16 || (C != nullptr && ldc != 16))
+    return MMA_ERR_UNSUPPORTED;
+  if (batch == 0) return MMA_OK;
+  if (A == nullptr || B == nullptr || D == nullptr) return MMA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) ||
+      (C != nullptr && !aligned16(C)))
+    return MMA_ERR_MISALIGNED;
+  int dev = -1;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info) return MMA_ERR_NO_DEVICE;
+  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  return launch_batched16(ctx, dtype_in == MMA_BF16, batch, G, a_broadcast_id,
+                          A, B, static_cast<const float*>(C),
+                          static_cast<float*>(D));
+}
+
+extern "C" mma_status_t mma_device_status(void* stream) {
+  int dev = -1;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info) return MMA_ERR_NO_DEVICE;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MMA_ERR_LAUNCH;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mma_status, sizeof(v)) != cudaSuccess)
+    return MMA_ERR_LAUNCH;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_mma_status, &zero, sizeof(zero)) != cudaSuccess)
+      return MMA_ERR_LAUNCH;
+    return MMA_ERR_TIMEOUT;
+  }
+  return MMA_OK;
+}
+
+extern "C" const char* mma_status_string(int status) {
+  switch (status) {
+    case MMA_OK: return "MMA_OK";
+    case MMA_ERR_INVALID_ARG: return "MMA_ERR_INVALID_ARG";
+    case MMA_ERR_UNSUPPORTED: return "MMA_ERR_UNSUPPORTED";
+    case MMA_ERR_MISALIGNED: return "MMA_ERR_MISALIGNED";
+    case MMA_ERR_LAUNCH: return "MMA_ERR_LAUNCH";
+    case MMA_ERR_TIMEOUT: return "MMA_ERR_TIMEOUT";
+    case MMA_ERR_NO_DEVICE: return "MMA_ERR_NO_DEVICE";
+    default: return "MMA_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int mma_version(void) { return 100; }

@@ -1,0 +1,141 @@
+// FP64 GEMM on the double-precision tensor path (mma.sync m8n8k4 DMMA):
+//   D = A * B + C, all FP64, A row-major, B column- or row-major.
+//
+// Page "CDNA2 dense MFMA builtins", section "Builtin reference", FP64-
+// accumulate builtins: FP64 inputs accumulate in FP64 with IEEE round-to-
+// nearest-even (no round-toward-zero partial products).  DMMA accumulates
+// each product with a fused multiply-add in FP64, which satisfies that.
+//
+// Block tile 64 x 64, K step 16, four warps each owning a 32 x 32 sub-tile
+// (4 x 4 fragments of 8 x 8).  Operand tiles are staged through shared
+// memory with register double buffering: the next K panel is fetched from
+// global memory while the current one feeds the DMMAs.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mmagb {
+namespace {
+
+constexpr int TM = 64, TN = 64, TK = 16;
+constexpr int kThreads = 128;
+constexpr int LDS = TK + 4;  // padded row (doubles) of the shared tiles
+
+template <bool B_ROW>
+__global__ void __launch_bounds__(kThreads)
+    gemm_f64_kernel(const double* __restrict__ A, int64_t lda,
+                    const double* __restrict__ B, int64_t ldb,
+                    const double* __restrict__ C, int64_t ldc,
+                    double* __restrict__ D, int64_t ldd, int M, int N, int K) {
+  __shared__ double As[TM * LDS];
+  __shared__ double Bs[TN * LDS];  // Bs[n][k]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int wm = (warp >> 1) * 32, wn = (warp & 1) * 32;
+  const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
+
+  double acc[4][4][2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = 0.0;
+
+  // Each thread fetches 8 elements of each operand tile per K panel.
+  double ra[8], rb[8];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // A: 64 rows x 16 k; thread covers row tid/2, k (tid%2)*8 + i
+      const int r = tid >> 1, k = (tid & 1) * 8 + i;
+      const int gm = m0 + r, gk = k0 + k;
+      ra[i] = (gm < M && gk < K) ? __ldg(A + int64_t(gm) * lda + gk) : 0.0;
+    }
+    if constexpr (!B_ROW) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int n = tid >> 1, k = (tid & 1) * 8 + i;
+        const int gn = n0 + n, gk = k0 + k;
+        rb[i] = (gn < N && gk < K) ? __ldg(B + int64_t(gn) * ldb + gk) : 0.0;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        // row-major B: 16 k-rows of 64 n; thread covers n = tid%64,
+        // k = (tid/64)*8 + i (coalesced along n)
+        const int n = tid & 63, k = (tid >> 6) * 8 + i;
+        const int gn = n0 + n, gk = k0 + k;
+        rb[i] = (gn < N && gk < K) ? __ldg(B + int64_t(gk) * ldb + gn) : 0.0;
+      }
+    }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      As[(tid >> 1) * LDS + (tid & 1) * 8 + i] = ra[i];
+      if constexpr (!B_ROW)
+        Bs[(tid >> 1) * LDS + (tid & 1) * 8 + i] = rb[i];
+      else
+        Bs[(tid & 63) * LDS + (tid >> 6) * 8 + i] = rb[i];
+    }
+  };
+
+  const int num_k = (K + TK - 1) / TK;
+  if (num_k > 0) fetch(0);
+  for (int kt = 0; kt < num_k; ++kt) {
+    __syncthreads();
+    stash();
+    __syncthreads();
+    if (kt + 1 < num_k) fetch((kt + 1) * TK);
+#pragma unroll
+    for (int kk = 0; kk < TK; kk += 4) {
+      double af[4], bfr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) af[i] = As[(wm + i * 8 + g) * LDS + kk + t];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bfr[j] = Bs[(wn + j * 8 + g) * LDS + kk + t];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_f64_884(acc[i][j], af[i], bfr[j]);
+    }
+  }
+
+  // fragment (i, j): rows wm + 8i + g, columns wn + 8j + 2t, +1
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = m0 + wm + i * 8 + g;
+    if (r >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = n0 + wn + j * 8 + 2 * t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (c + h < N) {
+          const double cv = C ? C[int64_t(r) * ldc + c + h] : 0.0;
+          D[int64_t(r) * ldd + c + h] = acc[i][j][h] + cv;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+mma_status_t launch_gemm_f64(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
+                             const double* A, int64_t lda, const double* B,
+                             int64_t ldb, bool b_row_major, const double* C,
+                             int64_t ldc, double* D, int64_t ldd) {
+  const int64_t gx = (N + TN - 1) / TN, gy = (M + TM - 1) / TM;
+  if (gy > 65535) return MMA_ERR_UNSUPPORTED;
+  const dim3 grid{unsigned(gx), unsigned(gy), 1u};
+  if (b_row_major)
+    gemm_f64_kernel<true><<<grid, kThreads, 0, ctx.stream>>>(
+        A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K));
+  else
+    gemm_f64_kernel<false><<<grid, kThreads, 0, ctx.stream>>>(
+        A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K));
+  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}
+
+}  // namespace mmagb

@@ -1,0 +1,49 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+// Arguments arrive here already validated (sizes, pointers, alignment).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mma_gb300.h"
+
+namespace mmagb {
+
+struct Ctx {
+  cudaStream_t stream;
+  int device;
+  int num_sms;
+  unsigned* status;  // device status word (bounded-wait timeouts)
+};
+
+// tcgen05 GEMM, FP16/BF16 inputs, FP32 accumulate, column-major B.
+mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, int64_t M,
+                                int64_t N, int64_t K, const void* A,
+                                int64_t lda, const void* B, int64_t ldb,
+                                const float* C, int64_t ldc, float* D,
+                                int64_t ldd);
+
+// INT8 GEMM on the warp-level IMMA pipe, column-major B.
+mma_status_t launch_gemm_i8_imma(const Ctx& ctx, int64_t M, int64_t N,
+                                 int64_t K, const int8_t* A, int64_t lda,
+                                 const int8_t* B, int64_t ldb,
+                                 const int32_t* C, int64_t ldc, int32_t* D,
+                                 int64_t ldd);
+
+// FP64 GEMM (DMMA), B column- or row-major.
+mma_status_t launch_gemm_f64(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
+                             const double* A, int64_t lda, const double* B,
+                             int64_t ldb, bool b_row_major, const double* C,
+                             int64_t ldc, double* D, int64_t ldd);
+
+// Batched 16x16x16 FP16/BF16 -> FP32 with A-block broadcast.
+mma_status_t launch_batched16(const Ctx& ctx, bool bf16, int64_t batch,
+                              int group, int abid, const void* A,
+                              const void* B, const float* C, float* D);
+
+// K == 0: D = C (or 0), elementwise, element size 4 or 8 bytes.
+mma_status_t launch_copy_c(const Ctx& ctx, int64_t M, int64_t N,
+                           int elem_bytes, const void* C, int64_t ldc, void* D,
+                           int64_t ldd);
+
+}  // namespace mmagb

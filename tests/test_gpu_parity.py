@@ -1,0 +1,229 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small and ragged shapes are compared element by element over the whole
+output; the full-size workloads are compared on random row x column blocks
+of the output (the oracle computes each block from the gathered rows of A
+and columns of B), except the batched workload, which is compared in full.
+Tolerances are in tests/helpers.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_dense_02_gb300 import binding, synth
+
+from helpers import check, dev_padded, oracle_ref, to_dev
+
+pytestmark = pytest.mark.gpu
+
+OUT_NP = {"f16": np.float32, "bf16": np.float32, "i8": np.int32, "f64": np.float64}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mixed_precision_dense_02_gb300 import build
+    build.build()
+    binding.load()
+    yield
+    binding.device_status()
+
+
+def run_gemm(g, *, pad=0, use_c=True, inplace=False):
+    """Run the GPU GEMM for GemmInputs g with padded leading dimensions."""
+    import torch
+    A = dev_padded(g.A, g.dtype_in, extra=pad)
+    B = dev_padded(g.B, g.dtype_in, extra=pad)
+    C = dev_padded(g.C, extra=pad) if use_c else None
+    if inplace:
+        D = C
+    else:
+        D = dev_padded(np.zeros_like(g.C), extra=pad + 1)
+    out = binding.gemm_ex(A, B, C, D, b_layout=g.b_layout)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+SHAPES = [(1, 1, 1), (16, 16, 16), (128, 128, 64), (127, 129, 65),
+          (256, 256, 256), (200, 300, 100), (333, 257, 1000), (64, 520, 40),
+          (1000, 136, 520), (130, 17, 3)]
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8", "f64"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_small_shapes(dtype_in, M, N, K):
+    g = synth.gemm_inputs(f"par_{M}_{N}_{K}", dtype_in, M, N, K, dist="uniform")
+    want, ab = oracle_ref(g)
+    check(dtype_in, run_gemm(g), want, ab, f"{dtype_in} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8", "f64"])
+def test_padding_no_c_and_in_place(dtype_in):
+    M, N, K = 260, 392, 328
+    g = synth.gemm_inputs("par_pad", dtype_in, M, N, K, dist="normal")
+    want, ab = oracle_ref(g)
+    check(dtype_in, run_gemm(g, pad=3), want, ab, "padded")
+    check(dtype_in, run_gemm(g, inplace=True), want, ab, "in place")
+    g0 = synth.GemmInputs(dtype_in, M, N, K, g.A, g.B, np.zeros_like(g.C))
+    want0, ab0 = oracle_ref(g0)
+    check(dtype_in, run_gemm(g, use_c=False), want0, ab0, "C = NULL")
+
+
+def test_f64_row_major_b():
+    for (M, N, K) in [(1, 1, 1), (65, 63, 17), (256, 192, 300)]:
+        g = synth.gemm_inputs(f"par_f64row_{M}", "f64", M, N, K, b_layout="row")
+        want, ab = oracle_ref(g)
+        check("f64", run_gemm(g), want, ab, f"f64 row-B {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8", "f64"])
+def test_k_zero_gives_c(dtype_in):
+    M, N = 37, 44
+    g = synth.gemm_inputs("par_k0", dtype_in, M, N, 8)
+    g = synth.GemmInputs(dtype_in, M, N, 0, g.A[:, :0], g.B[:, :0], g.C)
+    import torch
+    C = to_dev(g.C)
+    A = to_dev(np.zeros((M, 8), g.A.dtype), dtype_in)[:, :0]
+    B = to_dev(np.zeros((N, 8), g.B.dtype), dtype_in)[:, :0]
+    D = binding.gemm(A, B, C)
+    torch.cuda.synchronize()
+    assert np.array_equal(D.cpu().numpy(), g.C)
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8"])
+def test_all_ones_closed_form_exact(dtype_in):
+    """A = B = 1: D_ij = K + C_ij.  Integer partial sums below 2^24 are exact
+    in FP32, so FP16/BF16 must match bit for bit as well."""
+    M, N, K = 300, 260, 4096
+    one = {"f16": np.uint16(0x3C00), "bf16": np.uint16(0x3F80), "i8": np.int8(1)}[dtype_in]
+    A = np.full((M, K), one)
+    B = np.full((N, K), one)
+    g0 = synth.gemm_inputs("par_ones", dtype_in, M, N, 16)
+    C = g0.C
+    if dtype_in != "i8":
+        C = np.round(C * 64).astype(np.float32)  # integers: K + C exact
+    g = synth.GemmInputs(dtype_in, M, N, K, A, B, C)
+    got = run_gemm(g)
+    assert np.array_equal(got, (C.astype(np.float64) + K).astype(got.dtype))
+
+
+@pytest.mark.parametrize("dtype_in", ["bf16", "f64"])
+def test_identity_closed_form(dtype_in):
+    """B = I: D = A + C (one rounding)."""
+    n = 384
+    g = synth.gemm_inputs("par_eye", dtype_in, n, n, n)
+    if dtype_in == "bf16":
+        eye = np.where(np.eye(n, dtype=bool), np.uint16(0x3F80), np.uint16(0)).astype(np.uint16)
+        a = synth.bf16_bits_to_f32(g.A).astype(np.float64)
+    else:
+        eye = np.eye(n)
+        a = g.A
+    g = synth.GemmInputs(dtype_in, n, n, n, g.A, eye, g.C)
+    got = run_gemm(g)
+    assert np.array_equal(got, (a + g.C.astype(np.float64)).astype(got.dtype))
+
+
+@pytest.mark.parametrize("dtype_in", ["bf16", "i8"])
+def test_transpose_property(dtype_in):
+    """(A B + C)^T computed as B^T A^T + C^T agrees within tolerance."""
+    M, N, K = 384, 272, 520
+    g = synth.gemm_inputs("par_T", dtype_in, M, N, K)
+    gT = synth.GemmInputs(dtype_in, N, M, K, g.B, g.A, np.ascontiguousarray(g.C.T))
+    want, ab = oracle_ref(g)
+    check(dtype_in, run_gemm(gT).T, want, None if ab is None else ab, "transposed")
+
+
+def test_i8_extremes_exact():
+    M, N, K = 256, 256, 4096
+    C = synth.int_uniform(0, 3, M * N, -(1 << 20), 1 << 20).astype(np.int32).reshape(M, N)
+    for a, b in ((-128, -128), (-128, 127), (127, 127)):
+        g = synth.GemmInputs("i8", M, N, K, np.full((M, K), a, np.int8),
+                             np.full((N, K), b, np.int8), C)
+        assert np.array_equal(run_gemm(g), C + K * a * b)
+
+
+# ------------------------------------------------------------ batched
+
+def run_batched(bi):
+    import torch
+    D = binding.gemm_batched(to_dev(bi.A, bi.dtype_in), to_dev(bi.B, bi.dtype_in),
+                             to_dev(bi.C), group=bi.group, abid=bi.abid)
+    torch.cuda.synchronize()
+    return D.cpu().numpy()
+
+
+def batched_absab(bi):
+    return oracle.gemm_batched(bi.dtype_in, bi.A & 0x7FFF, bi.B & 0x7FFF, None,
+                               group=bi.group, abid=bi.abid).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("G,abid,batch", [(1, 0, 1), (1, 0, 7), (2, 1, 6), (4, 1, 64),
+                                          (4, 3, 1028), (8, 5, 80), (16, 0, 160)])
+def test_batched_small(dtype_in, G, abid, batch):
+    bi = synth.batched_inputs(f"par_b_{G}_{batch}", dtype_in, batch, group=G, abid=abid)
+    want = oracle.gemm_batched(dtype_in, bi.A, bi.B, bi.C, group=G, abid=abid)
+    check(dtype_in, run_batched(bi), want, batched_absab(bi), f"batched G={G}")
+
+
+def test_batched_worked_example_on_gpu():
+    """The broadcast example of "Common MFMA parameters" (cbsz = 2, abid = 1):
+    A tile t = (t+1) I and B = I, so D_b = (src(b)+1) I identifies src(b)."""
+    import torch
+    batch, n = 16, 16
+    A = np.zeros((batch, n, n), np.uint16)
+    for t in range(batch):
+        A[t] = np.where(np.eye(n, dtype=bool), synth.round_bf16_bits(np.array([t + 1.0]))[0], 0)
+    B = np.broadcast_to(np.where(np.eye(n, dtype=bool), np.uint16(0x3F80), np.uint16(0)),
+                        (batch, n, n)).astype(np.uint16)
+    D = binding.gemm_batched(to_dev(A, "bf16"), to_dev(B, "bf16"), None, group=4, abid=1)
+    torch.cuda.synchronize()
+    D = D.cpu().numpy()
+    for b, src in [(0, 1), (1, 1), (2, 1), (3, 1), (4, 5), (5, 5), (6, 5), (7, 5)]:
+        assert np.array_equal(D[b], (src + 1) * np.eye(n, dtype=np.float32))
+
+
+# ------------------------------------------------- full-size workloads
+
+def _sample_blocks(g, rng, nrow, ncol):
+    rows = np.sort(rng.choice(g.M, size=min(nrow, g.M), replace=False))
+    cols = np.sort(rng.choice(g.N, size=min(ncol, g.N), replace=False))
+    # always include the last row/column (ragged tile edges)
+    rows[-1], cols[-1] = g.M - 1, g.N - 1
+    return np.unique(rows), np.unique(cols)
+
+
+@pytest.mark.parametrize("name", ["gemm_f16_256", "gemm_i8_4096", "gemm_bf16_8192",
+                                  "gemm_f64_4096_rowB",
+                                  "gemm_bf16_skinny_16384x128x4096"])
+def test_full_size_workload(name):
+    import torch
+    w = synth.WORKLOADS[name]
+    g = synth.gemm_inputs(name, w["dtype_in"], w["M"], w["N"], w["K"],
+                          dist=w.get("dist", "normal"),
+                          b_layout=w.get("b_layout", "col"))
+    D = binding.gemm_ex(to_dev(g.A, g.dtype_in), to_dev(g.B, g.dtype_in),
+                        to_dev(g.C), b_layout=g.b_layout)
+    torch.cuda.synchronize()
+    if g.M * g.N * g.K <= 256 ** 3:
+        want, ab = oracle_ref(g)
+        check(g.dtype_in, D.cpu().numpy(), want, ab, name)
+        return
+    rng = np.random.default_rng(1234)
+    rows, cols = _sample_blocks(g, rng, 96, 96)
+    got = D[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    want, ab = oracle_ref(g, rows, cols)
+    check(g.dtype_in, got, want, ab, name)
+    assert bool(torch.isfinite(D.double()).all()) if g.dtype_in != "i8" else True
+
+
+def test_full_size_batched_workload():
+    name = "batched_bf16_16x16x16_b262144_g4_abid1"
+    w = synth.WORKLOADS[name]
+    bi = synth.batched_inputs(name, "bf16", w["batch"], group=w["group"], abid=w["abid"])
+    got = run_batched(bi)
+    want = oracle.gemm_batched("bf16", bi.A, bi.B, bi.C, group=bi.group, abid=bi.abid)
+    check("bf16", got, want, batched_absab(bi), name)
