@@ -1,0 +1,599 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 dense multiply-accumulate path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--headline-only]
+
+One step is one D = A*B + C call (operand staging, the MMA K loop and the
++C epilogue) on the headline workload: the INT8 -> INT32 GEMM with
+M = N = K = 4096 (A row-major, B column-major, C/D int32), seeded synthetic
+inputs already resident in HBM.  Several input sets are rotated so that the
+bytes touched between two uses of a set exceed the 129 MB L2.  Rank 0 prints
+one JSON line: whole-job TOP/s (all ranks' operations / max-over-ranks time),
+the dominant kernel's roofline (per-launch CUDA-event durations recorded by
+the library on the launching stream), an end-to-end figure through host
+buffers, SM clocks sampled during the timed region, the CPU oracle timed on
+a bounded sample, and a per-dtype table of the other workloads.
+
+Multi-GPU: every rank runs its own independent problem (weak scaling, no
+data-path collective); torch.distributed is used only for the barrier and
+the max-over-ranks time.
+
+``--impl reference`` times the CPU oracle (the plain C reference
+implementation) on the host cores instead, on a bounded sample of the same
+workload per step; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (TOP/s int8) and % of GB300 dense tensor peak per dtype"
+HEADLINE = "gemm_i8_4096"
+L2_BYTES = 129 * 1024 * 1024
+MAX_SET_BYTES = 8 << 30  # device memory cap for the rotating input sets
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_FP64_TFLOPS = 1.25
+
+# DRAM bytes per launch of each dominant kernel from one ncu capture, keyed
+# by the SHA-256 of the kernel's source file at capture time (a changed
+# source makes the figure stale, and it is then reported as null).
+NCU_TRAFFIC: dict = {
+    # ncu --set full, one launch after 3 warm-up launches (profiles/*.md)
+    "gemm_i8_4096": {"sha": "ba41bff384236b62", "bytes": 101056512 + 41768960},
+    "gemm_bf16_8192": {"sha": "8a795dd324c11a86", "bytes": 1372195000 + 252497920},
+    "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "24a0b2e421dd643e",
+                                               "bytes": 436229888 + 226331648},
+}
+
+
+# --------------------------------------------------------------- helpers
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(rel):
+    try:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+class Dist:
+    """Rank bookkeeping; torch.distributed only when WORLD_SIZE > 1."""
+
+    def __init__(self, want_cuda: bool):
+        self.rank = _env_int("RANK", 0)
+        self.world = _env_int("WORLD_SIZE", 1)
+        self.local_rank = _env_int("LOCAL_RANK", 0)
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as td
+            backend = "nccl" if want_cuda else "gloo"
+            td.init_process_group(backend=backend)
+            self.pg = td
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = torch.device("cuda", self.local_rank) if torch.cuda.is_available() \
+            and self.pg.get_backend() == "nccl" else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def whole_job(units_per_step: float, steps: int, world: int, seconds: float):
+    """Aggregate throughput: all ranks' units over the max-over-ranks time."""
+    return units_per_step * steps * world / seconds
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []  # (host time, fields...)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not win:
+            win = [p for (_, p) in self.samples]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        pw = [num(p[3]) for p in win if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4)
+                          if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+# ------------------------------------------------------------ workloads
+
+def workload_meta(name):
+    from mixed_precision_dense_02_gb300 import synth
+    w = dict(synth.WORKLOADS[name])
+    if w["kind"] == "gemm":
+        ops = 2.0 * w["M"] * w["N"] * w["K"]
+        isz = {"f16": 2, "bf16": 2, "i8": 1, "f64": 8}[w["dtype_in"]]
+        osz = 8 if w["dtype_in"] == "f64" else 4
+        nbytes = (w["M"] * w["K"] + w["N"] * w["K"]) * isz + 2 * w["M"] * w["N"] * osz
+    else:
+        ops = 2.0 * w["batch"] * w["M"] * w["N"] * w["K"]
+        tile_in = w["M"] * w["K"] * 2
+        nbytes = (w["batch"] // w["group"]) * tile_in + w["batch"] * (
+            w["N"] * w["K"] * 2 + 2 * w["M"] * w["N"] * 4)
+    w["ops"] = ops
+    w["algorithmic_bytes"] = nbytes
+    w["unit"] = "TOP/s" if w["dtype_in"] == "i8" else "TFLOP/s"
+    return w
+
+
+def roofline_bound(name, w):
+    """(bound, unit, peak, peak_note) of the workload's dominant kernel."""
+    peaks, src = load_peaks()
+    if w["kind"] == "batched" or "skinny" in name:
+        return "hbm", "GB/s", peaks["hbm_gbs"], f"hbm_gbs of {src}"
+    if w["dtype_in"] == "f64":
+        p = peaks["bf16_tflops"] * NOMINAL_FP64_TFLOPS / NOMINAL_BF16_TFLOPS
+        return "tensor", "TFLOP/s", p, f"bf16_tflops of {src} x nominal fp64/bf16 (1.25/2250)"
+    return "tensor", "TFLOP/s", peaks["bf16_tflops"], f"bf16_tflops (burst) of {src}"
+
+
+def kernel_source(w):
+    if w["kind"] == "batched":
+        return "mixed_precision_dense_02_gb300/csrc/batched16.cu"
+    return {"f16": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
+            "bf16": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
+            "i8": "mixed_precision_dense_02_gb300/csrc/gemm_i8.cu",
+            "f64": "mixed_precision_dense_02_gb300/csrc/gemm_f64.cu"}[w["dtype_in"]]
+
+
+class GpuWorkload:
+    """Device-resident input sets of one workload and its step function."""
+
+    def __init__(self, name, seed=0):
+        import numpy as np
+        import torch
+        from mixed_precision_dense_02_gb300 import binding, synth
+        self.name = name
+        self.w = workload_meta(name)
+        self.binding = binding
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        w = self.w
+        if w["kind"] == "gemm":
+            g = synth.gemm_inputs(name, w["dtype_in"], w["M"], w["N"], w["K"],
+                                  dist=w.get("dist", "normal"),
+                                  b_layout=w.get("b_layout", "col"), seed=seed)
+            host = [g.A, g.B, g.C]
+            self.b_layout = g.b_layout
+        else:
+            bi = synth.batched_inputs(name, w["dtype_in"], w["batch"], w["M"],
+                                      w["N"], w["K"], group=w["group"],
+                                      abid=w["abid"], dist=w.get("dist", "uniform"),
+                                      seed=seed)
+            host = [bi.A, bi.B, bi.C]
+        self.dtype_in = w["dtype_in"]
+        self.host = [self._pinned(x) for x in host]
+        # A, B, C and D of one set; rotate enough sets that more than twice
+        # the L2 capacity is touched between two uses of the same set
+        per_set = (sum(t.numel() * t.element_size() for t in self.host)
+                   + self.host[2].numel() * self.host[2].element_size())
+        self.per_set_bytes = per_set
+        self.nsets = max(1, min(max(1, MAX_SET_BYTES // per_set),
+                                math.ceil(2 * L2_BYTES / per_set) + 1))
+        self.l2_note = (f"{self.nsets} rotating input sets of {per_set / 1e6:.1f} MB"
+                        f" ({self.nsets * per_set / 1e6:.0f} MB > 2 x L2 between reuses of a set)")
+        self.sets = []
+        for _ in range(self.nsets):
+            A, B, C = (self._dev(t) for t in self.host)
+            D = torch.empty_like(C)
+            self.sets.append((A, B, C, D))
+        self.host_D = torch.empty(self.host[2].shape, dtype=self.sets[0][3].dtype,
+                                  pin_memory=True)
+        self.launches_per_step = 1
+
+    def _pinned(self, x):
+        import numpy as np
+        import torch
+        if x.dtype == np.uint16:
+            x = x.view(np.int16)
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        return t.pin_memory()
+
+    def _dev(self, t):
+        import torch
+        d = t.to(self.dev, non_blocking=False)
+        if d.dtype == torch.int16:
+            d = d.view(torch.bfloat16 if self.dtype_in == "bf16" else torch.float16)
+        return d
+
+    def call(self, A, B, C, D):
+        w = self.w
+        if w["kind"] == "gemm":
+            self.binding.gemm_ex(A, B, C, D, b_layout=self.b_layout)
+        else:
+            self.binding.gemm_batched(A, B, C, D, group=w["group"], abid=w["abid"])
+
+    def step(self, i):
+        self.call(*self.sets[i % self.nsets])
+
+    def e2e_step(self):
+        """Host -> device inputs, the call, device -> host result."""
+        A, B, C, D = self.sets[0]
+        for dst, src in zip((A, B, C), self.host):
+            dst.view(src.dtype).copy_(src, non_blocking=True)
+        self.call(A, B, C, D)
+        self.host_D.copy_(D, non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host)
+
+    @property
+    def d2h_bytes(self):
+        return self.host_D.numel() * self.host_D.element_size()
+
+
+def time_steps(torch, dist, fn, steps, warmup):
+    """Warm up, then time exactly `steps` calls between barriers + syncs."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    start.record()
+    for i in range(steps):
+        fn(warmup + i)
+    stop.record()
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    dist.barrier()
+    ms = start.elapsed_time(stop)
+    return ms / 1e3, t_host0, t_host1
+
+
+def measure_workload(torch, dist, name, steps, warmup, with_e2e, sustain_s=0.0):
+    wl = GpuWorkload(name)
+    w = wl.w
+    b = wl.binding
+    # throughput pass: no profiling events in the stream
+    secs, t0, t1 = time_steps(torch, dist, wl.step, steps, warmup)
+    secs_max = dist.max(secs)
+    if sustain_s and t1 - t0 < sustain_s:
+        # The timed region is shorter than the clock sampling needs: keep the
+        # same step loop running (untimed) so the sampled window, which
+        # starts at the timed region, covers a sustained load.
+        i = 0
+        while time.time() - t0 < sustain_s:
+            for _ in range(16):
+                wl.step(i)
+                i += 1
+            torch.cuda.synchronize()
+        t1 = time.time()
+    value = whole_job(w["ops"], steps, dist.world, secs_max) / 1e12
+    # per-launch durations of the dominant kernel, same loop, events on the
+    # launching stream recorded by the library
+    b.profile_begin()
+    time_steps(torch, dist, wl.step, steps, 0)
+    launch_ms = b.profile_end()
+    b.device_status()
+    mean_ms = statistics.fmean(launch_ms) if launch_ms else float("nan")
+    bound, unit, peak, note = roofline_bound(name, w)
+    if unit == "GB/s":
+        achieved = w["algorithmic_bytes"] / (mean_ms * 1e-3) / 1e9
+    else:
+        achieved = w["ops"] / (mean_ms * 1e-3) / 1e12
+    src = kernel_source(w)
+    traffic = None
+    rec = NCU_TRAFFIC.get(name)
+    if rec and rec.get("sha") == source_sha(src):
+        traffic = rec["bytes"]
+    res = {
+        "value": value, "unit": w["unit"], "ms_per_step": secs_max * 1e3 / steps,
+        "steps": steps, "warmup": warmup, "l2": wl.l2_note,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": note, "kernel_launches_timed": len(launch_ms),
+                     "kernel_ms_mean": mean_ms,
+                     "algorithmic_bytes_per_launch": w["algorithmic_bytes"],
+                     "ops_per_launch": w["ops"]},
+        "pct_of_bf16_peak": None, "host_window": (t0, t1),
+        "gpu_launches": steps * wl.launches_per_step,
+    }
+    if w["kind"] == "gemm" and w["dtype_in"] != "f64":
+        res["pct_of_bf16_peak"] = 100.0 * value / load_peaks()[0]["bf16_tflops"]
+    if with_e2e:
+        e_steps = max(3, min(steps, 20))
+        secs_e, _, _ = time_steps(torch, dist, lambda i: wl.e2e_step(), e_steps,
+                                  min(warmup, 3))
+        secs_e = dist.max(secs_e)
+        res["e2e"] = {"value": whole_job(w["ops"], e_steps, dist.world, secs_e) / 1e12,
+                      "unit": w["unit"], "h2d_bytes_per_step": wl.h2d_bytes,
+                      "d2h_bytes_per_step": wl.d2h_bytes, "steps": e_steps}
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------- CPU oracle
+
+def oracle_sample_step(name, rows, seed=0):
+    """One oracle run on the first `rows` rows (or batch entries) of the
+    workload; returns (seconds, operations)."""
+    import numpy as np
+    import oracle
+    w = workload_meta(name)
+    if w["kind"] == "gemm":
+        g = _sample_inputs_cache(name, seed)
+        A = np.ascontiguousarray(g.A[:rows])
+        C = np.ascontiguousarray(g.C[:rows])
+        t = time.perf_counter()
+        oracle.gemm(g.dtype_in, A, g.B, C, b_layout=g.b_layout)
+        dt = time.perf_counter() - t
+        return dt, 2.0 * rows * w["N"] * w["K"]
+    bi = _sample_inputs_cache(name, seed)
+    n = rows - rows % w["group"] or w["group"]
+    t = time.perf_counter()
+    oracle.gemm_batched(bi.dtype_in, bi.A[:n], bi.B[:n], bi.C[:n],
+                        group=bi.group, abid=bi.abid)
+    dt = time.perf_counter() - t
+    return dt, 2.0 * n * w["M"] * w["N"] * w["K"]
+
+
+_INPUT_CACHE = {}
+
+
+def _sample_inputs_cache(name, seed):
+    from mixed_precision_dense_02_gb300 import synth
+    if name not in _INPUT_CACHE:
+        w = synth.WORKLOADS[name]
+        if w["kind"] == "gemm":
+            _INPUT_CACHE[name] = synth.gemm_inputs(
+                name, w["dtype_in"], w["M"], w["N"], w["K"],
+                dist=w.get("dist", "normal"), b_layout=w.get("b_layout", "col"),
+                seed=seed)
+        else:
+            _INPUT_CACHE[name] = synth.batched_inputs(
+                name, w["dtype_in"], w["batch"], w["M"], w["N"], w["K"],
+                group=w["group"], abid=w["abid"], dist=w.get("dist", "uniform"),
+                seed=seed)
+    return _INPUT_CACHE[name]
+
+
+def calibrate_rows(name, target_s):
+    """Rows (or batch entries) of the workload that take about target_s."""
+    w = workload_meta(name)
+    total = w["M"] if w["kind"] == "gemm" else w["batch"]
+    rows = 4 if w["kind"] == "gemm" else 4096
+    dt, _ = oracle_sample_step(name, rows)
+    while dt < 0.2 and rows < total:
+        rows = min(total, rows * 4)
+        dt, _ = oracle_sample_step(name, rows)
+    rows = int(min(total, max(1, rows * target_s / max(dt, 1e-6))))
+    return rows
+
+
+def cpu_baseline(name, target_s=10.0):
+    import oracle
+    rows = calibrate_rows(name, target_s)
+    dt, ops = oracle_sample_step(name, rows)
+    w = workload_meta(name)
+    what = "rows of A (with all of B, C)" if w["kind"] == "gemm" else "batch entries"
+    return {"value": ops / dt / 1e12, "unit": w["unit"],
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {rows} {what} of {name}; {dt:.1f} s, {ops:.3e} ops"}
+
+
+# ------------------------------------------------------------------ main
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return 0
+    import oracle
+    name = args.workload
+    w = workload_meta(name)
+    per_step = max(0.2, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows = calibrate_rows(name, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_step(name, rows)
+    tot_s, tot_ops = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, ops = oracle_sample_step(name, rows)
+        tot_s += dt
+        tot_ops += ops
+    value = tot_ops / tot_s / 1e12
+    what = "rows of A (with all of B, C)" if w["kind"] == "gemm" else "batch entries"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": w["unit"],
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": _dtype_tag(w),
+        "data": "synthetic", "config": _config(name, w, "n/a (host CPU)"),
+        "cpu_baseline": {"value": value, "unit": w["unit"],
+                         "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"first {rows} {what} of {name} per step"},
+        "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _dtype_tag(w):
+    return {"f16": "f16", "bf16": "bf16", "i8": "i8", "f64": "f64"}[w["dtype_in"]]
+
+
+def _config(name, w, l2):
+    cfg = {"workload": name, "l2": l2}
+    for k in ("M", "N", "K", "batch", "group", "abid", "dtype_in"):
+        if k in w:
+            cfg[k] = w[k]
+    if w["kind"] == "gemm":
+        cfg["layout"] = ("A row-major, B " + ("row" if w.get("b_layout") == "row"
+                         else "column") + "-major, C/D row-major")
+    return cfg
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--headline-only", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        dist = Dist(want_cuda=False)
+        try:
+            return run_reference(args, dist)
+        finally:
+            dist.close()
+
+    import torch
+    torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+    dist = Dist(want_cuda=True)
+    import mixed_precision_dense_02_gb300 as pkg
+    pkg.load()
+    w = workload_meta(args.workload)
+
+    clocks = ClockSampler(dist.local_rank)
+    clocks.start()
+    time.sleep(0.5)
+    res = measure_workload(torch, dist, args.workload, args.steps, args.warmup,
+                           with_e2e=True, sustain_s=2.0)
+    clocks.stop()
+    clk = clocks.summary(*res["host_window"])
+
+    per_dtype = {}
+    if not args.headline_only:
+        from mixed_precision_dense_02_gb300 import synth
+        for name in synth.WORKLOADS:
+            if name == args.workload:
+                continue
+            wm = workload_meta(name)
+            k = 3 if wm["dtype_in"] == "f64" else max(3, min(args.steps, 20))
+            r = measure_workload(torch, dist, name, k, 3, with_e2e=False)
+            per_dtype[name] = {"value": r["value"], "unit": r["unit"],
+                               "ms_per_step": r["ms_per_step"], "steps": k,
+                               "pct_of_bf16_peak": r["pct_of_bf16_peak"],
+                               "l2": r["l2"],
+                               "roofline": r["roofline"]}
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1:
+        cpu = cpu_baseline(args.workload)
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": res["value"], "unit": res["unit"],
+            "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": _dtype_tag(w),
+            "data": "synthetic (seeded Philox; shapes/distributions of the workload)",
+            "config": _config(args.workload, w, res["l2"]),
+            "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+            "clocks": clk, "gpu_launches": res["gpu_launches"],
+            "per_dtype": per_dtype,
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

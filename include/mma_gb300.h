@@ -161,6 +161,29 @@ mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc, int64_t M,
  */
 mma_status_t mma_device_status(void *stream);
 
+/*
+ * mma_profile_begin / mma_profile_end -- per-launch timing of the dominant
+ * kernel (the contraction kernel of each mma_gemm* call), for measuring it
+ * against its roofline.  The pages time each kernel launch after warm-up
+ * runs ("RDNA3 dense WMMA builtins", section "Instantiating the kernel");
+ * this is the device-side counterpart.
+ *
+ * mma_profile_begin: start recording, on the current device, one CUDA event
+ * pair on the caller's stream immediately around the dominant kernel of
+ * each subsequent call (at most 4096 calls; later calls are not recorded).
+ * The event pool is created on the first begin (never per call).  Returns
+ * MMA_ERR_NO_DEVICE without a device, MMA_ERR_INVALID_ARG if the pool
+ * belongs to another device.
+ *
+ * mma_profile_end: stop recording, wait for the recorded events, write the
+ * durations in milliseconds of the first min(count, max_count) recorded
+ * launches to ms[] (host array owned by the caller) and the number recorded
+ * to *count.  Returns MMA_ERR_INVALID_ARG if profiling was not active.
+ * Not thread-safe with concurrent calls on other threads.
+ */
+mma_status_t mma_profile_begin(void);
+mma_status_t mma_profile_end(float *ms, int max_count, int *count);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mma_status_string(int status);
 

@@ -32,6 +32,9 @@ SIGNATURES = {
                                 _i64, _p, _i64, _p, _i64, _i64, _int, _int,
                                 _p]),
     "mma_device_status": (_int, [_p]),
+    "mma_profile_begin": (_int, []),
+    "mma_profile_end": (_int, [ctypes.POINTER(ctypes.c_float), _int,
+                               ctypes.POINTER(_int)]),
     "mma_status_string": (ctypes.c_char_p, [_int]),
     "mma_version": (_int, []),
 }
@@ -203,6 +206,19 @@ def gemm_batched(A, B, C=None, D=None, *, group: int = 1, abid: int = 0,
                           _stream(stream))
     _check("mma_gemm_batched", st)
     return D
+
+
+def profile_begin() -> None:
+    """Start recording the duration of each call's dominant kernel."""
+    _check("mma_profile_begin", load().mma_profile_begin())
+
+
+def profile_end(max_count: int = 4096) -> list:
+    """Stop recording; durations (ms) of the recorded dominant kernels."""
+    buf = (ctypes.c_float * max_count)()
+    n = _int(0)
+    _check("mma_profile_end", load().mma_profile_end(buf, max_count, ctypes.byref(n)))
+    return [float(buf[i]) for i in range(min(n.value, max_count))]
 
 
 def device_status(stream=None) -> None:

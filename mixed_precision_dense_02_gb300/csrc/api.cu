@@ -27,6 +27,29 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
+// Profiling ring: while active, each call records one event pair around its
+// dominant kernel.  Events are created once and reused.
+constexpr int kProfMax = 4096;
+struct Profile {
+  bool active = false;
+  int device = -1;
+  int count = 0;
+  cudaEvent_t ev[2 * kProfMax] = {};
+  bool created = false;
+};
+Profile g_prof;
+std::mutex g_prof_mu;
+
+// Attach the next profiling event pair (if any) to a launch context.
+void attach_profile(Ctx& ctx) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof.active || g_prof.device != ctx.device || g_prof.count >= kProfMax)
+    return;
+  ctx.prof_start = g_prof.ev[2 * g_prof.count];
+  ctx.prof_stop = g_prof.ev[2 * g_prof.count + 1];
+  ++g_prof.count;
+}
+
 // Per-device set-up, once, with that device current: SM count, the
 // architecture check and the device address of the status word.
 const DeviceInfo* device_info(int* dev_out) {
@@ -159,6 +182,7 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
   const DeviceInfo* info = device_info(&dev);
   if (!info) return MMA_ERR_NO_DEVICE;
   Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  attach_profile(ctx);
 
   if (K == 0) return launch_copy_c(ctx, M, N, int(ea), C, ldc, D, ldd);
   switch (dtype_in) {
@@ -220,6 +244,7 @@ extern "C" mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc,
   const DeviceInfo* info = device_info(&dev);
   if (!info) return MMA_ERR_NO_DEVICE;
   Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  attach_profile(ctx);
   return launch_batched16(ctx, dtype_in == MMA_BF16, batch, G, a_broadcast_id,
                           A, B, static_cast<const float*>(C),
                           static_cast<float*>(D));
@@ -239,6 +264,45 @@ extern "C" mma_status_t mma_device_status(void* stream) {
     if (cudaMemcpyToSymbol(g_mma_status, &zero, sizeof(zero)) != cudaSuccess)
       return MMA_ERR_LAUNCH;
     return MMA_ERR_TIMEOUT;
+  }
+  return MMA_OK;
+}
+
+extern "C" mma_status_t mma_profile_begin(void) {
+  int dev = -1;
+  if (!device_info(&dev)) return MMA_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof.created && g_prof.device != dev) return MMA_ERR_INVALID_ARG;
+  if (!g_prof.created) {
+    for (int i = 0; i < 2 * kProfMax; ++i) {
+      if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
+        cudaGetLastError();
+        return MMA_ERR_LAUNCH;
+      }
+    }
+    g_prof.created = true;
+    g_prof.device = dev;
+  }
+  g_prof.active = true;
+  g_prof.count = 0;
+  return MMA_OK;
+}
+
+extern "C" mma_status_t mma_profile_end(float* ms, int max_count,
+                                        int* count) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof.active) return MMA_ERR_INVALID_ARG;
+  g_prof.active = false;
+  const int n = g_prof.count < max_count ? g_prof.count : max_count;
+  if (count) *count = g_prof.count;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms[i], g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return MMA_ERR_LAUNCH;
+    }
   }
   return MMA_OK;
 }

@@ -120,9 +120,11 @@ mma_status_t run(const Ctx& ctx, int64_t batch, int abid, const void* A,
   int64_t blocks = (units + warps_per_block - 1) / warps_per_block;
   const int64_t cap = int64_t(ctx.num_sms) * 8;
   if (blocks > cap) blocks = cap;
+  ctx.mark_start();
   batched16_kernel<G, BF16><<<int(blocks), kThreads, 0, ctx.stream>>>(
       static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), C, D,
       batch, abid);
+  ctx.mark_stop();
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }
 

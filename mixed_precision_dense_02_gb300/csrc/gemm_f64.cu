@@ -129,12 +129,14 @@ mma_status_t launch_gemm_f64(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   const int64_t gx = (N + TN - 1) / TN, gy = (M + TM - 1) / TM;
   if (gy > 65535) return MMA_ERR_UNSUPPORTED;
   const dim3 grid{unsigned(gx), unsigned(gy), 1u};
+  ctx.mark_start();
   if (b_row_major)
     gemm_f64_kernel<true><<<grid, kThreads, 0, ctx.stream>>>(
         A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K));
   else
     gemm_f64_kernel<false><<<grid, kThreads, 0, ctx.stream>>>(
         A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K));
+  ctx.mark_stop();
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }
 

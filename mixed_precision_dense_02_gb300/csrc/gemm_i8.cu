@@ -164,9 +164,11 @@ mma_status_t launch_gemm_i8_imma(const Ctx& ctx, int64_t M, int64_t N,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return MMA_ERR_LAUNCH;
+  ctx.mark_start();
   gemm_i8_imma_kernel<<<dim3(unsigned(gx), unsigned(gy)), kThreads, smem,
                         ctx.stream>>>(A, lda, B, ldb, C, ldc, D, ldd, int(M),
                                       int(N), int(K));
+  ctx.mark_stop();
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }
 

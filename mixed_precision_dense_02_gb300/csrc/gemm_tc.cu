@@ -317,9 +317,11 @@ mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
     return MMA_ERR_LAUNCH;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = int(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  ctx.mark_start();
   kern<<<grid, kThreads, L::ALLOC, ctx.stream>>>(ta, tb, C, ldc, D, ldd,
                                                  int(M), int(N), int(K),
                                                  ctx.status);
+  ctx.mark_stop();
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }
 

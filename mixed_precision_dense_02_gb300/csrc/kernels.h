@@ -14,6 +14,17 @@ struct Ctx {
   int device;
   int num_sms;
   unsigned* status;  // device status word (bounded-wait timeouts)
+  // When profiling is active: events recorded on `stream` immediately
+  // before and after the call's dominant (contraction) kernel; else null.
+  cudaEvent_t prof_start = nullptr;
+  cudaEvent_t prof_stop = nullptr;
+
+  void mark_start() const {
+    if (prof_start) cudaEventRecord(prof_start, stream);
+  }
+  void mark_stop() const {
+    if (prof_stop) cudaEventRecord(prof_stop, stream);
+  }
 };
 
 // tcgen05 GEMM, FP16/BF16 inputs, FP32 accumulate, column-major B.

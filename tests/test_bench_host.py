@@ -1,0 +1,96 @@
+"""Host-side logic of bench.py on CPU: the multi-rank path over gloo
+(world size 2), the reference arm's JSON line, and the clock summary."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    d = bench.Dist(want_cuda=False)
+    d.barrier()
+    m = d.max(1.0 + rank)           # each rank's own "time"
+    v = bench.whole_job(10.0, 4, d.world, m)
+    d.close()
+    q.put((rank, m, v))
+
+
+def test_two_rank_max_and_whole_job_over_gloo():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # both ranks see the max time (2.0) and the whole-job value 10*4*2/2
+    assert out == [(0, 2.0, 40.0), (1, 2.0, 40.0)]
+
+
+def test_reference_arm_prints_one_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"),
+                          "--impl", "reference", "--steps", "1", "--warmup", "0",
+                          "--workload", "gemm_f16_256"],
+                         capture_output=True, text=True, timeout=300, check=True)
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["value"] > 0
+    assert rec["unit"] == "TFLOP/s" and rec["warmup"] >= 3
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_non_zero_rank_is_silent():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1",
+               MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+    # rank 1 alone: its process group cannot form, so run the rank logic
+    # directly instead of the whole program
+    args = type("A", (), dict(steps=1, warmup=0, workload="gemm_f16_256", gpus=2))
+    d = type("D", (), dict(rank=1, world=2))
+    assert bench.run_reference(args, d) == 0
+    del env
+
+
+def test_clock_summary_window_and_reasons():
+    c = bench.ClockSampler(0)
+    row = lambda mhz, pc: ["0", str(mhz), "2070", "900", "0x0", "Not Active",
+                           "Not Active", "Not Active", pc]
+    c.samples = [(1.0, row(800, "Not Active")), (10.0, row(1800, "Active")),
+                 (11.0, row(1900, "Not Active")), (30.0, row(700, "Not Active"))]
+    s = c.summary(9.9, 11.1)
+    assert s["sm_mhz"] == 1850 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+
+
+def test_workload_meta_algorithmic_figures():
+    w = bench.workload_meta("batched_bf16_16x16x16_b262144_g4_abid1")
+    assert w["algorithmic_bytes"] == 704643072
+    assert w["ops"] == 262144 * 2 * 16 ** 3
+    w = bench.workload_meta("gemm_i8_4096")
+    assert w["ops"] == 2 * 4096 ** 3 and w["unit"] == "TOP/s"
+    assert w["algorithmic_bytes"] == 2 * 4096 ** 2 + 2 * 4 * 4096 ** 2
