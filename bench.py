@@ -231,10 +231,25 @@ def roofline_bound(name, w):
 def kernel_source(w):
     if w["kind"] == "batched":
         return "mixed_precision_dense_02_gb300/csrc/batched16.cu"
+    if w["dtype_in"] == "i8" and not i8_on_tensor_pipe(w):
+        return "mixed_precision_dense_02_gb300/csrc/gemm_i8.cu"
     return {"f16": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
             "bf16": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
-            "i8": "mixed_precision_dense_02_gb300/csrc/gemm_i8.cu",
+            "i8": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
             "f64": "mixed_precision_dense_02_gb300/csrc/gemm_f64.cu"}[w["dtype_in"]]
+
+
+def i8_on_tensor_pipe(w):
+    """INT8 problems with M*N*K >= 2^24 run on the tcgen05 BF16 pipe."""
+    return float(w["M"]) * w["N"] * w["K"] >= 2.0 ** 24
+
+
+def launches_per_call(w):
+    """Kernels one library call launches: the exact-INT8 path adds a
+    conversion kernel before the GEMM; every other path launches one."""
+    if w["kind"] == "gemm" and w["dtype_in"] == "i8" and i8_on_tensor_pipe(w):
+        return 2
+    return 1
 
 
 class GpuWorkload:
@@ -279,7 +294,7 @@ class GpuWorkload:
             self.sets.append((A, B, C, D))
         self.host_D = torch.empty(self.host[2].shape, dtype=self.sets[0][3].dtype,
                                   pin_memory=True)
-        self.launches_per_step = 1
+        self.launches_per_step = launches_per_call(self.w)
 
     def _pinned(self, x):
         import numpy as np

@@ -31,10 +31,17 @@
  *   C, D  M x N row-major:  C[i][j] at C[i*ldc + j],  ldc, ldd >= N
  *
  * Pointers and ownership: A, B, C and D are device pointers owned by the
- * caller; the library keeps no reference to them after the call returns and
- * allocates no memory per call.  C may be NULL (read as zero).  C may equal D
- * (in place) only when ldc == ldd; any other overlap between D and an input
- * is undefined.
+ * caller; the library keeps no reference to them after the call returns.
+ * C may be NULL (read as zero).  C may equal D (in place) only when
+ * ldc == ldd; any other overlap between D and an input is undefined.
+ *
+ * Device memory owned by the library: INT8 products with M*N*K >= 2^24 run
+ * on the BF16 tensor pipe and need (M + N) * roundup(K, 8) * 2 bytes of
+ * scratch for BF16 copies of A and B.  That buffer is allocated once per
+ * device by the first such call, grown (cudaMalloc, after the previous user
+ * finishes) only when a larger problem arrives, and kept until the process
+ * exits; calls on different streams are ordered on it by an event.  Failure
+ * to grow it returns MMA_ERR_NO_MEMORY.  No other call allocates.
  *
  * Alignment: every non-NULL base pointer must be 16-byte aligned and every
  * leading dimension times the element size must be a multiple of 16 bytes
@@ -80,7 +87,8 @@ typedef enum {
   MMA_ERR_MISALIGNED = 3,  /* pointer or leading dimension not 16 B       */
   MMA_ERR_LAUNCH = 4,      /* CUDA reported an error at launch            */
   MMA_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out            */
-  MMA_ERR_NO_DEVICE = 6    /* no usable sm_103 device is current          */
+  MMA_ERR_NO_DEVICE = 6,   /* no usable sm_103 device is current          */
+  MMA_ERR_NO_MEMORY = 7    /* the INT8 scratch buffer could not be grown  */
 } mma_status_t;
 
 /*

@@ -18,7 +18,7 @@ MMA_F16, MMA_BF16, MMA_I8, MMA_F64, MMA_F32, MMA_I32 = 1, 2, 3, 4, 5, 6
 MMA_COL_MAJOR, MMA_ROW_MAJOR = 0, 1
 STATUS = {0: "MMA_OK", 1: "MMA_ERR_INVALID_ARG", 2: "MMA_ERR_UNSUPPORTED",
           3: "MMA_ERR_MISALIGNED", 4: "MMA_ERR_LAUNCH", 5: "MMA_ERR_TIMEOUT",
-          6: "MMA_ERR_NO_DEVICE"}
+          6: "MMA_ERR_NO_DEVICE", 7: "MMA_ERR_NO_MEMORY"}
 
 # The exported entry points and their ctypes signatures (kept in step with
 # include/mma_gb300.h; tests check both lists against the header).

@@ -40,6 +40,19 @@ struct Profile {
 Profile g_prof;
 std::mutex g_prof_mu;
 
+// INT8 scratch: one buffer per device for the BF16 copies of A and B,
+// allocated on the first INT8 call that needs it and grown (never shrunk)
+// when a larger problem arrives; kept until the process exits.  An event
+// records the last call that used it, and a call on another stream waits
+// for that event first, so concurrent calls never share it in flight.
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  cudaEvent_t done = nullptr;
+};
+Workspace g_ws[kMaxDevices];
+std::mutex g_ws_mu;
+
 // Attach the next profiling event pair (if any) to a launch context.
 void attach_profile(Ctx& ctx) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
@@ -129,6 +142,51 @@ using namespace mmagb;
 
 namespace {
 
+// Problems at least this large (M*N*K) take the tcgen05 exact-INT8 path;
+// smaller ones stay on the IMMA kernel, which needs no scratch.
+constexpr double kI8TensorCoreMinWork = 16777216.0;  // 2^24
+
+mma_status_t gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
+                        const int8_t* A, int64_t lda, const int8_t* B,
+                        int64_t ldb, const int32_t* C, int64_t ldc,
+                        int32_t* D, int64_t ldd) {
+  const size_t need = gemm_i8_tc_workspace_bytes(M, N, K);
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  Workspace& w = g_ws[ctx.device];
+  if (!w.done &&
+      cudaEventCreateWithFlags(&w.done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    w.done = nullptr;
+    return MMA_ERR_LAUNCH;
+  }
+  if (w.bytes < need) {
+    if (w.ptr) {
+      if (cudaEventSynchronize(w.done) != cudaSuccess) return MMA_ERR_LAUNCH;
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    const size_t grain = size_t(64) << 20;
+    const size_t bytes = (need + grain - 1) / grain * grain;
+    if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      w.ptr = nullptr;
+      return MMA_ERR_NO_MEMORY;
+    }
+    w.bytes = bytes;
+  }
+  if (cudaStreamWaitEvent(ctx.stream, w.done, 0) != cudaSuccess)
+    return MMA_ERR_LAUNCH;
+  const mma_status_t st =
+      launch_gemm_i8_tc(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, w.ptr);
+  if (cudaEventRecord(w.done, ctx.stream) != cudaSuccess) return MMA_ERR_LAUNCH;
+  return st;
+}
+
+}  // namespace
+
+namespace {
+
 // Element sizes of a supported (dtype_in, dtype_acc) pair, or false.
 bool pair_sizes(int in, int acc, int64_t* in_b, int64_t* acc_b) {
   if ((in == MMA_F16 || in == MMA_BF16) && acc == MMA_F32) {
@@ -192,6 +250,11 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
                                 ldb, static_cast<const float*>(C), ldc,
                                 static_cast<float*>(D), ldd);
     case MMA_I8:
+      if (double(M) * double(N) * double(K) >= kI8TensorCoreMinWork)
+        return gemm_i8_tc(ctx, M, N, K, static_cast<const int8_t*>(A), lda,
+                          static_cast<const int8_t*>(B), ldb,
+                          static_cast<const int32_t*>(C), ldc,
+                          static_cast<int32_t*>(D), ldd);
       return launch_gemm_i8_imma(ctx, M, N, K, static_cast<const int8_t*>(A),
                                  lda, static_cast<const int8_t*>(B), ldb,
                                  static_cast<const int32_t*>(C), ldc,
@@ -316,6 +379,7 @@ extern "C" const char* mma_status_string(int status) {
     case MMA_ERR_LAUNCH: return "MMA_ERR_LAUNCH";
     case MMA_ERR_TIMEOUT: return "MMA_ERR_TIMEOUT";
     case MMA_ERR_NO_DEVICE: return "MMA_ERR_NO_DEVICE";
+    case MMA_ERR_NO_MEMORY: return "MMA_ERR_NO_MEMORY";
     default: return "MMA_ERR_UNKNOWN";
   }
 }

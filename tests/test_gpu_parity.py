@@ -145,6 +145,34 @@ def test_i8_extremes_exact():
         assert np.array_equal(run_gemm(g), C + K * a * b)
 
 
+def test_i8_exact_large_partial_sums_then_unit_steps():
+    """Each 1024-deep K chunk first accumulates 512 products of 2^14 (partial
+    sum 2^23) and then 512 products of +-1, so every unit step must land
+    exactly on a value near 2^23..2^24 -- where FP32 has no spare bits."""
+    M, N, K = 256, 384, 4096
+    rng = np.random.default_rng(77)
+    A = rng.choice(np.array([-1, 1], np.int8), size=(M, K))
+    B = rng.choice(np.array([-1, 1], np.int8), size=(N, K))
+    for k0 in range(0, K, 1024):
+        A[:, k0:k0 + 512] = -128
+        B[:, k0:k0 + 512] = -128
+    A[::7, 1024:1536] = 127          # mixed signs in some rows
+    C = synth.int_uniform(0, 5, M * N, -(1 << 20), 1 << 20).astype(np.int32).reshape(M, N)
+    g = synth.GemmInputs("i8", M, N, K, A, B, C)
+    want, _ = oracle_ref(g)
+    check("i8", run_gemm(g), want, None, "large partial sums then unit steps")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (129, 300, 1025), (513, 257, 3000),
+                                   (1024, 1024, 8192)])
+def test_i8_tensor_pipe_shapes_exact(M, N, K):
+    """Shapes on the tcgen05 exact-INT8 path: ragged tiles, K tails and
+    several K chunks."""
+    g = synth.gemm_inputs(f"i8tc_{M}_{N}_{K}", "i8", M, N, K)
+    want, _ = oracle_ref(g)
+    check("i8", run_gemm(g, pad=1), want, None, f"i8 {M}x{N}x{K}")
+
+
 # ------------------------------------------------------------ batched
 
 def run_batched(bi):
