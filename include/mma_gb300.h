@@ -192,6 +192,36 @@ mma_status_t mma_device_status(void *stream);
 mma_status_t mma_profile_begin(void);
 mma_status_t mma_profile_end(float *ms, int max_count, int *count);
 
+/*
+ * mma_gemm_i8_noalloc -- the exact INT8 -> INT32 product of mma_gemm
+ * (column-major B, same layouts, alignment, C handling and status codes),
+ * computed on the tensor pipe without allocating any device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot let a library allocate device memory.  mma_gemm grows a scratch
+ * buffer with cudaMalloc for large INT8 problems; a program whose pool
+ * allocator has already reserved the memory it may use, or a service that
+ * forbids allocation after start-up (cudaMalloc/cudaFree can block and
+ * synchronise the device), calls this instead.  Its scratch is a fixed
+ * array of MMA_NOALLOC_SCRATCH_BYTES in the library's device image, held by
+ * every GPU that loads the library until the process exits.
+ *
+ * Limit: (M + N) * roundup(K, 8) * 2 bytes must fit in
+ * MMA_NOALLOC_SCRATCH_BYTES (for example M = N = K = 4096); larger problems
+ * return MMA_ERR_UNSUPPORTED and launch nothing.
+ * Set-up: the first call on each device, made with that device current,
+ * looks up the array's device address (cudaGetSymbolAddress) and caches it;
+ * make that first call before any stream capture begins.
+ * Sharing: all calls on a device use the same array and leave their data in
+ * it (nothing there needs to start at zero); calls whose work overlaps on
+ * the GPU race on it, so order calls issued on different streams.
+ */
+#define MMA_NOALLOC_SCRATCH_BYTES (64u << 20)
+mma_status_t mma_gemm_i8_noalloc(int64_t M, int64_t N, int64_t K,
+                                 const void *A, int64_t lda, const void *B,
+                                 int64_t ldb, const void *C, int64_t ldc,
+                                 void *D, int64_t ldd, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mma_status_string(int status);
 

@@ -31,6 +31,8 @@ SIGNATURES = {
     "mma_gemm_batched": (_int, [_int, _int, _i64, _i64, _i64, _p, _i64, _p,
                                 _i64, _p, _i64, _p, _i64, _i64, _int, _int,
                                 _p]),
+    "mma_gemm_i8_noalloc": (_int, [_i64, _i64, _i64, _p, _i64, _p, _i64, _p,
+                                   _i64, _p, _i64, _p]),
     "mma_device_status": (_int, [_p]),
     "mma_profile_begin": (_int, []),
     "mma_profile_end": (_int, [ctypes.POINTER(ctypes.c_float), _int,
@@ -99,6 +101,13 @@ def mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C, ldc, D,
     return load().mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B,
                                    ldb, C, ldc, D, ldd, batch, group, abid,
                                    stream)
+
+
+def mma_gemm_i8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd,
+                        stream) -> int:
+    """INT8 -> INT32 GEMM that allocates no device memory (fixed scratch)."""
+    return load().mma_gemm_i8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd,
+                                      stream)
 
 
 def mma_device_status(stream) -> int:

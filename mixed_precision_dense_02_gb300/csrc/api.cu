@@ -125,6 +125,15 @@ __global__ void copy_c_kernel(const uint8_t* __restrict__ C, int64_t ldc_b,
 
 }  // namespace
 
+bool current_ctx(void* stream, Ctx* out) {
+  int dev = -1;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info) return false;
+  *out = Ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms,
+             info->status};
+  return true;
+}
+
 mma_status_t launch_copy_c(const Ctx& ctx, int64_t M, int64_t N,
                            int elem_bytes, const void* C, int64_t ldc, void* D,
                            int64_t ldd) {

@@ -62,6 +62,10 @@ mma_status_t launch_batched16(const Ctx& ctx, bool bf16, int64_t batch,
                               int group, int abid, const void* A,
                               const void* B, const float* C, float* D);
 
+// Launch context for the current device (false if it is not a usable
+// sm_103 device).
+bool current_ctx(void* stream, Ctx* out);
+
 // K == 0: D = C (or 0), elementwise, element size 4 or 8 bytes.
 mma_status_t launch_copy_c(const Ctx& ctx, int64_t M, int64_t N,
                            int elem_bytes, const void* C, int64_t ldc, void* D,
