@@ -27,6 +27,7 @@
 // add nothing to the sum) and the epilogue predicates its stores.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "kernels.h"
@@ -57,16 +58,25 @@ enum class Epi { F32, I32EXACT };
 // integers.
 constexpr int kI8ChunkK = 1024;
 
-template <int BN, int STAGES>
+// Epilogue staging: each epilogue warp owns two 32-row x 16-column FP32
+// blocks (64-byte rows, 64-byte TMA swizzle) through which C arrives and D
+// leaves by TMA.
+constexpr int kStgBytes = 32 * 16 * 4;
+
+// CL = 2: each CTA of a pair stages its own half of the B box.
+template <int BN, int STAGES, int CL>
 struct Layout {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (BN / CL) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int STG_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFFSET = STG_OFFSET + kEpiWarps * 2 * kStgBytes;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kEpiWarps;
   static constexpr int TOTAL = BAR_OFFSET + NUM_BARS * 8 + 16;
   static constexpr int ALLOC = TOTAL + 1024;  // room to align the base
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  // two accumulators of BN columns, rounded up to a power of two
+  static constexpr uint32_t TMEM_COLS =
+      2 * BN <= 256 ? 256u : 512u;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n,
@@ -93,14 +103,29 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity,
   }
 }
 
-template <int BN, int STAGES, bool BF16, Epi EPI>
+// 320 threads (10 warps, so three share an SM sub-partition's 16K
+// registers): at most 168 registers per thread.
+//
+// CL = 2 runs one MMA over a pair of CTAs (a cluster of two SMs): the
+// pair computes a 256 x BN tile with tcgen05.mma.cta_group::2, each CTA
+// holding 128 rows of A, half (BN/2 rows) of B and its 128 rows of the
+// accumulator.  Per K step each SM stages 128 + BN/2 operand rows instead
+// of 128 + BN, which cuts the shared-memory traffic (TMA writes plus MMA
+// reads) that bounds the single-CTA kernel.  Both CTAs' loads complete on
+// the leader CTA's (rank 0) full barrier; the leader's one MMA thread
+// issues the pair's MMAs, whose commits release the stage in both CTAs and
+// announce the accumulator to both CTAs' epilogues; every epilogue warp of
+// the pair returns the accumulator on the leader's tempty barrier.
+template <int BN, int STAGES, bool BF16, Epi EPI, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmD,
                    const void* __restrict__ Cv, int64_t ldc,
                    void* __restrict__ Dv, int64_t ldd, int M, int N, int K,
                    int kb_per_chunk, unsigned* status) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, CL>;
   constexpr int HALF = BN / 2;  // columns per epilogue warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -110,13 +135,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* cbar = done + 1;  // two per epilogue warp: C block landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 2 * kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;
-  const int tiles = num_m * num_n;
+  // Work units: CL vertically adjacent tiles per cluster.  The CTA of rank
+  // r in its cluster takes m-block (unit row) * CL + r.
+  const int unit_m = (num_m + CL - 1) / CL;
+  const int units = unit_m * num_n;
+  const int first_unit = blockIdx.x / CL;
+  const int unit_step = gridDim.x / CL;
+  const int rank = CL > 1 ? int(cluster_ctarank()) : 0;
   const int num_kb = (K + BK - 1) / BK;
   const int kpc = EPI == Epi::F32 ? num_kb : kb_per_chunk;
   const int chunks = (num_kb + kpc - 1) / kpc;
@@ -128,9 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiThreads);
+      mbar_init(&tempty[a], CL * kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(done, 1);
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&cbar[i], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -138,13 +171,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane_id() == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+    if (Cv) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, L::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CL == 1) {
+      tmem_alloc(tmem_slot, L::TMEM_COLS);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL > 1)
+    cluster_sync();  // the peer's barriers exist before anything targets them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -155,18 +198,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        int mb, nb;
-        tile_coords(t, num_m, num_n, mb, nb);
+      // the leader CTA's full barriers, which count both CTAs' bytes
+      const uint32_t full_lead =
+          CL > 1 ? mapa_shared(smem_u32(&full[0]), 0) : 0u;
+      for (int u = first_unit; u < units && ok; u += unit_step) {
+        int mu, nb;
+        tile_coords(u, unit_m, num_n, mu, nb);
+        const int mb = mu * CL + rank;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + stage * L::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-          tma_load_2d(&tmA, &full[stage], sa, kb * BK, mb * BM);
-          tma_load_2d(&tmB, &full[stage], sa + L::A_BYTES, kb * BK, nb * BN);
+          if constexpr (CL == 1) {
+            mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            tma_load_2d(&tmA, &full[stage], sa, kb * BK, mb * BM);
+            tma_load_2d(&tmB, &full[stage], sa + L::A_BYTES, kb * BK, nb * BN);
+          } else {
+            // the leader expects the bytes of both CTAs' stage
+            if (rank == 0)
+              mbar_arrive_expect_tx(&full[stage], CL * L::STAGE_BYTES);
+            const uint32_t fb = full_lead + uint32_t(stage) * 8u;
+            tma_load_2d_pair(&tmA, fb, sa, kb * BK, mb * BM);
+            tma_load_2d_pair(&tmB, fb, sa + L::A_BYTES, kb * BK,
+                             nb * BN + rank * (BN / CL));
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -174,24 +231,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
-        // Let every load still in flight land before the CTA exits.
-        for (int s = 0; s < STAGES; ++s) {
-          const uint32_t fills = issued / STAGES + (uint32_t(s) < issued % STAGES);
-          if (fills) mbar_wait_drain(&full[s], (fills - 1) & 1u, status);
-        }
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t fills = issued / STAGES + (uint32_t(s) < issued % STAGES);
+        if (!fills) continue;
+        // Let every load still in flight land before the CTA exits (the
+        // leader's full barriers also count the peer's loads).
+        if (!ok && rank == 0)
+          mbar_wait_drain(&full[s], (fills - 1) & 1u, status);
+        // With a pair, the last release of each stage is the leader's
+        // commit; wait until it has arrived on this CTA.
+        if (CL > 1) mbar_wait_drain(&empty[s], (fills - 1) & 1u, status);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (elect_one()) {
-      constexpr uint32_t idesc = idesc_f16_f32(BF16, BM, BN);
+    // (with a pair, only the leader CTA issues)
+    if (rank == 0 && elect_one()) {
+      constexpr uint32_t idesc = idesc_f16_f32(BF16, BM * CL, BN);
+      constexpr uint16_t kPairMask = 3u;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int u = first_unit; u < units && ok; u += unit_step) {
         for (int ch = 0; ch < chunks && ok; ++ch) {
           if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) {
             ok = false;
@@ -213,45 +277,113 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
               // advance 16 elements (32 bytes) along K inside the swizzle row
-              umma_f16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k),
-                       idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+              const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+              if constexpr (CL == 1)
+                umma_f16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k),
+                         idesc, accum);
+              else
+                umma_f16_pair(d_tmem, da + uint64_t(2 * k),
+                              db + uint64_t(2 * k), idesc, accum);
             }
-            umma_commit(&empty[stage]);
+            if constexpr (CL == 1)
+              umma_commit(&empty[stage]);
+            else
+              umma_commit_pair(&empty[stage], kPairMask);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(&tfull[acc]);
+          if constexpr (CL == 1)
+            umma_commit(&tfull[acc]);
+          else
+            umma_commit_pair(&tfull[acc], kPairMask);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
       // Every MMA issued above completes before tensor memory is released.
-      umma_commit(done);
+      if constexpr (CL == 1)
+        umma_commit(done);
+      else
+        umma_commit_pair(done, 1u);
       mbar_wait_drain(done, 0, status);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------ epilogue warps
+    // Each warp owns a 32-row quarter of the tile (its TMEM lane quarter)
+    // and one column half.  D leaves through the warp's two staging blocks
+    // by TMA store (coalesced, asynchronous); in FP32 mode C arrives the
+    // same way, one block ahead of its use.  The INT32 sums of the exact
+    // mode start from C fetched at the start of the tile.
     const int ew = warp - 2;           // 0 .. 7
     const int q = warp & 3;            // tensor-memory lane quarter
     const int h = ew >> 2;             // column half of the tile
     const int lane = threadIdx.x & 31;
+    uint8_t* stg = smem + L::STG_OFFSET + ew * 2 * kStgBytes;
+    uint64_t* wbar = &cbar[2 * ew];
+    const bool has_c = Cv != nullptr;
+    constexpr int NBLK = HALF / 16;
+    uint32_t sb = 0;  // staging blocks used so far by this warp
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      int mb, nb;
-      tile_coords(t, num_m, num_n, mb, nb);
-      const int row = mb * BM + q * 32 + lane;
-      const int colh = nb * BN + h * HALF;  // first column of this half
-      [[maybe_unused]] uint32_t iacc[EPI == Epi::I32EXACT ? HALF : 1];
-      if constexpr (EPI == Epi::I32EXACT) {
-#pragma unroll
-        for (int j = 0; j < HALF; ++j) iacc[j] = 0u;
+    // Row `lane` of a staging block, 16-byte chunk c, 64-byte swizzle.
+    auto chunk = [&](uint8_t* buf, int c) {
+      return reinterpret_cast<uint4*>(buf + lane * 64 +
+                                      ((c ^ ((lane >> 1) & 3)) << 4));
+    };
+    // Return accumulator buffer `a` to the MMA issuer once this warp's TMEM
+    // reads of it are complete (to the leader CTA's barrier for a pair).
+    auto release_acc = [&](int a) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CL == 1)
+          mbar_arrive(&tempty[a]);
+        else
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[a]), 0));
       }
-      for (int ch = 0; ch < chunks; ++ch) {
+    };
+    // Store staging block `buf` to D at (col, row0), or close an empty
+    // bulk group when the block lies wholly outside D.
+    auto store_block = [&](uint8_t* buf, int col, int row0) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (col < N && row0 < M) tma_store_2d(&tmD, buf, col, row0);
+        bulk_commit_group();
+      }
+      __syncwarp();
+    };
+    for (int u = first_unit; u < units && ok; u += unit_step) {
+      int mu, nb;
+      tile_coords(u, unit_m, num_n, mu, nb);
+      const int row0 = (mu * CL + rank) * BM + q * 32;
+      const int row = row0 + lane;
+      const int colh = nb * BN + h * HALF;  // first column of this half
+      const bool row_ok = row < M;
+      if constexpr (EPI == Epi::F32) {
+        // C block j goes to staging buffer (sb + j) & 1, whose previous
+        // store must have finished reading it.
+        auto fetch_c = [&](int j) {
+          const uint32_t b = (sb + j) & 1u;
+          if (row0 < M && colh + j * 16 < N) {
+            mbar_arrive_expect_tx(&wbar[b], kStgBytes);
+            tma_load_2d(&tmC, &wbar[b], stg + b * kStgBytes, colh + j * 16,
+                        row0);
+          } else {
+            // wholly outside C (and D): nothing to load or store
+            mbar_arrive(&wbar[b]);
+          }
+        };
+        if (has_c && lane == 0) {
+          bulk_wait_group_read<1>();
+          fetch_c(0);
+        }
+        __syncwarp();
         ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -260,125 +392,195 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
                                (uint32_t(q * 32) << 16);
-        if constexpr (EPI == Epi::F32) {
-          const float* C = static_cast<const float*>(Cv);
-          float* D = static_cast<float*>(Dv);
 #pragma unroll 1
-          for (int c = 0; c < HALF / 32; ++c) {
-            const int col0 = colh + c * 32;
-            if (col0 >= N) break;
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
-            tmem_ld_wait();
-            if (row < M) {
-              float* drow = D + int64_t(row) * ldd + col0;
-              const float* crow = C ? C + int64_t(row) * ldc + col0 : nullptr;
-              if (col0 + 32 <= N) {
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                  float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
-                  if (crow) cv = __ldg(reinterpret_cast<const float4*>(crow) + v);
-                  float4 o;
-                  o.x = __uint_as_float(r[4 * v + 0]) + cv.x;
-                  o.y = __uint_as_float(r[4 * v + 1]) + cv.y;
-                  o.z = __uint_as_float(r[4 * v + 2]) + cv.z;
-                  o.w = __uint_as_float(r[4 * v + 3]) + cv.w;
-                  reinterpret_cast<float4*>(drow)[v] = o;
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  if (col0 + j < N)
-                    drow[j] = __uint_as_float(r[j]) + (crow ? crow[j] : 0.f);
-                }
+        for (int j = 0; j < NBLK; ++j) {
+          const uint32_t g = sb + uint32_t(j);
+          uint8_t* buf = stg + (g & 1u) * kStgBytes;
+          if (lane == 0) {
+            if (has_c) {
+              if (j + 1 < NBLK) {
+                bulk_wait_group_read<0>();
+                fetch_c(j + 1);
               }
+            } else {
+              bulk_wait_group_read<1>();
             }
+          }
+          __syncwarp();
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
+          tmem_ld_wait();
+          // every TMEM read of this accumulator is done: release it
+          if (j == NBLK - 1) release_acc(acc);
+          if (has_c) {
+            ok = mbar_wait(&wbar[g & 1u], (g >> 1) & 1u, abort_flag, status);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4* p = chunk(buf, c);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has_c) {
+              const uint4 w = *p;
+              v = make_float4(__uint_as_float(w.x), __uint_as_float(w.y),
+                              __uint_as_float(w.z), __uint_as_float(w.w));
+            }
+            v.x += __uint_as_float(r[4 * c + 0]);
+            v.y += __uint_as_float(r[4 * c + 1]);
+            v.z += __uint_as_float(r[4 * c + 2]);
+            v.w += __uint_as_float(r[4 * c + 3]);
+            *p = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y),
+                            __float_as_uint(v.z), __float_as_uint(v.w));
+          }
+          store_block(buf, colh + j * 16, row0);
+        }
+        sb += NBLK;
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      } else {
+        const int32_t* C = static_cast<const int32_t*>(Cv);
+        const int32_t* crow =
+            (C && row_ok) ? C + int64_t(row) * ldc + colh : nullptr;
+        // The INT32 sums start from C, fetched before the first chunk.
+        uint32_t iacc[HALF];
+        if (crow && colh + HALF <= N) {
+#pragma unroll
+          for (int v = 0; v < HALF / 4; ++v) {
+            const int4 cv = __ldcs(reinterpret_cast<const int4*>(crow) + v);
+            iacc[4 * v + 0] = uint32_t(cv.x);
+            iacc[4 * v + 1] = uint32_t(cv.y);
+            iacc[4 * v + 2] = uint32_t(cv.z);
+            iacc[4 * v + 3] = uint32_t(cv.w);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < HALF / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
+          for (int j = 0; j < HALF; ++j)
+            iacc[j] = (crow && colh + j < N) ? uint32_t(crow[j]) : 0u;
+        }
+        for (int ch = 0; ch < chunks; ++ch) {
+          ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
+                                 (uint32_t(q * 32) << 16);
+#pragma unroll
+          for (int c = 0; c < HALF / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(taddr + uint32_t(c * 16), r);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              iacc[c * 32 + j] += uint32_t(__float2int_rn(__uint_as_float(r[j])));
+            for (int j = 0; j < 16; ++j)
+              iacc[c * 16 + j] += uint32_t(__float2int_rn(__uint_as_float(r[j])));
           }
+          release_acc(acc);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      }
-      if constexpr (EPI == Epi::I32EXACT) {
-        if (ok && row < M) {
-          const int32_t* C = static_cast<const int32_t*>(Cv);
-          int32_t* D = static_cast<int32_t*>(Dv);
-          int32_t* drow = D + int64_t(row) * ldd + colh;
-          const int32_t* crow = C ? C + int64_t(row) * ldc + colh : nullptr;
-          if (colh + HALF <= N) {
+        if (!ok) break;
 #pragma unroll
-            for (int v = 0; v < HALF / 4; ++v) {
-              int4 cv = make_int4(0, 0, 0, 0);
-              if (crow) cv = __ldg(reinterpret_cast<const int4*>(crow) + v);
-              int4 o;
-              o.x = int32_t(iacc[4 * v + 0] + uint32_t(cv.x));
-              o.y = int32_t(iacc[4 * v + 1] + uint32_t(cv.y));
-              o.z = int32_t(iacc[4 * v + 2] + uint32_t(cv.z));
-              o.w = int32_t(iacc[4 * v + 3] + uint32_t(cv.w));
-              reinterpret_cast<int4*>(drow)[v] = o;
-            }
-          } else {
+        for (int j = 0; j < NBLK; ++j) {
+          uint8_t* buf = stg + ((sb + uint32_t(j)) & 1u) * kStgBytes;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) {
-              if (colh + j < N)
-                drow[j] = int32_t(iacc[j] + uint32_t(crow ? crow[j] : 0));
-            }
-          }
+          for (int c = 0; c < 4; ++c)
+            *chunk(buf, c) = make_uint4(iacc[j * 16 + 4 * c + 0],
+                                        iacc[j * 16 + 4 * c + 1],
+                                        iacc[j * 16 + 4 * c + 2],
+                                        iacc[j * 16 + 4 * c + 3]);
+          store_block(buf, colh + j * 16, row0);
         }
+        sb += NBLK;
       }
     }
+    // every store of this warp has landed before the CTA finishes
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL > 1)
+    cluster_sync();  // neither CTA leaves while the other may still signal it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, L::TMEM_COLS);
+    if constexpr (CL == 1)
+      tmem_dealloc(tmem_base, L::TMEM_COLS);
+    else
+      tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
   }
 }
 
 // int8 -> bfloat16 (exact: every int8 value has at most 8 significant bits).
-// One flat index over 16-byte chunks of the rows of A then of B.
-__global__ void __launch_bounds__(256)
+__device__ __forceinline__ void i8x16_to_bf16(const int4 v, uint4& o0, uint4& o1) {
+  const uint32_t w[4] = {uint32_t(v.x), uint32_t(v.y), uint32_t(v.z),
+                         uint32_t(v.w)};
+  uint32_t o[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int lo = int(int8_t((w[j >> 1] >> (16 * (j & 1))) & 0xFF));
+    const int hi = int(int8_t((w[j >> 1] >> (16 * (j & 1) + 8)) & 0xFF));
+    o[j] = (__float_as_uint(float(lo)) >> 16) |
+           (__float_as_uint(float(hi)) & 0xFFFF0000u);
+  }
+  o0 = make_uint4(o[0], o[1], o[2], o[3]);
+  o1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// One flat index over the 16-byte chunks of the rows of A then of B.  Each
+// block takes 4 x 256 consecutive chunks, thread t the chunks t, t + 256,
+// t + 512 and t + 768 of them: the four loads are in flight together and
+// every warp-wide load and store covers one contiguous run of memory.
+constexpr int kConvThreads = 256;
+constexpr int kConvUnroll = 4;
+
+__global__ void __launch_bounds__(kConvThreads)
     i8_to_bf16_kernel(const int8_t* __restrict__ A, int64_t lda, int M,
                       const int8_t* __restrict__ B, int64_t ldb, int N, int K,
                       uint16_t* __restrict__ W, int64_t ldw) {
   const int64_t cpr = (K + 15) / 16;  // chunks per row
   const int64_t total = int64_t(M + N) * cpr;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = i / cpr;
-    const int c = int(i - r * cpr) * 16;
-    const int8_t* src = r < M ? A + r * lda + c : B + (r - M) * ldb + c;
-    uint16_t* dst = W + r * ldw + c;
-    if (c + 16 <= K) {
-      const int4 v = __ldcs(reinterpret_cast<const int4*>(src));
-      const uint32_t w[4] = {uint32_t(v.x), uint32_t(v.y), uint32_t(v.z),
-                             uint32_t(v.w)};
-      uint32_t o[8];
+  constexpr int64_t kSpan = int64_t(kConvThreads) * kConvUnroll;
+  for (int64_t base = int64_t(blockIdx.x) * kSpan; base < total;
+       base += int64_t(gridDim.x) * kSpan) {
+    int4 v[kConvUnroll];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int lo = int(int8_t((w[j >> 1] >> (16 * (j & 1))) & 0xFF));
-        const int hi = int(int8_t((w[j >> 1] >> (16 * (j & 1) + 8)) & 0xFF));
-        o[j] = (__float_as_uint(float(lo)) >> 16) |
-               (__float_as_uint(float(hi)) & 0xFFFF0000u);
+    for (int u = 0; u < kConvUnroll; ++u) {
+      const int64_t i = base + threadIdx.x + int64_t(u) * kConvThreads;
+      v[u] = make_int4(0, 0, 0, 0);
+      if (i < total) {
+        const int64_t r = i / cpr;
+        const int c = int(i - r * cpr) * 16;
+        if (c + 16 <= K) {
+          const int8_t* src = r < M ? A + r * lda + c : B + (r - M) * ldb + c;
+          v[u] = __ldcs(reinterpret_cast<const int4*>(src));
+        }
       }
-      reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-    } else {
-      for (int j = 0; c + j < K; ++j)
-        dst[j] = uint16_t(__float_as_uint(float(src[j])) >> 16);
+    }
+#pragma unroll
+    for (int u = 0; u < kConvUnroll; ++u) {
+      const int64_t i = base + threadIdx.x + int64_t(u) * kConvThreads;
+      if (i >= total) continue;
+      const int64_t r = i / cpr;
+      const int c = int(i - r * cpr) * 16;
+      uint16_t* dst = W + r * ldw + c;
+      if (c + 16 <= K) {
+        uint4 o0, o1;
+        i8x16_to_bf16(v[u], o0, o1);
+        reinterpret_cast<uint4*>(dst)[0] = o0;
+        reinterpret_cast<uint4*>(dst)[1] = o1;
+      } else {
+        const int8_t* src = r < M ? A + r * lda + c : B + (r - M) * ldb + c;
+        for (int j = 0; c + j < K; ++j)
+          dst[j] = uint16_t(__float_as_uint(float(src[j])) >> 16);
+      }
     }
   }
 }
@@ -420,33 +622,131 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t K,
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool BF16, Epi EPI>
+// 2-D row-major C/D map (4-byte elements): 16 x 32 box, 64-byte swizzle,
+// matching the epilogue's staging blocks.
+bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
+                 int64_t ld_elems, bool is_int) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(M)};
+  cuuint64_t strides[1] = {cuuint64_t(ld_elems) * 4};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map,
+                   is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool BF16, Epi EPI, int CL>
 mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd) {
-  using L = Layout<BN, STAGES>;
-  CUtensorMap ta, tb;
+  using L = Layout<BN, STAGES, CL>;
+  constexpr bool kInt = EPI == Epi::I32EXACT;
+  CUtensorMap ta, tb, tc, td;
   if (!make_kmajor_map(&ta, A, K, M, lda, BM, BF16) ||
-      !make_kmajor_map(&tb, B, K, N, ldb, BN, BF16))
+      !make_kmajor_map(&tb, B, K, N, ldb, BN / CL, BF16) ||
+      !make_cd_map(&td, D, N, M, ldd, kInt))
     return MMA_ERR_LAUNCH;
-  auto kern = gemm_tc_kernel<BN, STAGES, BF16, EPI>;
+  if (C != nullptr) {
+    if (!make_cd_map(&tc, C, N, M, ldc, kInt)) return MMA_ERR_LAUNCH;
+  } else {
+    tc = td;  // never read: the kernel loads C only when it is given
+  }
+  auto kern = gemm_tc_kernel<BN, STAGES, BF16, EPI, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::ALLOC) != cudaSuccess)
     return MMA_ERR_LAUNCH;
-  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = int(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  const int64_t units = ((M + BM * CL - 1) / (BM * CL)) * ((N + BN - 1) / BN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: as many clusters as can be resident at once (at most one
+  // per unit of work)
+  int64_t clusters = ctx.num_sms / CL;
+  if (CL > 1) {
+    static int resident[64] = {};
+    int& r = resident[ctx.device & 63];
+    if (r == 0) {
+      cfg.gridDim = dim3(unsigned(CL * (ctx.num_sms / CL)), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return MMA_ERR_LAUNCH;
+      }
+      r = n;
+    }
+    clusters = r;
+  }
+  if (clusters > units) clusters = units;
+  cfg.gridDim = dim3(unsigned(clusters * CL), 1, 1);
   ctx.mark_start();
-  kern<<<grid, kThreads, L::ALLOC, ctx.stream>>>(ta, tb, C, ldc, D, ldd,
-                                                 int(M), int(N), int(K),
-                                                 kI8ChunkK / BK, ctx.status);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, C, ldc, D, ldd, int(M), int(N),
+                         int(K), kI8ChunkK / BK, ctx.status);
   ctx.mark_stop();
-  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MMA_ERR_LAUNCH;
+  }
+  return MMA_OK;
 }
 
-// Wide tiles when there are enough of them to fill the chip, else narrow.
-bool use_wide(const Ctx& ctx, int64_t M, int64_t N) {
+// Cluster size: CTA pairs sharing one MMA (cta_group::2) for problems large
+// enough to keep many pairs busy (at least two m-blocks); single CTAs
+// otherwise.
+// MMA_GB300_CLUSTER (1 or 2) overrides the choice, for tuning.
+int cluster_size(int64_t M, int64_t N, int64_t K) {
+  static const int forced = [] {
+    const char* e = getenv("MMA_GB300_CLUSTER");
+    const int v = e ? atoi(e) : 0;
+    return (v == 1 || v == 2) ? v : 0;
+  }();
+  if (forced) return forced;
+  const double work = double(M) * double(N) * double(K);
+  return (M > BM && work >= 1073741824.0) ? 2 : 1;
+}
+
+template <bool BF16, Epi EPI>
+mma_status_t dispatch(const Ctx& ctx, int bn, int cl, int64_t M, int64_t N,
+                      int64_t K, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, const void* C, int64_t ldc, void* D,
+                      int64_t ldd) {
+  // stages: 192 KB of operand ring (a pair stages half of B per CTA)
+  if (bn == 256)
+    return cl == 2 ? run<256, 6, BF16, EPI, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
+                   : run<256, 4, BF16, EPI, 1>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+  return cl == 2 ? run<128, 8, BF16, EPI, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
+                 : run<128, 6, BF16, EPI, 1>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+}
+
+// Tile width (columns of D per CTA): 256 when there are enough such tiles
+// to occupy every SM, else 128 (more, smaller tiles).  Measured on the
+// INT8 4096^3, BF16 8192^3 and 16384 x 128 x 4096 workloads, 256-wide tiles
+// beat 192 and 128 wherever they fill the chip.  MMA_GB300_TILE_N (128 or
+// 256) overrides the choice, for tuning.
+int tile_n(const Ctx& ctx, int64_t M, int64_t N) {
+  static const int forced = [] {
+    const char* e = getenv("MMA_GB300_TILE_N");
+    const int v = e ? atoi(e) : 0;
+    return (v == 128 || v == 256) ? v : 0;
+  }();
+  if (forced) return forced;
   const int64_t wide_tiles = ((M + BM - 1) / BM) * ((N + 255) / 256);
-  return N > 128 && wide_tiles >= ctx.num_sms;
+  return (N > 128 && wide_tiles >= ctx.num_sms) ? 256 : 128;
 }
 
 }  // namespace
@@ -456,12 +756,12 @@ mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, int64_t M,
                                 int64_t lda, const void* B, int64_t ldb,
                                 const float* C, int64_t ldc, float* D,
                                 int64_t ldd) {
-  const bool wide = use_wide(ctx, M, N);
-  if (bf16)
-    return wide ? run<256, 4, true, Epi::F32>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-                : run<128, 6, true, Epi::F32>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
-  return wide ? run<256, 4, false, Epi::F32>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-              : run<128, 6, false, Epi::F32>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+  const int bn = tile_n(ctx, M, N);
+  const int cl = cluster_size(M, N, K);
+  return bf16 ? dispatch<true, Epi::F32>(ctx, bn, cl, M, N, K, A, lda, B, ldb,
+                                         C, ldc, D, ldd)
+              : dispatch<false, Epi::F32>(ctx, bn, cl, M, N, K, A, lda, B, ldb,
+                                          C, ldc, D, ldd);
 }
 
 size_t gemm_i8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -477,18 +777,17 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
   const int64_t ldw = (K + 7) / 8 * 8;
   uint16_t* W = static_cast<uint16_t*>(workspace);
   const int64_t chunks = (M + N) * ((K + 15) / 16);
-  int64_t blocks = (chunks + 255) / 256;
-  if (blocks > int64_t(ctx.num_sms) * 16) blocks = int64_t(ctx.num_sms) * 16;
-  i8_to_bf16_kernel<<<int(blocks), 256, 0, ctx.stream>>>(
+  const int64_t span = int64_t(kConvThreads) * kConvUnroll;
+  int64_t blocks = (chunks + span - 1) / span;
+  if (blocks > int64_t(ctx.num_sms) * 8) blocks = int64_t(ctx.num_sms) * 8;
+  i8_to_bf16_kernel<<<int(blocks), kConvThreads, 0, ctx.stream>>>(
       A, lda, int(M), B, ldb, int(N), int(K), W, ldw);
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
   const uint16_t* Aw = W;
   const uint16_t* Bw = W + M * ldw;
-  return use_wide(ctx, M, N)
-             ? run<256, 4, true, Epi::I32EXACT>(ctx, M, N, K, Aw, ldw, Bw, ldw,
-                                                C, ldc, D, ldd)
-             : run<128, 6, true, Epi::I32EXACT>(ctx, M, N, K, Aw, ldw, Bw, ldw,
-                                                C, ldc, D, ldd);
+  return dispatch<true, Epi::I32EXACT>(ctx, tile_n(ctx, M, N),
+                                       cluster_size(M, N, K), M, N, K, Aw, ldw,
+                                       Bw, ldw, C, ldc, D, ldd);
 }
 
 }  // namespace mmagb
