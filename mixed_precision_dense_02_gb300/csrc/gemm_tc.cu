@@ -201,6 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the leader CTA's full barriers, which count both CTAs' bytes
       const uint32_t full_lead =
           CL > 1 ? mapa_shared(smem_u32(&full[0]), 0) : 0u;
+      // A and B may be produced by the kernel launched just before this one
+      // (the INT8 widening pass, launched as a programmatic dependency):
+      // only the operand loads wait for it; the rest of the prologue and
+      // the epilogue's C prefetch overlap its tail.
+      grid_dependency_wait();
       for (int u = first_unit; u < units && ok; u += unit_step) {
         int mu, nb;
         tile_coords(u, unit_m, num_n, mu, nb);
@@ -315,9 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue warps
     // Each warp owns a 32-row quarter of the tile (its TMEM lane quarter)
     // and one column half.  D leaves through the warp's two staging blocks
-    // by TMA store (coalesced, asynchronous); in FP32 mode C arrives the
-    // same way, one block ahead of its use.  The INT32 sums of the exact
-    // mode start from C fetched at the start of the tile.
+    // by TMA store (coalesced, asynchronous).  In FP32 mode C arrives the
+    // same way, one block ahead of its use.  In the exact INT8 mode the
+    // INT32 sums of the chunks are kept in registers, starting from C
+    // fetched at the start of the tile (hidden behind the first chunk's
+    // MMAs).  (Accumulating the chunks into D with TMA reduce-add instead
+    // was measured slower: the L2 atomics cost more than the registers.)
     const int ew = warp - 2;           // 0 .. 7
     const int q = warp & 3;            // tensor-memory lane quarter
     const int h = ew >> 2;             // column half of the tile
@@ -349,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Store staging block `buf` to D at (col, row0), or close an empty
     // bulk group when the block lies wholly outside D.
-    auto store_block = [&](uint8_t* buf, int col, int row0) {
+    auto emit_block = [&](uint8_t* buf, int col, int row0) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -362,10 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mu, nb;
       tile_coords(u, unit_m, num_n, mu, nb);
       const int row0 = (mu * CL + rank) * BM + q * 32;
-      const int row = row0 + lane;
       const int colh = nb * BN + h * HALF;  // first column of this half
-      const bool row_ok = row < M;
       if constexpr (EPI == Epi::F32) {
+        // one chunk per tile: the whole K loop in one accumulator
+        const bool use_c = has_c;
         // C block j goes to staging buffer (sb + j) & 1, whose previous
         // store must have finished reading it.
         auto fetch_c = [&](int j) {
@@ -379,16 +387,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&wbar[b]);
           }
         };
-        if (has_c && lane == 0) {
-          bulk_wait_group_read<1>();
-          fetch_c(0);
+        if (lane == 0) {
+          if (use_c) {
+            bulk_wait_group_read<1>();
+            fetch_c(0);
+          }
         }
         __syncwarp();
         ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
+        if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
                                (uint32_t(q * 32) << 16);
@@ -397,12 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t g = sb + uint32_t(j);
           uint8_t* buf = stg + (g & 1u) * kStgBytes;
           if (lane == 0) {
-            if (has_c) {
-              if (j + 1 < NBLK) {
-                bulk_wait_group_read<0>();
-                fetch_c(j + 1);
-              }
-            } else {
+            if (use_c && j + 1 < NBLK) {
+              bulk_wait_group_read<0>();
+              fetch_c(j + 1);
+            } else if (!use_c) {
               bulk_wait_group_read<1>();
             }
           }
@@ -412,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           // every TMEM read of this accumulator is done: release it
           if (j == NBLK - 1) release_acc(acc);
-          if (has_c) {
+          if (use_c) {
             ok = mbar_wait(&wbar[g & 1u], (g >> 1) & 1u, abort_flag, status);
             if (!__all_sync(0xffffffffu, ok)) {
               ok = false;
@@ -422,25 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint4* p = chunk(buf, c);
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has_c) {
-              const uint4 w = *p;
-              v = make_float4(__uint_as_float(w.x), __uint_as_float(w.y),
-                              __uint_as_float(w.z), __uint_as_float(w.w));
-            }
-            v.x += __uint_as_float(r[4 * c + 0]);
-            v.y += __uint_as_float(r[4 * c + 1]);
-            v.z += __uint_as_float(r[4 * c + 2]);
-            v.w += __uint_as_float(r[4 * c + 3]);
-            *p = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y),
-                            __float_as_uint(v.z), __float_as_uint(v.w));
+            const uint4 w = use_c ? *p : make_uint4(0u, 0u, 0u, 0u);
+            uint4 o;
+            o.x = __float_as_uint(__uint_as_float(w.x) + __uint_as_float(r[4 * c + 0]));
+            o.y = __float_as_uint(__uint_as_float(w.y) + __uint_as_float(r[4 * c + 1]));
+            o.z = __float_as_uint(__uint_as_float(w.z) + __uint_as_float(r[4 * c + 2]));
+            o.w = __float_as_uint(__uint_as_float(w.w) + __uint_as_float(r[4 * c + 3]));
+            *p = o;
           }
-          store_block(buf, colh + j * 16, row0);
+          emit_block(buf, colh + j * 16, row0);
         }
         sb += NBLK;
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       } else {
+        const int row = row0 + lane;
+        const bool row_ok = row < M;
         const int32_t* C = static_cast<const int32_t*>(Cv);
         const int32_t* crow =
             (C && row_ok) ? C + int64_t(row) * ldc + colh : nullptr;
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         iacc[j * 16 + 4 * c + 1],
                                         iacc[j * 16 + 4 * c + 2],
                                         iacc[j * 16 + 4 * c + 3]);
-          store_block(buf, colh + j * 16, row0);
+          emit_block(buf, colh + j * 16, row0);
         }
         sb += NBLK;
       }
@@ -659,19 +661,27 @@ mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
     tc = td;  // never read: the kernel loads C only when it is given
   }
   auto kern = gemm_tc_kernel<BN, STAGES, BF16, EPI, CL>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::ALLOC) != cudaSuccess)
-    return MMA_ERR_LAUNCH;
+  static bool smem_set[64] = {};  // per device, once per instantiation
+  if (!smem_set[ctx.device & 63]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::ALLOC) != cudaSuccess)
+      return MMA_ERR_LAUNCH;
+    smem_set[ctx.device & 63] = true;
+  }
   const int64_t units = ((M + BM * CL - 1) / (BM * CL)) * ((N + BN - 1) / BN);
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::ALLOC;
   cfg.stream = ctx.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // The exact INT8 mode follows its widening pass on the stream: let it
+  // launch as a programmatic dependent of that pass.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // persistent: as many clusters as can be resident at once (at most one
@@ -693,6 +703,7 @@ mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   }
   if (clusters > units) clusters = units;
   cfg.gridDim = dim3(unsigned(clusters * CL), 1, 1);
+  if (EPI == Epi::I32EXACT) cfg.numAttrs = 2;
   ctx.mark_start();
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, C, ldc, D, ldd, int(M), int(N),

@@ -76,6 +76,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
       : "memory");
 }
 
+// Programmatic dependent launch: wait until the grid this one depends on
+// has completed and its memory operations are visible (a no-op when the
+// kernel was launched without the programmatic-serialization attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
