@@ -58,20 +58,20 @@ enum class Epi { F32, I32EXACT };
 // integers.
 constexpr int kI8ChunkK = 1024;
 
-// Epilogue staging: each epilogue warp owns two 32-row x 16-column FP32
-// blocks (64-byte rows, 64-byte TMA swizzle) through which C arrives and D
-// leaves by TMA.
+// Epilogue staging: each epilogue warp owns NSTG 32-row x 16-column blocks
+// of 4-byte elements (64-byte rows, 64-byte TMA swizzle), a ring through
+// which C arrives and D leaves by TMA.
 constexpr int kStgBytes = 32 * 16 * 4;
 
 // CL = 2: each CTA of a pair stages its own half of the B box.
-template <int BN, int STAGES, int CL>
+template <int BN, int STAGES, int CL, int NSTG>
 struct Layout {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = (BN / CL) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STG_OFFSET = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFFSET = STG_OFFSET + kEpiWarps * 2 * kStgBytes;
-  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kEpiWarps;
+  static constexpr int BAR_OFFSET = STG_OFFSET + kEpiWarps * NSTG * kStgBytes;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + NSTG * kEpiWarps;
   static constexpr int TOTAL = BAR_OFFSET + NUM_BARS * 8 + 16;
   static constexpr int ALLOC = TOTAL + 1024;  // room to align the base
   // two accumulators of BN columns, rounded up to a power of two
@@ -116,7 +116,7 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity,
 // issues the pair's MMAs, whose commits release the stage in both CTAs and
 // announce the accumulator to both CTAs' epilogues; every epilogue warp of
 // the pair returns the accumulator on the leader's tempty barrier.
-template <int BN, int STAGES, bool BF16, Epi EPI, int CL>
+template <int BN, int STAGES, bool BF16, Epi EPI, int CL, int NSTG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const void* __restrict__ Cv, int64_t ldc,
                    void* __restrict__ Dv, int64_t ldd, int M, int N, int K,
                    int kb_per_chunk, unsigned* status) {
-  using L = Layout<BN, STAGES, CL>;
+  using L = Layout<BN, STAGES, CL, NSTG>;
   constexpr int HALF = BN / 2;  // columns per epilogue warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -135,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint64_t* cbar = done + 1;  // two per epilogue warp: C block landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 2 * kEpiWarps);
+  uint64_t* cbar = done + 1;  // NSTG per epilogue warp: C block landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + NSTG * kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[a], CL * kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(done, 1);
-    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&cbar[i], 1);
+    for (int i = 0; i < NSTG * kEpiWarps; ++i) mbar_init(&cbar[i], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -319,22 +319,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ epilogue warps
     // Each warp owns a 32-row quarter of the tile (its TMEM lane quarter)
-    // and one column half.  D leaves through the warp's two staging blocks
-    // by TMA store (coalesced, asynchronous).  In FP32 mode C arrives the
-    // same way, one block ahead of its use.  In the exact INT8 mode the
-    // INT32 sums of the chunks are kept in registers, starting from C
-    // fetched at the start of the tile (hidden behind the first chunk's
-    // MMAs).  (Accumulating the chunks into D with TMA reduce-add instead
-    // was measured slower: the L2 atomics cost more than the registers.)
+    // and one column half, emitted as 16-column blocks through a ring of
+    // NSTG staging blocks: D leaves by TMA store, and C arrives by TMA PF
+    // blocks ahead of its use -- across tile boundaries, so the next tile's
+    // first C blocks are in flight while this tile finishes.  In the exact
+    // INT8 mode the chunks' INT32 sums are kept in registers (starting from
+    // zero) and C is added only as each block is emitted, so no chunk drain
+    // ever waits on memory.  (Accumulating the chunks into D with TMA
+    // reduce-add instead was measured slower: the L2 atomics cost more than
+    // the registers.)
     const int ew = warp - 2;           // 0 .. 7
     const int q = warp & 3;            // tensor-memory lane quarter
     const int h = ew >> 2;             // column half of the tile
     const int lane = threadIdx.x & 31;
-    uint8_t* stg = smem + L::STG_OFFSET + ew * 2 * kStgBytes;
-    uint64_t* wbar = &cbar[2 * ew];
+    uint8_t* stg = smem + L::STG_OFFSET + ew * NSTG * kStgBytes;
+    uint64_t* wbar = &cbar[NSTG * ew];
     const bool has_c = Cv != nullptr;
     constexpr int NBLK = HALF / 16;
-    uint32_t sb = 0;  // staging blocks used so far by this warp
+    // The C of block g + PF is requested while block g is processed; its
+    // ring slot last held block g + PF - NSTG, whose store must have
+    // finished reading it, which leaves at most WAITN later stores pending.
+    constexpr int PF = NSTG > 2 ? NSTG - 2 : 1;
+    constexpr int WAITN = NSTG - PF - 1;
+    static_assert(PF <= NBLK, "C is prefetched at most one tile ahead");
+    uint32_t g = 0;  // blocks emitted so far by this warp
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -366,102 +374,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    for (int u = first_unit; u < units && ok; u += unit_step) {
+    // This warp's first row and first column in work unit u.
+    auto unit_origin = [&](int u, int& row0, int& colh) {
       int mu, nb;
       tile_coords(u, unit_m, num_n, mu, nb);
-      const int row0 = (mu * CL + rank) * BM + q * 32;
-      const int colh = nb * BN + h * HALF;  // first column of this half
-      if constexpr (EPI == Epi::F32) {
-        // one chunk per tile: the whole K loop in one accumulator
-        const bool use_c = has_c;
-        // C block j goes to staging buffer (sb + j) & 1, whose previous
-        // store must have finished reading it.
-        auto fetch_c = [&](int j) {
-          const uint32_t b = (sb + j) & 1u;
-          if (row0 < M && colh + j * 16 < N) {
-            mbar_arrive_expect_tx(&wbar[b], kStgBytes);
-            tma_load_2d(&tmC, &wbar[b], stg + b * kStgBytes, colh + j * 16,
-                        row0);
-          } else {
-            // wholly outside C (and D): nothing to load or store
-            mbar_arrive(&wbar[b]);
-          }
-        };
-        if (lane == 0) {
-          if (use_c) {
-            bulk_wait_group_read<1>();
-            fetch_c(0);
-          }
-        }
-        __syncwarp();
-        ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
-                               (uint32_t(q * 32) << 16);
-#pragma unroll 1
-        for (int j = 0; j < NBLK; ++j) {
-          const uint32_t g = sb + uint32_t(j);
-          uint8_t* buf = stg + (g & 1u) * kStgBytes;
-          if (lane == 0) {
-            if (use_c && j + 1 < NBLK) {
-              bulk_wait_group_read<0>();
-              fetch_c(j + 1);
-            } else if (!use_c) {
-              bulk_wait_group_read<1>();
-            }
-          }
-          __syncwarp();
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
-          tmem_ld_wait();
-          // every TMEM read of this accumulator is done: release it
-          if (j == NBLK - 1) release_acc(acc);
-          if (use_c) {
-            ok = mbar_wait(&wbar[g & 1u], (g >> 1) & 1u, abort_flag, status);
-            if (!__all_sync(0xffffffffu, ok)) {
-              ok = false;
-              break;
-            }
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4* p = chunk(buf, c);
-            const uint4 w = use_c ? *p : make_uint4(0u, 0u, 0u, 0u);
-            uint4 o;
-            o.x = __float_as_uint(__uint_as_float(w.x) + __uint_as_float(r[4 * c + 0]));
-            o.y = __float_as_uint(__uint_as_float(w.y) + __uint_as_float(r[4 * c + 1]));
-            o.z = __float_as_uint(__uint_as_float(w.z) + __uint_as_float(r[4 * c + 2]));
-            o.w = __float_as_uint(__uint_as_float(w.w) + __uint_as_float(r[4 * c + 3]));
-            *p = o;
-          }
-          emit_block(buf, colh + j * 16, row0);
-        }
-        sb += NBLK;
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+      row0 = (mu * CL + rank) * BM + q * 32;
+      colh = nb * BN + h * HALF;
+    };
+    // (lane 0) Request the C of block gg, which is block jj of unit u.
+    auto request_c = [&](uint32_t gg, int u, int jj) {
+      const uint32_t b = gg % NSTG;
+      int row0, colh;
+      unit_origin(u, row0, colh);
+      bulk_wait_group_read<WAITN>();
+      if (row0 < M && colh + jj * 16 < N) {
+        mbar_arrive_expect_tx(&wbar[b], kStgBytes);
+        tma_load_2d(&tmC, &wbar[b], stg + b * kStgBytes, colh + jj * 16, row0);
       } else {
-        const int row = row0 + lane;
-        const bool row_ok = row < M;
-        const int32_t* C = static_cast<const int32_t*>(Cv);
-        const int32_t* crow =
-            (C && row_ok) ? C + int64_t(row) * ldc + colh : nullptr;
-        // The INT32 sums start from C, fetched before the first chunk.
-        uint32_t iacc[HALF];
-        if (crow && colh + HALF <= N) {
+        mbar_arrive(&wbar[b]);  // wholly outside C and D: nothing to load
+      }
+    };
+    if (has_c && lane == 0 && first_unit < units)
+      for (int jj = 0; jj < PF; ++jj) request_c(uint32_t(jj), first_unit, jj);
+    __syncwarp();
+    for (int u = first_unit; u < units && ok; u += unit_step) {
+      int row0, colh;
+      unit_origin(u, row0, colh);
+      [[maybe_unused]] uint32_t iacc[EPI == Epi::I32EXACT ? HALF : 1];
+      uint32_t taddr = 0;
+      if constexpr (EPI == Epi::I32EXACT) {
 #pragma unroll
-          for (int v = 0; v < HALF / 4; ++v) {
-            const int4 cv = __ldcs(reinterpret_cast<const int4*>(crow) + v);
-            iacc[4 * v + 0] = uint32_t(cv.x);
-            iacc[4 * v + 1] = uint32_t(cv.y);
-            iacc[4 * v + 2] = uint32_t(cv.z);
-            iacc[4 * v + 3] = uint32_t(cv.w);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < HALF; ++j)
-            iacc[j] = (crow && colh + j < N) ? uint32_t(crow[j]) : 0u;
-        }
+        for (int j = 0; j < HALF; ++j) iacc[j] = 0u;
         for (int ch = 0; ch < chunks; ++ch) {
           ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
           if (!__all_sync(0xffffffffu, ok)) {
@@ -469,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
-                                 (uint32_t(q * 32) << 16);
+          taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
+                  (uint32_t(q * 32) << 16);
 #pragma unroll
           for (int c = 0; c < HALF / 16; ++c) {
             uint32_t r[16];
@@ -485,20 +428,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (acc == 0) acc_phase ^= 1u;
         }
         if (!ok) break;
+      } else {
+        ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
+                (uint32_t(q * 32) << 16);
+      }
 #pragma unroll
-        for (int j = 0; j < NBLK; ++j) {
-          uint8_t* buf = stg + ((sb + uint32_t(j)) & 1u) * kStgBytes;
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *chunk(buf, c) = make_uint4(iacc[j * 16 + 4 * c + 0],
-                                        iacc[j * 16 + 4 * c + 1],
-                                        iacc[j * 16 + 4 * c + 2],
-                                        iacc[j * 16 + 4 * c + 3]);
-          emit_block(buf, colh + j * 16, row0);
+      for (int j = 0; j < NBLK; ++j, ++g) {
+        uint8_t* buf = stg + (g % NSTG) * kStgBytes;
+        if (lane == 0) {
+          if (has_c) {
+            // the C of block g + PF, possibly in this warp's next unit
+            int jj = j + PF, uu = u;
+            if (jj >= NBLK) {
+              jj -= NBLK;
+              uu = u + unit_step;
+            }
+            if (uu < units) request_c(g + PF, uu, jj);
+          } else {
+            bulk_wait_group_read<NSTG - 1>();  // slot's last store has read it
+          }
         }
-        sb += NBLK;
+        __syncwarp();
+        [[maybe_unused]] uint32_t r[16];
+        if constexpr (EPI == Epi::F32) {
+          tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
+          tmem_ld_wait();
+          // every TMEM read of this accumulator is done: release it
+          if (j == NBLK - 1) release_acc(acc);
+        }
+        if (has_c) {
+          ok = mbar_wait(&wbar[g % NSTG], (g / NSTG) & 1u, abort_flag, status);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4* p = chunk(buf, c);
+          const uint4 w = has_c ? *p : make_uint4(0u, 0u, 0u, 0u);
+          uint4 o;
+          if constexpr (EPI == Epi::F32) {
+            o.x = __float_as_uint(__uint_as_float(w.x) + __uint_as_float(r[4 * c + 0]));
+            o.y = __float_as_uint(__uint_as_float(w.y) + __uint_as_float(r[4 * c + 1]));
+            o.z = __float_as_uint(__uint_as_float(w.z) + __uint_as_float(r[4 * c + 2]));
+            o.w = __float_as_uint(__uint_as_float(w.w) + __uint_as_float(r[4 * c + 3]));
+          } else {
+            // INT32 adds wrap modulo 2^32
+            o.x = w.x + iacc[j * 16 + 4 * c + 0];
+            o.y = w.y + iacc[j * 16 + 4 * c + 1];
+            o.z = w.z + iacc[j * 16 + 4 * c + 2];
+            o.w = w.w + iacc[j * 16 + 4 * c + 3];
+          }
+          *p = o;
+        }
+        emit_block(buf, colh + j * 16, row0);
+      }
+      if constexpr (EPI == Epi::F32) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
       }
     }
     // every store of this warp has landed before the CTA finishes
@@ -644,11 +635,12 @@ bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool BF16, Epi EPI, int CL>
+template <int BN, int STAGES, bool BF16, Epi EPI, int CL, int NSTG>
 mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd) {
-  using L = Layout<BN, STAGES, CL>;
+  using L = Layout<BN, STAGES, CL, NSTG>;
+  static_assert(L::ALLOC <= 232448, "shared memory per CTA");
   constexpr bool kInt = EPI == Epi::I32EXACT;
   CUtensorMap ta, tb, tc, td;
   if (!make_kmajor_map(&ta, A, K, M, lda, BM, BF16) ||
@@ -660,7 +652,7 @@ mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   } else {
     tc = td;  // never read: the kernel loads C only when it is given
   }
-  auto kern = gemm_tc_kernel<BN, STAGES, BF16, EPI, CL>;
+  auto kern = gemm_tc_kernel<BN, STAGES, BF16, EPI, CL, NSTG>;
   static bool smem_set[64] = {};  // per device, once per instantiation
   if (!smem_set[ctx.device & 63]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -736,12 +728,14 @@ mma_status_t dispatch(const Ctx& ctx, int bn, int cl, int64_t M, int64_t N,
                       int64_t K, const void* A, int64_t lda, const void* B,
                       int64_t ldb, const void* C, int64_t ldc, void* D,
                       int64_t ldd) {
-  // stages: 192 KB of operand ring (a pair stages half of B per CTA)
+  // Shared memory: operand ring (a pair stages half of B per CTA) plus the
+  // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
+  // tiles, whose 48 KB stages leave room for only 4 of them).
   if (bn == 256)
-    return cl == 2 ? run<256, 6, BF16, EPI, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-                   : run<256, 4, BF16, EPI, 1>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
-  return cl == 2 ? run<128, 8, BF16, EPI, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-                 : run<128, 6, BF16, EPI, 1>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+    return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
+                   : run<256, 4, BF16, EPI, 1, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
+                 : run<128, 5, BF16, EPI, 1, 4>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
 }
 
 // Tile width (columns of D per CTA): 256 when there are enough such tiles
