@@ -35,13 +35,15 @@
  * C may be NULL (read as zero).  C may equal D (in place) only when
  * ldc == ldd; any other overlap between D and an input is undefined.
  *
- * Device memory owned by the library: INT8 products with M*N*K >= 2^24 run
- * on the BF16 tensor pipe and need (M + N) * roundup(K, 8) * 2 bytes of
- * scratch for BF16 copies of A and B.  That buffer is allocated once per
- * device by the first such call, grown (cudaMalloc, after the previous user
- * finishes) only when a larger problem arrives, and kept until the process
- * exits; calls on different streams are ordered on it by an event.  Failure
- * to grow it returns MMA_ERR_NO_MEMORY.  No other call allocates.
+ * Device memory owned by the library: some paths first rewrite an operand
+ * into a scratch buffer -- INT8 products with M*N*K >= 2^24 (and every INT8
+ * product with row-major B) widen A and B to BF16 for the tensor pipe,
+ * (M + N) * roundup(K, 8) * 2 bytes; FP16/BF16 products with row-major B
+ * transpose B, N * roundup(K, 8) * 2 bytes.  That buffer is allocated once
+ * per device by the first such call, grown (cudaMalloc, after the previous
+ * user finishes) only when a larger problem arrives, and kept until the
+ * process exits; calls on different streams are ordered on it by an event.
+ * Failure to grow it returns MMA_ERR_NO_MEMORY.  No other call allocates.
  *
  * Alignment: every non-NULL base pointer must be 16-byte aligned and every
  * leading dimension times the element size must be a multiple of 16 bytes
@@ -88,7 +90,7 @@ typedef enum {
   MMA_ERR_LAUNCH = 4,      /* CUDA reported an error at launch            */
   MMA_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out            */
   MMA_ERR_NO_DEVICE = 6,   /* no usable sm_103 device is current          */
-  MMA_ERR_NO_MEMORY = 7    /* the INT8 scratch buffer could not be grown  */
+  MMA_ERR_NO_MEMORY = 7    /* the scratch buffer could not be grown       */
 } mma_status_t;
 
 /*

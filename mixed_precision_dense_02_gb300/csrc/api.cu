@@ -155,11 +155,11 @@ namespace {
 // smaller ones stay on the IMMA kernel, which needs no scratch.
 constexpr double kI8TensorCoreMinWork = 16777216.0;  // 2^24
 
-mma_status_t gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
-                        const int8_t* A, int64_t lda, const int8_t* B,
-                        int64_t ldb, const int32_t* C, int64_t ldc,
-                        int32_t* D, int64_t ldd) {
-  const size_t need = gemm_i8_tc_workspace_bytes(M, N, K);
+// Run `enqueue(workspace)` with at least `need` bytes of the device's
+// scratch buffer, growing it if needed, ordered after the buffer's previous
+// user (an event) and marking this stream as its new user.
+template <class F>
+mma_status_t with_workspace(const Ctx& ctx, size_t need, F&& enqueue) {
   std::lock_guard<std::mutex> lk(g_ws_mu);
   Workspace& w = g_ws[ctx.device];
   if (!w.done &&
@@ -186,8 +186,7 @@ mma_status_t gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   }
   if (cudaStreamWaitEvent(ctx.stream, w.done, 0) != cudaSuccess)
     return MMA_ERR_LAUNCH;
-  const mma_status_t st =
-      launch_gemm_i8_tc(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, w.ptr);
+  const mma_status_t st = enqueue(w.ptr);
   if (cudaEventRecord(w.done, ctx.stream) != cudaSuccess) return MMA_ERR_LAUNCH;
   return st;
 }
@@ -243,8 +242,6 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
   if (!aligned16(D) || !ld_ok(ldd, ea)) return MMA_ERR_MISALIGNED;
   if (C != nullptr && (!aligned16(C) || !ld_ok(ldc, ea)))
     return MMA_ERR_MISALIGNED;
-  if (b_row && dtype_in != MMA_F64) return MMA_ERR_UNSUPPORTED;
-
   int dev = -1;
   const DeviceInfo* info = device_info(&dev);
   if (!info) return MMA_ERR_NO_DEVICE;
@@ -254,20 +251,36 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
   if (K == 0) return launch_copy_c(ctx, M, N, int(ea), C, ldc, D, ldd);
   switch (dtype_in) {
     case MMA_F16:
-    case MMA_BF16:
-      return launch_gemm_tc_f16(ctx, dtype_in == MMA_BF16, M, N, K, A, lda, B,
-                                ldb, static_cast<const float*>(C), ldc,
-                                static_cast<float*>(D), ldd);
-    case MMA_I8:
-      if (double(M) * double(N) * double(K) >= kI8TensorCoreMinWork)
-        return gemm_i8_tc(ctx, M, N, K, static_cast<const int8_t*>(A), lda,
-                          static_cast<const int8_t*>(B), ldb,
-                          static_cast<const int32_t*>(C), ldc,
-                          static_cast<int32_t*>(D), ldd);
-      return launch_gemm_i8_imma(ctx, M, N, K, static_cast<const int8_t*>(A),
-                                 lda, static_cast<const int8_t*>(B), ldb,
-                                 static_cast<const int32_t*>(C), ldc,
-                                 static_cast<int32_t*>(D), ldd);
+    case MMA_BF16: {
+      const bool bf16 = dtype_in == MMA_BF16;
+      const float* Cf = static_cast<const float*>(C);
+      float* Df = static_cast<float*>(D);
+      if (!b_row)
+        return launch_gemm_tc_f16(ctx, bf16, M, N, K, A, lda, B, ldb, Cf, ldc,
+                                  Df, ldd);
+      return with_workspace(ctx, gemm_tc_rowb_workspace_bytes(N, K),
+                            [&](void* ws) {
+                              return launch_gemm_tc_f16_rowb(
+                                  ctx, bf16, M, N, K, A, lda, B, ldb, Cf, ldc,
+                                  Df, ldd, ws);
+                            });
+    }
+    case MMA_I8: {
+      const int8_t* A8 = static_cast<const int8_t*>(A);
+      const int8_t* B8 = static_cast<const int8_t*>(B);
+      const int32_t* Ci = static_cast<const int32_t*>(C);
+      int32_t* Di = static_cast<int32_t*>(D);
+      // Large problems, and every row-major B, take the tensor-pipe path.
+      if (b_row || double(M) * double(N) * double(K) >= kI8TensorCoreMinWork)
+        return with_workspace(ctx, gemm_i8_tc_workspace_bytes(M, N, K),
+                              [&](void* ws) {
+                                return launch_gemm_i8_tc(ctx, M, N, K, A8, lda,
+                                                         B8, ldb, Ci, ldc, Di,
+                                                         ldd, ws, b_row);
+                              });
+      return launch_gemm_i8_imma(ctx, M, N, K, A8, lda, B8, ldb, Ci, ldc, Di,
+                                 ldd);
+    }
     case MMA_F64:
       return launch_gemm_f64(ctx, M, N, K, static_cast<const double*>(A), lda,
                              static_cast<const double*>(B), ldb, b_row,

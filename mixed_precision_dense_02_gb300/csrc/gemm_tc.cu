@@ -635,8 +635,10 @@ bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
   return r == CUDA_SUCCESS;
 }
 
+// pdl: launch as a programmatic dependent of the kernel just before it on
+// the stream (a pass that produced A or B).
 template <int BN, int STAGES, bool BF16, Epi EPI, int CL, int NSTG>
-mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
+mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd) {
   using L = Layout<BN, STAGES, CL, NSTG>;
@@ -670,8 +672,6 @@ mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // The exact INT8 mode follows its widening pass on the stream: let it
-  // launch as a programmatic dependent of that pass.
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
@@ -695,7 +695,7 @@ mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   }
   if (clusters > units) clusters = units;
   cfg.gridDim = dim3(unsigned(clusters * CL), 1, 1);
-  if (EPI == Epi::I32EXACT) cfg.numAttrs = 2;
+  if (pdl) cfg.numAttrs = 2;
   ctx.mark_start();
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, C, ldc, D, ldd, int(M), int(N),
@@ -723,21 +723,6 @@ int cluster_size(int64_t M, int64_t N, int64_t K) {
   return (M > BM && work >= 1073741824.0) ? 2 : 1;
 }
 
-template <bool BF16, Epi EPI>
-mma_status_t dispatch(const Ctx& ctx, int bn, int cl, int64_t M, int64_t N,
-                      int64_t K, const void* A, int64_t lda, const void* B,
-                      int64_t ldb, const void* C, int64_t ldc, void* D,
-                      int64_t ldd) {
-  // Shared memory: operand ring (a pair stages half of B per CTA) plus the
-  // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
-  // tiles, whose 48 KB stages leave room for only 4 of them).
-  if (bn == 256)
-    return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-                   : run<256, 4, BF16, EPI, 1, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
-  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-                 : run<128, 5, BF16, EPI, 1, 4>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
-}
-
 // Tile width (columns of D per CTA): 256 when there are enough such tiles
 // to occupy every SM, else 128 (more, smaller tiles).  Measured on the
 // INT8 4096^3, BF16 8192^3 and 16384 x 128 x 4096 workloads, 256-wide tiles
@@ -754,6 +739,63 @@ int tile_n(const Ctx& ctx, int64_t M, int64_t N) {
   return (N > 128 && wide_tiles >= ctx.num_sms) ? 256 : 128;
 }
 
+template <bool BF16, Epi EPI>
+mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
+                      int64_t N, int64_t K, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, const void* C, int64_t ldc,
+                      void* D, int64_t ldd) {
+  // Shared memory: operand ring (a pair stages half of B per CTA) plus the
+  // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
+  // tiles, whose 48 KB stages leave room for only 4 of them).
+  if (bn == 256)
+    return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
+                   : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
+                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+}
+
+// Row-major B (K x N, N contiguous) -> K-major copy W (N rows of K, leading
+// dimension ldw) of 16-bit elements, through 64 x 64 shared-memory tiles so
+// that both the reads and the writes are coalesced.  With I8 the int8
+// values are widened to bfloat16 on the way (exactly).
+template <bool I8>
+__global__ void __launch_bounds__(256)
+    transpose_b_kernel(const void* __restrict__ Bv, int64_t ldb, int K, int N,
+                       uint16_t* __restrict__ W, int64_t ldw) {
+  __shared__ uint16_t tile[64][66];  // [k][n], padded
+  const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
+  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
+    const int kk = i >> 6, nn = i & 63;
+    const int k = k0 + kk, n = n0 + nn;
+    uint16_t v = 0;
+    if (k < K && n < N) {
+      if constexpr (I8)
+        v = uint16_t(__float_as_uint(float(static_cast<const int8_t*>(Bv)[int64_t(k) * ldb + n])) >> 16);
+      else
+        v = static_cast<const uint16_t*>(Bv)[int64_t(k) * ldb + n];
+    }
+    tile[kk][nn] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
+    const int nn = i >> 6, kk = i & 63;
+    const int n = n0 + nn, k = k0 + kk;
+    if (n < N && k < K) W[int64_t(n) * ldw + k] = tile[kk][nn];
+  }
+}
+
+template <bool I8>
+mma_status_t launch_transpose_b(const Ctx& ctx, const void* B, int64_t ldb,
+                                int64_t K, int64_t N, uint16_t* W,
+                                int64_t ldw) {
+  const int64_t gy = (K + 63) / 64;
+  if (gy > 65535) return MMA_ERR_UNSUPPORTED;
+  const dim3 grid{unsigned((N + 63) / 64), unsigned(gy), 1u};
+  transpose_b_kernel<I8><<<grid, 256, 0, ctx.stream>>>(B, ldb, int(K), int(N),
+                                                        W, ldw);
+  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}
+
 }  // namespace
 
 mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, int64_t M,
@@ -763,10 +805,32 @@ mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, int64_t M,
                                 int64_t ldd) {
   const int bn = tile_n(ctx, M, N);
   const int cl = cluster_size(M, N, K);
-  return bf16 ? dispatch<true, Epi::F32>(ctx, bn, cl, M, N, K, A, lda, B, ldb,
-                                         C, ldc, D, ldd)
-              : dispatch<false, Epi::F32>(ctx, bn, cl, M, N, K, A, lda, B, ldb,
-                                          C, ldc, D, ldd);
+  return bf16 ? dispatch<true, Epi::F32>(ctx, false, bn, cl, M, N, K, A, lda,
+                                         B, ldb, C, ldc, D, ldd)
+              : dispatch<false, Epi::F32>(ctx, false, bn, cl, M, N, K, A, lda,
+                                          B, ldb, C, ldc, D, ldd);
+}
+
+size_t gemm_tc_rowb_workspace_bytes(int64_t N, int64_t K) {
+  const int64_t ldw = (K + 7) / 8 * 8;
+  return size_t(N) * size_t(ldw) * 2;
+}
+
+mma_status_t launch_gemm_tc_f16_rowb(const Ctx& ctx, bool bf16, int64_t M,
+                                     int64_t N, int64_t K, const void* A,
+                                     int64_t lda, const void* B, int64_t ldb,
+                                     const float* C, int64_t ldc, float* D,
+                                     int64_t ldd, void* workspace) {
+  const int64_t ldw = (K + 7) / 8 * 8;
+  uint16_t* W = static_cast<uint16_t*>(workspace);
+  const mma_status_t st = launch_transpose_b<false>(ctx, B, ldb, K, N, W, ldw);
+  if (st != MMA_OK) return st;
+  const int bn = tile_n(ctx, M, N);
+  const int cl = cluster_size(M, N, K);
+  return bf16 ? dispatch<true, Epi::F32>(ctx, true, bn, cl, M, N, K, A, lda,
+                                         W, ldw, C, ldc, D, ldd)
+              : dispatch<false, Epi::F32>(ctx, true, bn, cl, M, N, K, A, lda,
+                                          W, ldw, C, ldc, D, ldd);
 }
 
 size_t gemm_i8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -778,20 +842,26 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
                                int64_t K, const int8_t* A, int64_t lda,
                                const int8_t* B, int64_t ldb, const int32_t* C,
                                int64_t ldc, int32_t* D, int64_t ldd,
-                               void* workspace) {
+                               void* workspace, bool b_row_major) {
   const int64_t ldw = (K + 7) / 8 * 8;
   uint16_t* W = static_cast<uint16_t*>(workspace);
-  const int64_t chunks = (M + N) * ((K + 15) / 16);
+  uint16_t* Bw = W + M * ldw;
+  if (b_row_major) {
+    // B widened while transposed; the A pass below then runs last, so the
+    // GEMM's programmatic dependency is on it (and on B by stream order).
+    const mma_status_t st = launch_transpose_b<true>(ctx, B, ldb, K, N, Bw, ldw);
+    if (st != MMA_OK) return st;
+  }
+  const int64_t rows = b_row_major ? M : M + N;
+  const int64_t chunks = rows * ((K + 15) / 16);
   const int64_t span = int64_t(kConvThreads) * kConvUnroll;
   int64_t blocks = (chunks + span - 1) / span;
   if (blocks > int64_t(ctx.num_sms) * 8) blocks = int64_t(ctx.num_sms) * 8;
   i8_to_bf16_kernel<<<int(blocks), kConvThreads, 0, ctx.stream>>>(
-      A, lda, int(M), B, ldb, int(N), int(K), W, ldw);
+      A, lda, int(M), B, ldb, b_row_major ? 0 : int(N), int(K), W, ldw);
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
-  const uint16_t* Aw = W;
-  const uint16_t* Bw = W + M * ldw;
-  return dispatch<true, Epi::I32EXACT>(ctx, tile_n(ctx, M, N),
-                                       cluster_size(M, N, K), M, N, K, Aw, ldw,
+  return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N),
+                                       cluster_size(M, N, K), M, N, K, W, ldw,
                                        Bw, ldw, C, ldc, D, ldd);
 }
 

@@ -34,15 +34,24 @@ mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, int64_t M,
                                 const float* C, int64_t ldc, float* D,
                                 int64_t ldd);
 
-// Exact INT8 GEMM on the tcgen05 BF16 pipe (column-major B).  `workspace`
-// holds gemm_i8_tc_workspace_bytes(M, N, K) bytes of device scratch for the
-// BF16 copies of A and B.
+// Exact INT8 GEMM on the tcgen05 BF16 pipe.  `workspace` holds
+// gemm_i8_tc_workspace_bytes(M, N, K) bytes of device scratch for the BF16
+// copies of A and B (B is transposed into it when b_row_major).
 size_t gemm_i8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
                                int64_t K, const int8_t* A, int64_t lda,
                                const int8_t* B, int64_t ldb, const int32_t* C,
                                int64_t ldc, int32_t* D, int64_t ldd,
-                               void* workspace);
+                               void* workspace, bool b_row_major);
+
+// tcgen05 FP16/BF16 GEMM with row-major B: B is transposed into
+// `workspace` (gemm_tc_rowb_workspace_bytes(N, K) bytes) first.
+size_t gemm_tc_rowb_workspace_bytes(int64_t N, int64_t K);
+mma_status_t launch_gemm_tc_f16_rowb(const Ctx& ctx, bool bf16, int64_t M,
+                                     int64_t N, int64_t K, const void* A,
+                                     int64_t lda, const void* B, int64_t ldb,
+                                     const float* C, int64_t ldc, float* D,
+                                     int64_t ldd, void* workspace);
 
 // INT8 GEMM on the warp-level IMMA pipe, column-major B.
 mma_status_t launch_gemm_i8_imma(const Ctx& ctx, int64_t M, int64_t N,

@@ -107,5 +107,6 @@ extern "C" mma_status_t mma_gemm_i8_noalloc(int64_t M, int64_t N, int64_t K,
   return launch_gemm_i8_tc(ctx, M, N, K, static_cast<const int8_t*>(A), lda,
                            static_cast<const int8_t*>(B), ldb,
                            static_cast<const int32_t*>(C), ldc,
-                           static_cast<int32_t*>(D), ldd, scratch);
+                           static_cast<int32_t*>(D), ldd, scratch,
+                           /*b_row_major=*/false);
 }

@@ -82,7 +82,6 @@ def g(*, din=BF16, dacc=F32, M=64, N=64, K=64, A=P, lda=64, B=P, ldb=64,
     (dict(din=I8, dacc=I32, lda=72, ldb=64), MISAL),
     (dict(ldd=66), MISAL),
     (dict(din=F64, dacc=F64, lda=65), MISAL),
-    (dict(layout=1), UNSUP),         # row-major B: FP64 only
 ])
 def test_argument_errors_detected_before_launch(lib, kw, code):
     assert g(**kw) == code
@@ -100,6 +99,10 @@ def test_valid_arguments_reach_the_device_check(lib):
         pytest.skip("a device is present")
     assert g() == NODEV
     assert g(din=F64, dacc=F64, layout=1, lda=64, ldb=64) == NODEV
+    # row-major B is provided for every pair
+    assert g(layout=1) == NODEV
+    assert g(din=I8, dacc=I32, layout=1, lda=64, ldb=64) == NODEV
+    assert g(din=F16, dacc=F32, layout=1) == NODEV
     assert g(K=0, A=0, B=0) == NODEV
     assert g(C=0) == NODEV
 

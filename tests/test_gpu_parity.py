@@ -72,11 +72,20 @@ def test_padding_no_c_and_in_place(dtype_in):
     check(dtype_in, run_gemm(g, use_c=False), want0, ab0, "C = NULL")
 
 
-def test_f64_row_major_b():
-    for (M, N, K) in [(1, 1, 1), (65, 63, 17), (256, 192, 300)]:
-        g = synth.gemm_inputs(f"par_f64row_{M}", "f64", M, N, K, b_layout="row")
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8", "f64"])
+def test_row_major_b(dtype_in):
+    """mma_gemm_ex with B stored K x N row-major (FP64 reads it directly, the
+    others transpose it first into the library's scratch buffer)."""
+    for (M, N, K) in [(1, 1, 1), (65, 63, 17), (256, 192, 300), (300, 520, 1000),
+                      (1024, 768, 2048)]:
+        g = synth.gemm_inputs(f"par_row_{dtype_in}_{M}", dtype_in, M, N, K,
+                              b_layout="row")
         want, ab = oracle_ref(g)
-        check("f64", run_gemm(g), want, ab, f"f64 row-B {M}x{N}x{K}")
+        check(dtype_in, run_gemm(g, pad=1), want, ab, f"{dtype_in} row-B {M}x{N}x{K}")
+    g0 = synth.GemmInputs(dtype_in, M, N, K, g.A, g.B, np.zeros_like(g.C), "row")
+    want0, ab0 = oracle_ref(g0)
+    check(dtype_in, run_gemm(g, use_c=False), want0, ab0, "row-B, C = NULL")
+    check(dtype_in, run_gemm(g, inplace=True), want, ab, "row-B, in place")
 
 
 @pytest.mark.parametrize("dtype_in", ["f16", "bf16", "i8", "f64"])
