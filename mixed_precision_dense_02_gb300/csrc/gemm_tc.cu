@@ -511,18 +511,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// int8 -> bfloat16 (exact: every int8 value has at most 8 significant bits).
+// int8 -> bfloat16, exactly (every int8 value has at most 8 significant
+// bits), with full-rate integer/FP32 ALU operations instead of the slower
+// int-to-float conversion unit: for the byte x of v, u = x ^ 0x80 = v + 128
+// (two's complement); the float whose bits are 0x4B0000uu is 2^23 + u, so
+// subtracting 2^23 + 128 leaves v exactly, and its top 16 bits are the
+// bfloat16 of v.
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo_byte) {
+  // byte_perm picks byte `lo_byte` of w (made unsigned by the xor) into the
+  // low byte of 0x4B000000
+  const uint32_t f0 = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u + lo_byte);
+  const uint32_t f1 = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7541u + lo_byte);
+  const float v0 = __uint_as_float(f0) - 8388736.0f;  // 2^23 + 128
+  const float v1 = __uint_as_float(f1) - 8388736.0f;
+  // high halves of the two floats: (bf16(v1) << 16) | bf16(v0)
+  return __byte_perm(__float_as_uint(v0), __float_as_uint(v1), 0x7632);
+}
+
 __device__ __forceinline__ void i8x16_to_bf16(const int4 v, uint4& o0, uint4& o1) {
   const uint32_t w[4] = {uint32_t(v.x), uint32_t(v.y), uint32_t(v.z),
                          uint32_t(v.w)};
   uint32_t o[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int lo = int(int8_t((w[j >> 1] >> (16 * (j & 1))) & 0xFF));
-    const int hi = int(int8_t((w[j >> 1] >> (16 * (j & 1) + 8)) & 0xFF));
-    o[j] = (__float_as_uint(float(lo)) >> 16) |
-           (__float_as_uint(float(hi)) & 0xFFFF0000u);
-  }
+  for (int j = 0; j < 8; ++j) o[j] = i8x2_to_bf16x2(w[j >> 1], 2 * (j & 1));
   o0 = make_uint4(o[0], o[1], o[2], o[3]);
   o1 = make_uint4(o[4], o[5], o[6], o[7]);
 }

@@ -154,6 +154,19 @@ def test_i8_extremes_exact():
         assert np.array_equal(run_gemm(g), C + K * a * b)
 
 
+def test_i8_every_value_through_the_tensor_pipe():
+    """A[i][k] = int8(i + k) holds all 256 int8 values in every row; with
+    B = I (256 x 256, on the tensor-pipe path) D = A + C exactly."""
+    n = 256
+    A = ((np.arange(n)[:, None] + np.arange(n)[None, :]) % 256).astype(np.uint8).view(np.int8)
+    eye = np.eye(n, dtype=np.int8)
+    C = synth.int_uniform(0, 11, n * n, -(1 << 20), 1 << 20).astype(np.int32).reshape(n, n)
+    g = synth.GemmInputs("i8", n, n, n, A, eye, C)
+    assert np.array_equal(run_gemm(g), A.astype(np.int32) + C)
+    g = synth.GemmInputs("i8", n, n, n, eye, np.ascontiguousarray(A.T), C)
+    assert np.array_equal(run_gemm(g), A.astype(np.int32) + C)
+
+
 def test_i8_exact_large_partial_sums_then_unit_steps():
     """Each 1024-deep K chunk first accumulates 512 products of 2^14 (partial
     sum 2^23) and then 512 products of +-1, so every unit step must land
