@@ -53,9 +53,11 @@ NOMINAL_FP64_TFLOPS = 1.25
 # by the SHA-256 of the kernel's source file at capture time (a changed
 # source makes the figure stale, and it is then reported as null).
 NCU_TRAFFIC: dict = {
-    # ncu --set full, one launch after 3 warm-up launches (profiles/*.md)
-    "gemm_i8_4096": {"sha": "ba41bff384236b62", "bytes": 101056512 + 41768960},
-    "gemm_bf16_8192": {"sha": "8a795dd324c11a86", "bytes": 1372195000 + 252497920},
+    # ncu --set full, one launch after the warm-up launches (profiles/*.md)
+    "gemm_i8_4096": {"sha": "5e3f86df3c1b5816", "bytes": 184445952 + 43882496},
+    "gemm_bf16_8192": {"sha": "5e3f86df3c1b5816", "bytes": 1566695000 + 258763008},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "5e3f86df3c1b5816",
+                                        "bytes": 143704832 + 3984384},
     "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "24a0b2e421dd643e",
                                                "bytes": 436229888 + 226331648},
 }
