@@ -58,6 +58,14 @@ def lib() -> ctypes.CDLL:
         L.oracle_gemm_f16f32.argtypes = [_int, _i64, _i64, _i64, _p, _i64, _p,
                                          _i64, _int, _p, _i64, _p, _i64, _p,
                                          _i64]
+        L.oracle_gemm_f16f16.restype = _int
+        L.oracle_gemm_f16f16.argtypes = [_int, _i64, _i64, _i64, _p, _i64, _p,
+                                         _i64, _int, _p, _i64, _p, _i64, _p,
+                                         _i64]
+        L.oracle_double_to_f16.restype = ctypes.c_uint16
+        L.oracle_double_to_f16.argtypes = [ctypes.c_double]
+        L.oracle_double_to_bf16.restype = ctypes.c_uint16
+        L.oracle_double_to_bf16.argtypes = [ctypes.c_double]
         L.oracle_gemm_i8i32.restype = _i64
         L.oracle_gemm_i8i32.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64,
                                         _int, _p, _i64, _p, _i64]
@@ -82,6 +90,14 @@ def f16_to_double(bits: int) -> float:
 
 def bf16_to_double(bits: int) -> float:
     return float(lib().oracle_bf16_to_double(int(bits)))
+
+
+def double_to_f16(x: float) -> int:
+    return int(lib().oracle_double_to_f16(float(x)))
+
+
+def double_to_bf16(x: float) -> int:
+    return int(lib().oracle_double_to_bf16(float(x)))
 
 
 def _ptr(a):
@@ -172,6 +188,33 @@ def gemm(dtype_in: str, A, B, C=None, *, b_layout: str = "col",
     raise ValueError(f"unsupported dtype_in {dtype_in!r}")
 
 
+def gemm_acc16(dtype_in: str, A, B, C=None, *, b_layout: str = "col",
+               want_absab: bool = False):
+    """D = A*B + C with a 16-bit addend and result of the input's type
+    ("RDNA3 dense WMMA builtins" -- FP16/BF16-accumulate builtins).
+
+    ``A``, ``B``, ``C`` are uint16 bit patterns (or float16 arrays for
+    FP16); returns D as uint16 bit patterns, rounded once (nearest, ties to
+    even) from the exact-product double sum, and optionally (|A|*|B|).
+    """
+    if dtype_in not in ("f16", "bf16"):
+        raise ValueError(dtype_in)
+    M, N, K = _shape(A, B, b_layout)
+    A16, B16 = _bits16(A), _bits16(B)
+    C16 = None if C is None else _bits16(np.asarray(C))
+    if C16 is not None and C16.shape != (M, N):
+        raise ValueError("C must be M x N")
+    D = np.empty((M, N), np.uint16)
+    ab = np.empty((M, N), np.float64) if want_absab else None
+    rc = lib().oracle_gemm_f16f16(_DT[dtype_in], M, N, K, _ptr(A16), _ld(A16),
+                                  _ptr(B16), _ld(B16), _LAYOUT[b_layout],
+                                  _ptr(C16), _ld(C16) if C16 is not None else 0,
+                                  _ptr(D), N, _ptr(ab), N)
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_f16f16 failed")
+    return (D, ab) if want_absab else D
+
+
 def gemm_batched(dtype_in: str, A, B, C, *, group: int = 1, abid: int = 0,
                  b_layout: str = "col"):
     """Batched tiles with A-block broadcast ("Common MFMA parameters" --
@@ -213,5 +256,6 @@ def gemm_batched(dtype_in: str, A, B, C, *, group: int = 1, abid: int = 0,
     return D
 
 
-__all__ = ["gemm", "gemm_batched", "num_threads", "f16_to_double",
-           "bf16_to_double", "lib"]
+__all__ = ["gemm", "gemm_acc16", "gemm_batched", "num_threads",
+           "f16_to_double", "bf16_to_double", "double_to_f16",
+           "double_to_bf16", "lib"]

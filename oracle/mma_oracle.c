@@ -142,6 +142,82 @@ int oracle_gemm_f16f32(int in_kind, int64_t M, int64_t N, int64_t K,
   return 0;
 }
 
+/* ---- c2b: FP16/BF16 inputs, 16-bit accumulator and output ------------- *
+ * "RDNA3 dense WMMA builtins" -- FP16/BF16-accumulate builtins: the addend
+ * and the result are 16-bit.  The oracle keeps the exact-product double sum
+ * of c2, adds the decoded C and rounds once to the 16-bit format (nearest,
+ * ties to even).  (The builtins round the 16-bit accumulator after every
+ * K step; one final rounding is the plain definition of D = A*B + C in
+ * the output format.)                                                    */
+
+/* Round a double to the 16-bit format with `mant` stored fraction bits,
+ * exponent bias `bias` and all-ones exponent `emax_field`; nearest, ties to
+ * even; overflow to infinity; NaN to a quiet NaN.                        */
+static uint16_t round_double_16(double x, int mant, int bias, int emax_field) {
+  const uint16_t sign = signbit(x) ? (uint16_t)(1u << 15) : 0;
+  const uint16_t inf = (uint16_t)(sign | ((unsigned)emax_field << mant));
+  if (isnan(x)) return (uint16_t)(inf | (1u << (mant - 1)));
+  double a = fabs(x);
+  if (isinf(a)) return inf;
+  if (a == 0.0) return sign;
+  const int emin = 1 - bias;                 /* smallest normal exponent */
+  int e;
+  frexp(a, &e);                              /* a = f * 2^e, f in [0.5, 1) */
+  e -= 1;                                    /* a in [2^e, 2^(e+1)) */
+  if (e < emin) e = emin;                    /* subnormal quantum */
+  const double q = ldexp(1.0, e - mant);     /* spacing of the format at a */
+  const double m = rint(a / q);              /* exact division; RNE */
+  const double v = m * q;                    /* the rounded magnitude */
+  if (v >= ldexp(1.0, emax_field - bias)) return inf;
+  if (v < ldexp(1.0, emin)) return (uint16_t)(sign | (uint16_t)(v / ldexp(1.0, emin - mant)));
+  int ev;
+  frexp(v, &ev);
+  ev -= 1;
+  const unsigned frac = (unsigned)(v / ldexp(1.0, ev - mant)) - (1u << mant);
+  return (uint16_t)(sign | ((unsigned)(ev + bias) << mant) | frac);
+}
+
+uint16_t oracle_double_to_f16(double x) { return round_double_16(x, 10, 15, 31); }
+uint16_t oracle_double_to_bf16(double x) { return round_double_16(x, 7, 127, 255); }
+
+static void h16_row(const double *tab, int in_kind, int64_t i, int64_t N,
+                    int64_t K, const uint16_t *A, int64_t lda,
+                    const uint16_t *B, int64_t ldb, int b_layout,
+                    const uint16_t *C, int64_t ldc, uint16_t *D, int64_t ldd,
+                    double *absab, int64_t ldabs) {
+  for (int64_t j = 0; j < N; ++j) {
+    double s = 0.0, sa = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = tab[A[i * lda + k]];
+      const double b = tab[B[b_index(b_layout, k, j, ldb)]];
+      s += a * b;
+      if (absab) sa += fabs(a) * fabs(b);
+    }
+    const double c = C ? tab[C[i * ldc + j]] : 0.0;
+    D[i * ldd + j] = in_kind == OR_F16 ? oracle_double_to_f16(s + c)
+                                       : oracle_double_to_bf16(s + c);
+    if (absab) absab[i * ldabs + j] = sa;
+  }
+}
+
+/* C and D have the input's 16-bit type.  Returns 0, or -1. */
+int oracle_gemm_f16f16(int in_kind, int64_t M, int64_t N, int64_t K,
+                       const uint16_t *A, int64_t lda, const uint16_t *B,
+                       int64_t ldb, int b_layout, const uint16_t *C,
+                       int64_t ldc, uint16_t *D, int64_t ldd, double *absab,
+                       int64_t ldabs) {
+  if (in_kind != OR_F16 && in_kind != OR_BF16) return -1;
+  if (M < 0 || N < 0 || K < 0) return -1;
+  double *tab = decode_table(in_kind);
+  if (!tab) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < M; ++i)
+    h16_row(tab, in_kind, i, N, K, A, lda, B, ldb, b_layout, C, ldc, D, ldd,
+            absab, ldabs);
+  free(tab);
+  return 0;
+}
+
 /* ---- c3: INT8 inputs, INT32 accumulate -------------------------------- *
  * Exact int64 sum.  Outputs that do not fit in INT32 wrap in two's
  * complement and are counted.                                           */

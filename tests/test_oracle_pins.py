@@ -366,3 +366,99 @@ def test_broadcast_rejects_bad_groups(oracle_mod, G, abid, batch):
     A = np.zeros((batch, 16, 16), np.uint16)
     with pytest.raises(ValueError):
         oracle_mod.gemm_batched("bf16", A, A.copy(), None, group=G, abid=abid)
+
+
+# ------------------------------------- c2b FP16/BF16 -> 16-bit accumulate
+
+def round_fraction_16(q: Fraction, mant: int, bias: int, emax_field: int) -> int:
+    """Exact round-to-nearest-even of a rational to a 16-bit float format."""
+    sign = 0x8000 if q < 0 else 0
+    a = abs(q)
+    if a == 0:
+        return sign
+    emin = 1 - bias
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, emin)
+    quantum = Fraction(2) ** (e - mant)
+    m = math.floor(a / quantum)
+    rem = a / quantum - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    v = m * quantum
+    if v >= Fraction(2) ** (emax_field - bias):
+        return sign | (emax_field << mant)
+    if v < Fraction(2) ** emin:
+        return sign | int(v / Fraction(2) ** (emin - mant))
+    ev = e if v < Fraction(2) ** (e + 1) else e + 1
+    frac = int(v / Fraction(2) ** (ev - mant)) - (1 << mant)
+    return sign | ((ev + bias) << mant) | frac
+
+
+F16_FMT, BF16_FMT = (10, 15, 31), (7, 127, 255)
+
+
+@pytest.mark.parametrize("kind", ["f16", "bf16"])
+def test_double_to_16bit_rounding(oracle_mod, kind):
+    """The oracle's encoder against exact rational rounding: random values
+    over the whole range, exact ties, subnormals, the overflow boundary."""
+    fmt = F16_FMT if kind == "f16" else BF16_FMT
+    enc = oracle_mod.double_to_f16 if kind == "f16" else oracle_mod.double_to_bf16
+    rng = np.random.default_rng(21)
+    lo, hi = (-28, 17) if kind == "f16" else (-136, 128)
+    xs = list(rng.uniform(-1, 1, 3000) * np.exp2(rng.integers(lo, hi, 3000)))
+    mant, bias, _ = fmt
+    for e in (-14 if kind == "f16" else -126, -1, 0, 5):
+        for m in range(0, 12):
+            # exact ties between neighbours, and their neighbours
+            base = (1 + m * 2.0 ** -mant) * 2.0 ** e
+            tie = base + 2.0 ** (e - mant - 1)
+            xs += [tie, -tie, np.nextafter(tie, 0), np.nextafter(tie, np.inf)]
+    xs += [65504.0, 65519.9, 65520.0, 1e9, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26]
+    for x in xs:
+        want = round_fraction_16(Fraction(float(x)), *fmt)
+        assert enc(x) == want, (kind, x, hex(enc(x)), hex(want))
+    if kind == "f16":  # and against numpy's own double -> binary16
+        arr = np.array(xs[:3000])
+        assert np.array_equal(np.array([enc(x) for x in arr], np.uint16),
+                              arr.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 16), (17, 16, 17)])
+def test_acc16_exact_bruteforce(oracle_mod, dtype_in, M, N, K):
+    """Exact rational A*B + C rounded once to the 16-bit format."""
+    rng = np.random.default_rng(M * 31 + K)
+    A = f16_grid(rng, (M, K), dtype_in)
+    B = f16_grid(rng, (N, K), dtype_in)
+    rnd = synth.round_f16_bits if dtype_in == "f16" else synth.round_bf16_bits
+    C = rnd(rng.standard_normal((M, N)))
+    D = oracle_mod.gemm_acc16(dtype_in, A, B, C)
+    dec = frac_of_f16 if dtype_in == "f16" else frac_of_bf16
+    fmt = F16_FMT if dtype_in == "f16" else BF16_FMT
+    for i in range(M):
+        for j in range(N):
+            q = sum(dec(A[i, k]) * dec(B[j, k]) for k in range(K)) + dec(C[i, j])
+            assert int(D[i, j]) == round_fraction_16(q, *fmt)
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+def test_acc16_closed_forms(oracle_mod, dtype_in):
+    n = 24
+    one = 0x3C00 if dtype_in == "f16" else 0x3F80
+    eye = np.where(np.eye(n, dtype=bool), one, 0).astype(np.uint16)
+    rng = np.random.default_rng(4)
+    rnd = synth.round_f16_bits if dtype_in == "f16" else synth.round_bf16_bits
+    X = rnd(rng.uniform(-1, 1, (n, n)))
+    Z = np.zeros((n, n), np.uint16)
+    # B = I, C = 0: D = A exactly; A = I: D = B^T (column-major storage)
+    assert np.array_equal(oracle_mod.gemm_acc16(dtype_in, X, eye, Z), X)
+    assert np.array_equal(oracle_mod.gemm_acc16(dtype_in, eye, X, None), X.T)
+    # all ones, K = 64, C = 1: D = 65 (exact in both formats)
+    ones = np.full((3, 64), one, np.uint16)
+    D = oracle_mod.gemm_acc16(dtype_in, ones, ones, np.full((3, 3), one, np.uint16))
+    want = oracle_mod.double_to_f16(65.0) if dtype_in == "f16" else oracle_mod.double_to_bf16(65.0)
+    assert np.all(D == want)
