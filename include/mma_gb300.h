@@ -17,8 +17,15 @@
  *     dtype_in  dtype_acc   A, B element     C, D element
  *     MMA_F16   MMA_F32     IEEE binary16    float
  *     MMA_BF16  MMA_F32     bfloat16 bits    float
+ *     MMA_F16   MMA_F16     IEEE binary16    IEEE binary16  (16-bit accumulate)
+ *     MMA_BF16  MMA_BF16    bfloat16 bits    bfloat16 bits  (16-bit accumulate)
  *     MMA_I8    MMA_I32     signed int8      int32_t  (exact; wraps mod 2^32)
  *     MMA_F64   MMA_F64     double           double
+ *
+ * The 16-bit-accumulate pairs ("RDNA3 dense WMMA builtins", section
+ * "Builtin reference", FP16/BF16-accumulate builtins) accumulate in FP32
+ * inside and round A*B + C once to the 16-bit format (nearest, ties to
+ * even); the builtins round their 16-bit accumulator after every K step.
  *
  * Any other pair returns MMA_ERR_UNSUPPORTED.
  *
@@ -151,7 +158,7 @@ mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M, int64_t N,
  * < a_broadcast_group; batch % a_broadcast_group == 0 (else
  * MMA_ERR_INVALID_ARG).  Provided shapes: M = N = K = 16 with
  * (MMA_F16 | MMA_BF16, MMA_F32) and lda = ldb = ldc = ldd = 16; other
- * shapes or pairs return MMA_ERR_UNSUPPORTED.
+ * shapes or pairs (16-bit accumulate included) return MMA_ERR_UNSUPPORTED.
  */
 mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc, int64_t M,
                               int64_t N, int64_t K, const void *A, int64_t lda,

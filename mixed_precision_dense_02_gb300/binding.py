@@ -149,16 +149,24 @@ def _stream(stream):
     return getattr(stream, "cuda_stream", stream)
 
 
-def gemm_ex(A, B, C=None, D=None, *, b_layout: str = "col", stream=None):
+def gemm_ex(A, B, C=None, D=None, *, b_layout: str = "col", acc=None,
+            stream=None):
     """D = A @ B + C on the GPU.
 
     ``A``: (M, K) row-major; ``B`` as stored: (N, K) for column-major B
     (``b_layout="col"``) or (K, N) for row-major B; ``C``/``D``: (M, N).
     Input dtype float16/bfloat16 -> float32 output, int8 -> int32,
-    float64 -> float64.  ``D`` is allocated when not given.  Returns D.
+    float64 -> float64.  FP16/BF16 inputs accumulate into a 16-bit addend
+    and result of their own type when ``acc="same"`` or when C or D has
+    that dtype.  ``D`` is allocated when not given.  Returns D.
     """
     torch = _torch()
     dt_in, dt_acc, out_dtype = _dtypes(A)
+    if A.dtype in (torch.float16, torch.bfloat16):
+        given = D if D is not None else C
+        if acc == "same" or (acc is None and given is not None
+                             and given.dtype == A.dtype):
+            dt_acc, out_dtype = dt_in, A.dtype
     if B.dtype != A.dtype:
         raise TypeError("A and B must have the same dtype")
     M, K = A.shape
@@ -186,9 +194,9 @@ def gemm_ex(A, B, C=None, D=None, *, b_layout: str = "col", stream=None):
     return D
 
 
-def gemm(A, B, C=None, D=None, *, stream=None):
+def gemm(A, B, C=None, D=None, *, acc=None, stream=None):
     """D = A @ B + C with B given column-major as an (N, K) tensor."""
-    return gemm_ex(A, B, C, D, b_layout="col", stream=stream)
+    return gemm_ex(A, B, C, D, b_layout="col", acc=acc, stream=stream)
 
 
 def gemm_batched(A, B, C=None, D=None, *, group: int = 1, abid: int = 0,

@@ -115,6 +115,10 @@ __global__ void copy_c_kernel(const uint8_t* __restrict__ C, int64_t ldc_b,
       const uint64_t v =
           C ? *reinterpret_cast<const uint64_t*>(C + r * ldc_b + c * 8) : 0ull;
       *reinterpret_cast<uint64_t*>(D + r * ldd_b + c * 8) = v;
+    } else if (elem == 2) {
+      const uint16_t v =
+          C ? *reinterpret_cast<const uint16_t*>(C + r * ldc_b + c * 2) : 0u;
+      *reinterpret_cast<uint16_t*>(D + r * ldd_b + c * 2) = v;
     } else {
       const uint32_t v =
           C ? *reinterpret_cast<const uint32_t*>(C + r * ldc_b + c * 4) : 0u;
@@ -202,6 +206,11 @@ bool pair_sizes(int in, int acc, int64_t* in_b, int64_t* acc_b) {
     *acc_b = 4;
     return true;
   }
+  if ((in == MMA_F16 || in == MMA_BF16) && acc == in) {  // 16-bit accumulate
+    *in_b = 2;
+    *acc_b = 2;
+    return true;
+  }
   if (in == MMA_I8 && acc == MMA_I32) {
     *in_b = 1;
     *acc_b = 4;
@@ -253,16 +262,15 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
     case MMA_F16:
     case MMA_BF16: {
       const bool bf16 = dtype_in == MMA_BF16;
-      const float* Cf = static_cast<const float*>(C);
-      float* Df = static_cast<float*>(D);
+      const bool out16 = dtype_acc != MMA_F32;
       if (!b_row)
-        return launch_gemm_tc_f16(ctx, bf16, M, N, K, A, lda, B, ldb, Cf, ldc,
-                                  Df, ldd);
+        return launch_gemm_tc_f16(ctx, bf16, out16, M, N, K, A, lda, B, ldb, C,
+                                  ldc, D, ldd);
       return with_workspace(ctx, gemm_tc_rowb_workspace_bytes(N, K),
                             [&](void* ws) {
                               return launch_gemm_tc_f16_rowb(
-                                  ctx, bf16, M, N, K, A, lda, B, ldb, Cf, ldc,
-                                  Df, ldd, ws);
+                                  ctx, bf16, out16, M, N, K, A, lda, B, ldb, C,
+                                  ldc, D, ldd, ws);
                             });
     }
     case MMA_I8: {
@@ -317,7 +325,8 @@ extern "C" mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc,
   if (batch < 0 || M < 0 || N < 0 || K < 0) return MMA_ERR_INVALID_ARG;
   if (batch % G != 0) return MMA_ERR_INVALID_ARG;
   if (!(M == 16 && N == 16 && K == 16)) return MMA_ERR_UNSUPPORTED;
-  if (dtype_in != MMA_F16 && dtype_in != MMA_BF16) return MMA_ERR_UNSUPPORTED;
+  if ((dtype_in != MMA_F16 && dtype_in != MMA_BF16) || dtype_acc != MMA_F32)
+    return MMA_ERR_UNSUPPORTED;
   if (lda != 16 || ldb != 16 || ldd != 16 || (C != nullptr && ldc != 16))
     return MMA_ERR_UNSUPPORTED;
   if (batch == 0) return MMA_OK;

@@ -26,6 +26,8 @@
 // Ragged M/N/K edges: TMA zero-fills out-of-bounds box elements (so they
 // add nothing to the sum) and the epilogue predicates its stores.
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cstdlib>
 #include <mutex>
@@ -51,7 +53,9 @@ constexpr int kGroupM = 16;
 //            each chunk's FP32 accumulator holds an exact integer; the
 //            epilogue converts every chunk to INT32, sums the chunks, adds
 //            the INT32 C and stores INT32 D (wrapping modulo 2^32).
-enum class Epi { F32, I32EXACT };
+//   H16      D = acc + C rounded once to the 16-bit input format (FP16 or
+//            BF16 addend and result; FP32 accumulation inside)
+enum class Epi { F32, I32EXACT, H16 };
 
 // Chunk depth of the exact INT8 mode: |a*b| <= 2^14, so 1024 products keep
 // every partial sum within 2^24, the range where FP32 represents all
@@ -88,6 +92,27 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n,
   const int r = t - g * per_group;
   mb = first_m + r % gm;
   nb = r / gm;
+}
+
+// 16-bit float (bit pattern) <-> FP32, BF16 or FP16; rounding to nearest,
+// ties to even.
+template <bool BF16>
+__device__ __forceinline__ float half_to_f32(uint32_t bits) {
+  if constexpr (BF16)
+    return __uint_as_float(bits << 16);
+  else
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t f32x2_to_half2(float lo, float hi) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
 }
 
 // Wait without giving up on the abort flag (used only while draining).
@@ -150,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit_step = gridDim.x / CL;
   const int rank = CL > 1 ? int(cluster_ctarank()) : 0;
   const int num_kb = (K + BK - 1) / BK;
-  const int kpc = EPI == Epi::F32 ? num_kb : kb_per_chunk;
+  // only the exact INT8 mode cuts K into chunks (one accumulator each)
+  const int kpc = EPI == Epi::I32EXACT ? kb_per_chunk : num_kb;
   const int chunks = (num_kb + kpc - 1) / kpc;
 
   if (threadIdx.x == 0) {
@@ -335,7 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = smem + L::STG_OFFSET + ew * NSTG * kStgBytes;
     uint64_t* wbar = &cbar[NSTG * ew];
     const bool has_c = Cv != nullptr;
-    constexpr int NBLK = HALF / 16;
+    // columns per 64-byte staging row: 16 of 4 bytes, or 32 of 2 bytes
+    constexpr int COLS = EPI == Epi::H16 ? 32 : 16;
+    constexpr int NBLK = HALF / COLS;
     // The C of block g + PF is requested while block g is processed; its
     // ring slot last held block g + PF - NSTG, whose store must have
     // finished reading it, which leaves at most WAITN later stores pending.
@@ -387,9 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int row0, colh;
       unit_origin(u, row0, colh);
       bulk_wait_group_read<WAITN>();
-      if (row0 < M && colh + jj * 16 < N) {
+      if (row0 < M && colh + jj * COLS < N) {
         mbar_arrive_expect_tx(&wbar[b], kStgBytes);
-        tma_load_2d(&tmC, &wbar[b], stg + b * kStgBytes, colh + jj * 16, row0);
+        tma_load_2d(&tmC, &wbar[b], stg + b * kStgBytes, colh + jj * COLS,
+                    row0);
       } else {
         mbar_arrive(&wbar[b]);  // wholly outside C and D: nothing to load
       }
@@ -452,9 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        [[maybe_unused]] uint32_t r[16];
+        [[maybe_unused]] uint32_t r[COLS];
         if constexpr (EPI == Epi::F32) {
           tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
+        } else if constexpr (EPI == Epi::H16) {
+          tmem_ld_32x32b_x32(taddr + uint32_t(j * 32), r);
+        }
+        if constexpr (EPI != Epi::I32EXACT) {
           tmem_ld_wait();
           // every TMEM read of this accumulator is done: release it
           if (j == NBLK - 1) release_acc(acc);
@@ -471,7 +504,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4* p = chunk(buf, c);
           const uint4 w = has_c ? *p : make_uint4(0u, 0u, 0u, 0u);
           uint4 o;
-          if constexpr (EPI == Epi::F32) {
+          if constexpr (EPI == Epi::H16) {
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+            uint32_t ov[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float f0 = half_to_f32<BF16>(wv[e] & 0xFFFFu) +
+                               __uint_as_float(r[8 * c + 2 * e]);
+              const float f1 = half_to_f32<BF16>(wv[e] >> 16) +
+                               __uint_as_float(r[8 * c + 2 * e + 1]);
+              ov[e] = f32x2_to_half2<BF16>(f0, f1);
+            }
+            o = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+          } else if constexpr (EPI == Epi::F32) {
             o.x = __float_as_uint(__uint_as_float(w.x) + __uint_as_float(r[4 * c + 0]));
             o.y = __float_as_uint(__uint_as_float(w.y) + __uint_as_float(r[4 * c + 1]));
             o.z = __float_as_uint(__uint_as_float(w.z) + __uint_as_float(r[4 * c + 2]));
@@ -485,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *p = o;
         }
-        emit_block(buf, colh + j * 16, row0);
+        emit_block(buf, colh + j * COLS, row0);
       }
-      if constexpr (EPI == Epi::F32) {
+      if constexpr (EPI != Epi::I32EXACT) {
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -626,19 +671,17 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t K,
   return r == CUDA_SUCCESS;
 }
 
-// 2-D row-major C/D map (4-byte elements): 16 x 32 box, 64-byte swizzle,
-// matching the epilogue's staging blocks.
+// 2-D row-major C/D map: 64-byte (16 x 4-byte or 32 x 2-byte) x 32-row box,
+// 64-byte swizzle, matching the epilogue's staging blocks.
 bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
-                 int64_t ld_elems, bool is_int) {
+                 int64_t ld_elems, CUtensorMapDataType dt, int elem_bytes) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(M)};
-  cuuint64_t strides[1] = {cuuint64_t(ld_elems) * 4};
-  cuuint32_t box[2] = {16, 32};
+  cuuint64_t strides[1] = {cuuint64_t(ld_elems) * cuuint64_t(elem_bytes)};
+  cuuint32_t box[2] = {cuuint32_t(64 / elem_bytes), 32};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map,
-                   is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32
-                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  CUresult r = enc(map, dt,
                    2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -654,14 +697,19 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                  const void* C, int64_t ldc, void* D, int64_t ldd) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   static_assert(L::ALLOC <= 232448, "shared memory per CTA");
-  constexpr bool kInt = EPI == Epi::I32EXACT;
+  const CUtensorMapDataType cd_type =
+      EPI == Epi::I32EXACT ? CU_TENSOR_MAP_DATA_TYPE_INT32
+      : EPI == Epi::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+      : BF16               ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int cd_bytes = EPI == Epi::H16 ? 2 : 4;
   CUtensorMap ta, tb, tc, td;
   if (!make_kmajor_map(&ta, A, K, M, lda, BM, BF16) ||
       !make_kmajor_map(&tb, B, K, N, ldb, BN / CL, BF16) ||
-      !make_cd_map(&td, D, N, M, ldd, kInt))
+      !make_cd_map(&td, D, N, M, ldd, cd_type, cd_bytes))
     return MMA_ERR_LAUNCH;
   if (C != nullptr) {
-    if (!make_cd_map(&tc, C, N, M, ldc, kInt)) return MMA_ERR_LAUNCH;
+    if (!make_cd_map(&tc, C, N, M, ldc, cd_type, cd_bytes)) return MMA_ERR_LAUNCH;
   } else {
     tc = td;  // never read: the kernel loads C only when it is given
   }
@@ -809,17 +857,28 @@ mma_status_t launch_transpose_b(const Ctx& ctx, const void* B, int64_t ldb,
 
 }  // namespace
 
-mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, int64_t M,
-                                int64_t N, int64_t K, const void* A,
-                                int64_t lda, const void* B, int64_t ldb,
-                                const float* C, int64_t ldc, float* D,
-                                int64_t ldd) {
+template <Epi EPI>
+mma_status_t dispatch_f16(const Ctx& ctx, bool pdl, bool bf16, int64_t M,
+                          int64_t N, int64_t K, const void* A, int64_t lda,
+                          const void* B, int64_t ldb, const void* C,
+                          int64_t ldc, void* D, int64_t ldd) {
   const int bn = tile_n(ctx, M, N);
   const int cl = cluster_size(M, N, K);
-  return bf16 ? dispatch<true, Epi::F32>(ctx, false, bn, cl, M, N, K, A, lda,
-                                         B, ldb, C, ldc, D, ldd)
-              : dispatch<false, Epi::F32>(ctx, false, bn, cl, M, N, K, A, lda,
-                                          B, ldb, C, ldc, D, ldd);
+  return bf16 ? dispatch<true, EPI>(ctx, pdl, bn, cl, M, N, K, A, lda, B, ldb,
+                                    C, ldc, D, ldd)
+              : dispatch<false, EPI>(ctx, pdl, bn, cl, M, N, K, A, lda, B,
+                                     ldb, C, ldc, D, ldd);
+}
+
+mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, bool out16,
+                                int64_t M, int64_t N, int64_t K, const void* A,
+                                int64_t lda, const void* B, int64_t ldb,
+                                const void* C, int64_t ldc, void* D,
+                                int64_t ldd) {
+  return out16 ? dispatch_f16<Epi::H16>(ctx, false, bf16, M, N, K, A, lda, B,
+                                        ldb, C, ldc, D, ldd)
+               : dispatch_f16<Epi::F32>(ctx, false, bf16, M, N, K, A, lda, B,
+                                        ldb, C, ldc, D, ldd);
 }
 
 size_t gemm_tc_rowb_workspace_bytes(int64_t N, int64_t K) {
@@ -827,21 +886,19 @@ size_t gemm_tc_rowb_workspace_bytes(int64_t N, int64_t K) {
   return size_t(N) * size_t(ldw) * 2;
 }
 
-mma_status_t launch_gemm_tc_f16_rowb(const Ctx& ctx, bool bf16, int64_t M,
-                                     int64_t N, int64_t K, const void* A,
-                                     int64_t lda, const void* B, int64_t ldb,
-                                     const float* C, int64_t ldc, float* D,
-                                     int64_t ldd, void* workspace) {
+mma_status_t launch_gemm_tc_f16_rowb(const Ctx& ctx, bool bf16, bool out16,
+                                     int64_t M, int64_t N, int64_t K,
+                                     const void* A, int64_t lda, const void* B,
+                                     int64_t ldb, const void* C, int64_t ldc,
+                                     void* D, int64_t ldd, void* workspace) {
   const int64_t ldw = (K + 7) / 8 * 8;
   uint16_t* W = static_cast<uint16_t*>(workspace);
   const mma_status_t st = launch_transpose_b<false>(ctx, B, ldb, K, N, W, ldw);
   if (st != MMA_OK) return st;
-  const int bn = tile_n(ctx, M, N);
-  const int cl = cluster_size(M, N, K);
-  return bf16 ? dispatch<true, Epi::F32>(ctx, true, bn, cl, M, N, K, A, lda,
-                                         W, ldw, C, ldc, D, ldd)
-              : dispatch<false, Epi::F32>(ctx, true, bn, cl, M, N, K, A, lda,
-                                          W, ldw, C, ldc, D, ldd);
+  return out16 ? dispatch_f16<Epi::H16>(ctx, true, bf16, M, N, K, A, lda, W,
+                                        ldw, C, ldc, D, ldd)
+               : dispatch_f16<Epi::F32>(ctx, true, bf16, M, N, K, A, lda, W,
+                                        ldw, C, ldc, D, ldd);
 }
 
 size_t gemm_i8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {

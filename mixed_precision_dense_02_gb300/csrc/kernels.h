@@ -27,11 +27,12 @@ struct Ctx {
   }
 };
 
-// tcgen05 GEMM, FP16/BF16 inputs, FP32 accumulate, column-major B.
-mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, int64_t M,
-                                int64_t N, int64_t K, const void* A,
+// tcgen05 GEMM, FP16/BF16 inputs, column-major B; C and D are FP32, or
+// with out16 of the input's 16-bit type (FP32 accumulation, one rounding).
+mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, bool out16,
+                                int64_t M, int64_t N, int64_t K, const void* A,
                                 int64_t lda, const void* B, int64_t ldb,
-                                const float* C, int64_t ldc, float* D,
+                                const void* C, int64_t ldc, void* D,
                                 int64_t ldd);
 
 // Exact INT8 GEMM on the tcgen05 BF16 pipe.  `workspace` holds
@@ -47,11 +48,11 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
 // tcgen05 FP16/BF16 GEMM with row-major B: B is transposed into
 // `workspace` (gemm_tc_rowb_workspace_bytes(N, K) bytes) first.
 size_t gemm_tc_rowb_workspace_bytes(int64_t N, int64_t K);
-mma_status_t launch_gemm_tc_f16_rowb(const Ctx& ctx, bool bf16, int64_t M,
-                                     int64_t N, int64_t K, const void* A,
-                                     int64_t lda, const void* B, int64_t ldb,
-                                     const float* C, int64_t ldc, float* D,
-                                     int64_t ldd, void* workspace);
+mma_status_t launch_gemm_tc_f16_rowb(const Ctx& ctx, bool bf16, bool out16,
+                                     int64_t M, int64_t N, int64_t K,
+                                     const void* A, int64_t lda, const void* B,
+                                     int64_t ldb, const void* C, int64_t ldc,
+                                     void* D, int64_t ldd, void* workspace);
 
 // INT8 GEMM on the warp-level IMMA pipe, column-major B.
 mma_status_t launch_gemm_i8_imma(const Ctx& ctx, int64_t M, int64_t N,
@@ -75,7 +76,7 @@ mma_status_t launch_batched16(const Ctx& ctx, bool bf16, int64_t batch,
 // sm_103 device).
 bool current_ctx(void* stream, Ctx* out);
 
-// K == 0: D = C (or 0), elementwise, element size 4 or 8 bytes.
+// K == 0: D = C (or 0), elementwise, element size 2, 4 or 8 bytes.
 mma_status_t launch_copy_c(const Ctx& ctx, int64_t M, int64_t N,
                            int elem_bytes, const void* C, int64_t ldc, void* D,
                            int64_t ldd);

@@ -77,6 +77,30 @@ def check(dtype_in: str, got: np.ndarray, want: np.ndarray,
             f"max err/bound {np.max(err / np.maximum(bound, 1e-300)):.3f}")
 
 
+def decode16(bits: np.ndarray, dtype_in: str) -> np.ndarray:
+    bits = np.asarray(bits, np.uint16)
+    if dtype_in == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def check16(dtype_in: str, got_bits, want_bits, absab, what: str = "") -> None:
+    """16-bit accumulate: |D - D_ref| <= 1e-3 (|A||B|)_ij + 1e-6 + one ulp of
+    the 16-bit result (2^-10 |D_ref| for FP16, 2^-7 for BF16): the GPU rounds
+    its FP32 sum to 16 bits, the oracle its double sum."""
+    g = decode16(got_bits, dtype_in)
+    w = decode16(want_bits, dtype_in)
+    ulp = 2.0 ** -10 if dtype_in == "f16" else 2.0 ** -7
+    bound = 1e-3 * absab + 1e-6 + ulp * np.abs(w)
+    err = np.abs(g - w)
+    bad = (err > bound) | ~np.isfinite(g)
+    if np.any(bad):
+        idx = np.argwhere(bad)
+        i = tuple(idx[0])
+        raise AssertionError(f"{what}: {len(idx)} of {g.size} outside tolerance; "
+                             f"first at {i}: got {g[i]!r} want {w[i]!r} bound {bound[i]:.3e}")
+
+
 def oracle_ref(g, rows=None, cols=None):
     """Oracle D (and |A||B|) for GemmInputs g, optionally on a sub-block."""
     A, B, C = g.A, g.B, g.C

@@ -60,6 +60,9 @@ def g(*, din=BF16, dacc=F32, M=64, N=64, K=64, A=P, lda=64, B=P, ldb=64,
 
 @pytest.mark.parametrize("kw,code", [
     (dict(din=BF16, dacc=I32), UNSUP),
+    (dict(din=BF16, dacc=F16), UNSUP),
+    (dict(din=F16, dacc=BF16), UNSUP),
+    (dict(din=I8, dacc=I8), UNSUP),
     (dict(din=F32, dacc=F32), UNSUP),
     (dict(din=I8, dacc=F32), UNSUP),
     (dict(din=F64, dacc=F32), UNSUP),
@@ -103,6 +106,10 @@ def test_valid_arguments_reach_the_device_check(lib):
     assert g(layout=1) == NODEV
     assert g(din=I8, dacc=I32, layout=1, lda=64, ldb=64) == NODEV
     assert g(din=F16, dacc=F32, layout=1) == NODEV
+    # 16-bit accumulate pairs
+    assert g(din=F16, dacc=F16, ldc=64, ldd=64) == NODEV
+    assert g(din=BF16, dacc=BF16, layout=1) == NODEV
+    assert g(din=BF16, dacc=BF16, ldd=68) == MISAL   # 68 * 2 bytes
     assert g(K=0, A=0, B=0) == NODEV
     assert g(C=0) == NODEV
 
@@ -120,6 +127,9 @@ def b(*, din=BF16, dacc=F32, M=16, N=16, K=16, A=P, B=P, C=P, D=Q, ld=16,
     (dict(M=32), UNSUP), (dict(K=8), UNSUP),
     (dict(din=I8, dacc=I32), UNSUP), (dict(din=F64, dacc=F64), UNSUP),
     (dict(din=BF16, dacc=I32), UNSUP),
+    (dict(din=BF16, dacc=F16), UNSUP),
+    (dict(din=F16, dacc=BF16), UNSUP),
+    (dict(din=I8, dacc=I8), UNSUP),
     (dict(ld=32), UNSUP),
     (dict(A=0), INVALID), (dict(D=0), INVALID),
     (dict(A=P + 8), MISAL), (dict(C=P + 4), MISAL),

@@ -14,7 +14,7 @@ import pytest
 import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import check, dev_padded, oracle_ref, to_dev
+from helpers import check, check16, dev_padded, oracle_ref, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -193,6 +193,90 @@ def test_i8_tensor_pipe_shapes_exact(M, N, K):
     g = synth.gemm_inputs(f"i8tc_{M}_{N}_{K}", "i8", M, N, K)
     want, _ = oracle_ref(g)
     check("i8", run_gemm(g, pad=1), want, None, f"i8 {M}x{N}x{K}")
+
+
+# ----------------------------------------- FP16/BF16 with 16-bit accumulate
+
+def acc16_inputs(name, dtype_in, M, N, K, b_layout="col"):
+    g = synth.gemm_inputs(name, dtype_in, M, N, K, dist="uniform", b_layout=b_layout)
+    rnd = synth.round_f16_bits if dtype_in == "f16" else synth.round_bf16_bits
+    return synth.GemmInputs(dtype_in, M, N, K, g.A, g.B, rnd(g.C.astype(np.float64)),
+                            b_layout)
+
+
+def run_gemm16(g, *, pad=0, use_c=True, inplace=False):
+    import torch
+    A = dev_padded(g.A, g.dtype_in, extra=pad)
+    B = dev_padded(g.B, g.dtype_in, extra=pad)
+    C = dev_padded(g.C, g.dtype_in, extra=pad) if use_c else None
+    D = C if inplace else dev_padded(np.zeros_like(g.C), g.dtype_in, extra=pad + 1)
+    out = binding.gemm_ex(A, B, C, D, b_layout=g.b_layout, acc="same")
+    torch.cuda.synchronize()
+    return out.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle16(g, rows=None, cols=None):
+    A, B, C = g.A, g.B, g.C
+    if rows is not None:
+        A, C = np.ascontiguousarray(A[rows]), np.ascontiguousarray(C[rows])
+    if cols is not None:
+        B = np.ascontiguousarray(B[cols] if g.b_layout == "col" else B[:, cols])
+        C = np.ascontiguousarray(C[:, cols])
+    return oracle.gemm_acc16(g.dtype_in, A, B, C, b_layout=g.b_layout, want_absab=True)
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (16, 16, 16), (127, 129, 65),
+                                   (256, 256, 256), (333, 257, 1000), (1000, 136, 520),
+                                   (300, 264, 2500)])
+def test_acc16_small_shapes(dtype_in, M, N, K):
+    g = acc16_inputs(f"acc16_{M}_{N}_{K}", dtype_in, M, N, K)
+    want, ab = oracle16(g)
+    check16(dtype_in, run_gemm16(g), want, ab, f"{dtype_in}->{dtype_in} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+def test_acc16_padding_no_c_in_place_row_b(dtype_in):
+    M, N, K = 260, 392, 328
+    g = acc16_inputs("acc16_pad", dtype_in, M, N, K)
+    want, ab = oracle16(g)
+    check16(dtype_in, run_gemm16(g, pad=3), want, ab, "padded")
+    check16(dtype_in, run_gemm16(g, inplace=True), want, ab, "in place")
+    g0 = synth.GemmInputs(dtype_in, M, N, K, g.A, g.B, np.zeros_like(g.C))
+    want0, ab0 = oracle16(g0)
+    check16(dtype_in, run_gemm16(g, use_c=False), want0, ab0, "C = NULL")
+    gr = acc16_inputs("acc16_row", dtype_in, M, N, K, b_layout="row")
+    want, ab = oracle16(gr)
+    check16(dtype_in, run_gemm16(gr, pad=1), want, ab, "row-major B")
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+def test_acc16_exact_closed_form(dtype_in):
+    """All ones, K = 256, integer C: D = K + C exactly representable."""
+    M, N, K = 300, 260, 256
+    one = np.uint16(0x3C00 if dtype_in == "f16" else 0x3F80)
+    rnd = synth.round_f16_bits if dtype_in == "f16" else synth.round_bf16_bits
+    Cv = np.random.default_rng(2).integers(-64, 64, (M, N)).astype(np.float64)
+    g = synth.GemmInputs(dtype_in, M, N, K, np.full((M, K), one), np.full((N, K), one),
+                         rnd(Cv))
+    assert np.array_equal(run_gemm16(g), rnd(Cv + K))
+
+
+def test_acc16_full_size_sampled():
+    """BF16 -> BF16 at 8192^3 (the large BF16 workload's shape), sampled."""
+    import torch
+    M = N = K = 8192
+    g = acc16_inputs("acc16_8192", "bf16", M, N, K)
+    D = binding.gemm_ex(to_dev(g.A, "bf16"), to_dev(g.B, "bf16"), to_dev(g.C, "bf16"),
+                        acc="same")
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(99)
+    rows = np.unique(np.append(rng.choice(M, 64, replace=False), M - 1))
+    cols = np.unique(np.append(rng.choice(N, 64, replace=False), N - 1))
+    got = D[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()]
+    got = got.view(torch.int16).cpu().numpy().view(np.uint16)
+    want, ab = oracle16(g, rows, cols)
+    check16("bf16", got, want, ab, "bf16->bf16 8192^3")
 
 
 # ------------------------------------------------------------ batched
