@@ -206,7 +206,7 @@ def workload_meta(name):
     if w["kind"] == "gemm":
         ops = 2.0 * w["M"] * w["N"] * w["K"]
         isz = {"f16": 2, "bf16": 2, "i8": 1, "f64": 8}[w["dtype_in"]]
-        osz = 8 if w["dtype_in"] == "f64" else 4
+        osz = 8 if w["dtype_in"] == "f64" else (2 if w.get("acc16") else 4)
         nbytes = (w["M"] * w["K"] + w["N"] * w["K"]) * isz + 2 * w["M"] * w["N"] * osz
     else:
         ops = 2.0 * w["batch"] * w["M"] * w["N"] * w["K"]
@@ -269,9 +269,11 @@ class GpuWorkload:
         if w["kind"] == "gemm":
             g = synth.gemm_inputs(name, w["dtype_in"], w["M"], w["N"], w["K"],
                                   dist=w.get("dist", "normal"),
-                                  b_layout=w.get("b_layout", "col"), seed=seed)
+                                  b_layout=w.get("b_layout", "col"), seed=seed,
+                                  acc16=w.get("acc16", False))
             host = [g.A, g.B, g.C]
             self.b_layout = g.b_layout
+            self.acc16 = w.get("acc16", False)
         else:
             bi = synth.batched_inputs(name, w["dtype_in"], w["batch"], w["M"],
                                       w["N"], w["K"], group=w["group"],
@@ -280,6 +282,7 @@ class GpuWorkload:
             host = [bi.A, bi.B, bi.C]
         self.dtype_in = w["dtype_in"]
         self.host = [self._pinned(x) for x in host]
+        self.acc = "same" if getattr(self, "acc16", False) else None
         # A, B, C and D of one set; rotate enough sets that more than twice
         # the L2 capacity is touched between two uses of the same set
         per_set = (sum(t.numel() * t.element_size() for t in self.host)
@@ -316,7 +319,7 @@ class GpuWorkload:
     def call(self, A, B, C, D):
         w = self.w
         if w["kind"] == "gemm":
-            self.binding.gemm_ex(A, B, C, D, b_layout=self.b_layout)
+            self.binding.gemm_ex(A, B, C, D, b_layout=self.b_layout, acc=self.acc)
         else:
             self.binding.gemm_batched(A, B, C, D, group=w["group"], abid=w["abid"])
 
@@ -442,8 +445,9 @@ def oracle_sample_step(name, rows, seed=0):
         g = _sample_inputs_cache(name, seed)
         A = np.ascontiguousarray(g.A[:rows])
         C = np.ascontiguousarray(g.C[:rows])
+        fn = oracle.gemm_acc16 if w.get("acc16") else oracle.gemm
         t = time.perf_counter()
-        oracle.gemm(g.dtype_in, A, g.B, C, b_layout=g.b_layout)
+        fn(g.dtype_in, A, g.B, C, b_layout=g.b_layout)
         dt = time.perf_counter() - t
         return dt, 2.0 * rows * w["N"] * w["K"]
     bi = _sample_inputs_cache(name, seed)
@@ -466,7 +470,7 @@ def _sample_inputs_cache(name, seed):
             _INPUT_CACHE[name] = synth.gemm_inputs(
                 name, w["dtype_in"], w["M"], w["N"], w["K"],
                 dist=w.get("dist", "normal"), b_layout=w.get("b_layout", "col"),
-                seed=seed)
+                seed=seed, acc16=w.get("acc16", False))
         else:
             _INPUT_CACHE[name] = synth.batched_inputs(
                 name, w["dtype_in"], w["batch"], w["M"], w["N"], w["K"],

@@ -146,12 +146,14 @@ def _floats(dist: str, seed: int, stream: int, n: int) -> np.ndarray:
 
 def gemm_inputs(workload: str, dtype_in: str, M: int, N: int, K: int, *,
                 dist: str = "normal", c_dist: str = "normal", seed: int = 0,
-                b_layout: str = "col", c_int_bound: int = 1 << 20) -> GemmInputs:
+                b_layout: str = "col", c_int_bound: int = 1 << 20,
+                acc16: bool = False) -> GemmInputs:
     """Inputs of one D = A*B + C problem.
 
     ``dist`` is the A/B distribution ("uniform" on [-1, 1) or "normal"),
     rounded to the input type; ``c_dist`` the C distribution (FP32/FP64:
-    normal; INT32: uniform over [-c_int_bound, c_int_bound]).
+    normal; INT32: uniform over [-c_int_bound, c_int_bound]).  With
+    ``acc16`` (FP16/BF16 only) C is rounded to the input's 16-bit type.
     """
     sA, sB, sC = (stream_id(workload, t) for t in "ABC")
     bshape = (N, K) if b_layout == "col" else (K, N)
@@ -159,7 +161,8 @@ def gemm_inputs(workload: str, dtype_in: str, M: int, N: int, K: int, *,
         rnd = round_f16_bits if dtype_in == "f16" else round_bf16_bits
         A = rnd(_floats(dist, seed, sA, M * K)).reshape(M, K)
         B = rnd(_floats(dist, seed, sB, N * K)).reshape(bshape)
-        C = _floats(c_dist, seed, sC, M * N).astype(np.float32).reshape(M, N)
+        C = _floats(c_dist, seed, sC, M * N)
+        C = (rnd(C) if acc16 else C.astype(np.float32)).reshape(M, N)
     elif dtype_in == "i8":
         A = int8_uniform(seed, sA, M * K).reshape(M, K)
         B = int8_uniform(seed, sB, N * K).reshape(bshape)
@@ -231,4 +234,7 @@ WORKLOADS = {
     "gemm_bf16_skinny_16384x128x4096": dict(kind="gemm", dtype_in="bf16",
                                             M=16384, N=128, K=4096,
                                             dist="normal"),
+    # BF16 -> BF16 accumulate (16-bit addend and result), large square shape
+    "gemm_bf16_acc16_8192": dict(kind="gemm", dtype_in="bf16", M=8192, N=8192,
+                                 K=8192, dist="normal", acc16=True),
 }
