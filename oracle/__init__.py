@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_double_to_f16.argtypes = [ctypes.c_double]
         L.oracle_double_to_bf16.restype = ctypes.c_uint16
         L.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+        L.oracle_gemm_i8i32_ex.restype = _i64
+        L.oracle_gemm_i8i32_ex.argtypes = [_i64, _i64, _i64, _p, _i64, _int, _p,
+                                           _i64, _int, _int, _p, _i64, _p, _i64,
+                                           _int]
         L.oracle_gemm_i8i32.restype = _i64
         L.oracle_gemm_i8i32.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64,
                                         _int, _p, _i64, _p, _i64]
@@ -188,6 +192,28 @@ def gemm(dtype_in: str, A, B, C=None, *, b_layout: str = "col",
     raise ValueError(f"unsupported dtype_in {dtype_in!r}")
 
 
+def gemm_i8_ex(A, B, C=None, *, clamp: bool = False, b_layout: str = "col"):
+    """8-bit integer D = A*B + C with A and B signed (int8 arrays) or
+    unsigned (uint8 arrays) independently ("RDNA3 dense WMMA builtins" --
+    INT8 and UINT8 inputs, a_neg/b_neg and clamp).  Returns (D int32, the
+    number of outputs whose exact value overflowed INT32); overflowing
+    outputs saturate with ``clamp``, else wrap modulo 2^32."""
+    for t in (A, B):
+        if t.dtype not in (np.int8, np.uint8):
+            raise TypeError("8-bit integer operands are int8 or uint8 arrays")
+    M, N, K = _shape(A, B, b_layout)
+    Ci = None if C is None else np.asarray(C, dtype=np.int32)
+    D = np.empty((M, N), np.int32)
+    ov = lib().oracle_gemm_i8i32_ex(M, N, K, _ptr(A), _ld(A),
+                                    int(A.dtype == np.int8), _ptr(B), _ld(B),
+                                    int(B.dtype == np.int8), _LAYOUT[b_layout],
+                                    _ptr(Ci), _ld(Ci) if Ci is not None else 0,
+                                    _ptr(D), N, int(bool(clamp)))
+    if ov < 0:
+        raise RuntimeError("oracle_gemm_i8i32_ex failed")
+    return D, int(ov)
+
+
 def gemm_acc16(dtype_in: str, A, B, C=None, *, b_layout: str = "col",
                want_absab: bool = False):
     """D = A*B + C with a 16-bit addend and result of the input's type
@@ -256,6 +282,6 @@ def gemm_batched(dtype_in: str, A, B, C, *, group: int = 1, abid: int = 0,
     return D
 
 
-__all__ = ["gemm", "gemm_acc16", "gemm_batched", "num_threads",
+__all__ = ["gemm", "gemm_i8_ex", "gemm_acc16", "gemm_batched", "num_threads",
            "f16_to_double", "bf16_to_double", "double_to_f16",
            "double_to_bf16", "lib"]

@@ -249,6 +249,43 @@ int64_t oracle_gemm_i8i32(int64_t M, int64_t N, int64_t K, const int8_t *A,
   return overflow;
 }
 
+/* ---- c3b: INT8 / UINT8 inputs in any signedness, optional clamp ------- *
+ * "RDNA3 dense WMMA builtins" -- INT8 and UINT8 inputs: a_neg / b_neg select
+ * signed (else unsigned) 8-bit A / B; `clamp` saturates the INT32 result on
+ * overflow (else it wraps modulo 2^32).  Exact int64 sum plus C.  Returns
+ * the number of outputs whose exact value did not fit in INT32.          */
+int64_t oracle_gemm_i8i32_ex(int64_t M, int64_t N, int64_t K, const void *A,
+                             int64_t lda, int a_signed, const void *B,
+                             int64_t ldb, int b_signed, int b_layout,
+                             const int32_t *C, int64_t ldc, int32_t *D,
+                             int64_t ldd, int clamp) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  const int8_t *As = (const int8_t *)A;
+  const uint8_t *Au = (const uint8_t *)A;
+  const int8_t *Bs = (const int8_t *)B;
+  const uint8_t *Bu = (const uint8_t *)B;
+  int64_t overflow = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : overflow)
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      int64_t s = 0;
+      for (int64_t k = 0; k < K; ++k) {
+        const int64_t ia = i * lda + k, ib = b_index(b_layout, k, j, ldb);
+        const int64_t a = a_signed ? (int64_t)As[ia] : (int64_t)Au[ia];
+        const int64_t b = b_signed ? (int64_t)Bs[ib] : (int64_t)Bu[ib];
+        s += a * b;
+      }
+      int64_t d = s + (C ? (int64_t)C[i * ldc + j] : 0);
+      if (d < INT32_MIN || d > INT32_MAX) {
+        ++overflow;
+        if (clamp) d = d < 0 ? INT32_MIN : INT32_MAX;
+      }
+      D[i * ldd + j] = (int32_t)(uint32_t)(uint64_t)d;
+    }
+  }
+  return overflow;
+}
+
 /* ---- c4: FP64, compensated dot product (Dot2) ------------------------- */
 
 /* Knuth's TwoSum: s + e == a + b exactly, s = fl(a + b). */

@@ -462,3 +462,53 @@ def test_acc16_closed_forms(oracle_mod, dtype_in):
     D = oracle_mod.gemm_acc16(dtype_in, ones, ones, np.full((3, 3), one, np.uint16))
     want = oracle_mod.double_to_f16(65.0) if dtype_in == "f16" else oracle_mod.double_to_bf16(65.0)
     assert np.all(D == want)
+
+
+# ------------------------------- c3b INT8/UINT8 signedness and clamp
+
+@pytest.mark.parametrize("sa,sb", [(True, True), (True, False), (False, True), (False, False)])
+def test_i8_ex_bruteforce_signedness(oracle_mod, sa, sb):
+    rng = np.random.default_rng(int(sa) * 2 + int(sb))
+    M, N, K = 7, 9, 33
+    A = rng.integers(-128, 128, (M, K)).astype(np.int8)
+    B = rng.integers(-128, 128, (N, K)).astype(np.int8)
+    if not sa:
+        A = A.view(np.uint8)
+    if not sb:
+        B = B.view(np.uint8)
+    C = rng.integers(-(1 << 20), 1 << 20, (M, N)).astype(np.int32)
+    D, ov = oracle_mod.gemm_i8_ex(A, B, C)
+    assert ov == 0
+    for i in range(M):
+        for j in range(N):
+            s = sum(int(A[i, k]) * int(B[j, k]) for k in range(K)) + int(C[i, j])
+            assert int(D[i, j]) == s
+    # signed x signed agrees with the plain INT8 oracle
+    if sa and sb:
+        assert np.array_equal(D, oracle_mod.gemm("i8", A, B, C))
+
+
+def test_i8_ex_extremes_and_clamp(oracle_mod):
+    M, N, K = 3, 4, 4096
+    u = np.full((M, K), 255, np.uint8)
+    v = np.full((N, K), 255, np.uint8)
+    C = np.zeros((M, N), np.int32)
+    D, ov = oracle_mod.gemm_i8_ex(u, v, C)
+    assert ov == 0 and np.all(D == K * 255 * 255)     # 266,342,400 < 2^31
+    # push past INT32: C near the top, positive products
+    Ctop = np.full((M, N), 2 ** 31 - 1000, np.int32)
+    D, ov = oracle_mod.gemm_i8_ex(u, v, Ctop)
+    assert ov == M * N
+    exact = 2 ** 31 - 1000 + K * 65025
+    assert np.all(D == np.int32(np.int64(exact) - 2 ** 32))          # wraps
+    D, ov = oracle_mod.gemm_i8_ex(u, v, Ctop, clamp=True)
+    assert ov == M * N and np.all(D == 2 ** 31 - 1)                   # saturates
+    # and below INT32 with a mixed-sign product
+    neg = np.full((M, K), -128, np.int8)
+    Cbot = np.full((M, N), -(2 ** 31) + 5, np.int32)
+    D, ov = oracle_mod.gemm_i8_ex(neg, v, Cbot, clamp=True)
+    assert np.all(D == -(2 ** 31))
+    # no overflow: clamp changes nothing
+    D1, _ = oracle_mod.gemm_i8_ex(neg, v, None)
+    D2, _ = oracle_mod.gemm_i8_ex(neg, v, None, clamp=True)
+    assert np.array_equal(D1, D2) and np.all(D1 == -128 * 255 * K)
