@@ -241,9 +241,15 @@ def kernel_source(w):
             "f64": "mixed_precision_dense_02_gb300/csrc/gemm_f64.cu"}[w["dtype_in"]]
 
 
+def i8_plain(w):
+    """Signed x signed 8-bit inputs without saturation (mma_gemm's INT8)."""
+    return w.get("a_signed", True) and w.get("b_signed", True) and not w.get("clamp")
+
+
 def i8_on_tensor_pipe(w):
-    """INT8 problems with M*N*K >= 2^24 run on the tcgen05 BF16 pipe."""
-    return float(w["M"]) * w["N"] * w["K"] >= 2.0 ** 24
+    """INT8 problems with M*N*K >= 2^24, and every unsigned, mixed-sign or
+    saturating one, run on the tcgen05 BF16 pipe."""
+    return not i8_plain(w) or float(w["M"]) * w["N"] * w["K"] >= 2.0 ** 24
 
 
 def launches_per_call(w):
@@ -267,10 +273,7 @@ class GpuWorkload:
         self.dev = torch.device("cuda", torch.cuda.current_device())
         w = self.w
         if w["kind"] == "gemm":
-            g = synth.gemm_inputs(name, w["dtype_in"], w["M"], w["N"], w["K"],
-                                  dist=w.get("dist", "normal"),
-                                  b_layout=w.get("b_layout", "col"), seed=seed,
-                                  acc16=w.get("acc16", False))
+            g = synth.workload_gemm_inputs(name, seed)
             host = [g.A, g.B, g.C]
             self.b_layout = g.b_layout
             self.acc16 = w.get("acc16", False)
@@ -318,7 +321,10 @@ class GpuWorkload:
 
     def call(self, A, B, C, D):
         w = self.w
-        if w["kind"] == "gemm":
+        if w["kind"] == "gemm" and w["dtype_in"] == "i8" and not i8_plain(w):
+            self.binding.gemm_i8_ex(A, B, C, D, clamp=w.get("clamp", False),
+                                    b_layout=self.b_layout)
+        elif w["kind"] == "gemm":
             self.binding.gemm_ex(A, B, C, D, b_layout=self.b_layout, acc=self.acc)
         else:
             self.binding.gemm_batched(A, B, C, D, group=w["group"], abid=w["abid"])
@@ -445,9 +451,13 @@ def oracle_sample_step(name, rows, seed=0):
         g = _sample_inputs_cache(name, seed)
         A = np.ascontiguousarray(g.A[:rows])
         C = np.ascontiguousarray(g.C[:rows])
-        fn = oracle.gemm_acc16 if w.get("acc16") else oracle.gemm
         t = time.perf_counter()
-        fn(g.dtype_in, A, g.B, C, b_layout=g.b_layout)
+        if g.dtype_in == "i8" and not i8_plain(w):
+            oracle.gemm_i8_ex(A, g.B, C, clamp=w.get("clamp", False),
+                              b_layout=g.b_layout)
+        else:
+            fn = oracle.gemm_acc16 if w.get("acc16") else oracle.gemm
+            fn(g.dtype_in, A, g.B, C, b_layout=g.b_layout)
         dt = time.perf_counter() - t
         return dt, 2.0 * rows * w["N"] * w["K"]
     bi = _sample_inputs_cache(name, seed)
@@ -467,10 +477,7 @@ def _sample_inputs_cache(name, seed):
     if name not in _INPUT_CACHE:
         w = synth.WORKLOADS[name]
         if w["kind"] == "gemm":
-            _INPUT_CACHE[name] = synth.gemm_inputs(
-                name, w["dtype_in"], w["M"], w["N"], w["K"],
-                dist=w.get("dist", "normal"), b_layout=w.get("b_layout", "col"),
-                seed=seed, acc16=w.get("acc16", False))
+            _INPUT_CACHE[name] = synth.workload_gemm_inputs(name, seed)
         else:
             _INPUT_CACHE[name] = synth.batched_inputs(
                 name, w["dtype_in"], w["batch"], w["M"], w["N"], w["K"],
@@ -539,12 +546,16 @@ def run_reference(args, dist):
 
 
 def _dtype_tag(w):
-    return {"f16": "f16", "bf16": "bf16", "i8": "i8", "f64": "f64"}[w["dtype_in"]]
+    if w["dtype_in"] == "i8":
+        sa, sb = w.get("a_signed", True), w.get("b_signed", True)
+        return "i8" if sa and sb else ("u8" if not (sa or sb) else "u8/i8")
+    return {"f16": "f16", "bf16": "bf16", "f64": "f64"}[w["dtype_in"]]
 
 
 def _config(name, w, l2):
     cfg = {"workload": name, "l2": l2}
-    for k in ("M", "N", "K", "batch", "group", "abid", "dtype_in"):
+    for k in ("M", "N", "K", "batch", "group", "abid", "dtype_in", "a_signed",
+              "b_signed", "clamp"):
         if k in w:
             cfg[k] = w[k]
     if w["kind"] == "gemm":

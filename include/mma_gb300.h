@@ -135,6 +135,34 @@ mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M, int64_t N,
                          void *D, int64_t ldd, void *stream);
 
 /*
+ * mma_gemm_i8_ex -- 8-bit integer D = A * B + C with INT32 C and D, each of
+ * A and B signed or unsigned, and optional saturation.
+ *
+ * Passage: "RDNA3 dense WMMA builtins", sections "INT32-accumulate
+ * builtins" (integer inputs signed or unsigned, chosen per operand by
+ * a_neg and b_neg) and "INT8 and UINT8 inputs" (the iu8 builtin:
+ * srcA x srcB + srcC, and `clamp`: saturate the output on overflow).
+ *
+ * a_neg, b_neg : nonzero -- A (B) holds int8 values in [-128, 127];
+ *                zero    -- uint8 values in [0, 255].
+ * clamp        : zero    -- D is the exact value modulo 2^32 (wrapping, as
+ *                           mma_gemm's INT8 product);
+ *                nonzero -- D is the exact value of A*B + C, saturated once
+ *                           to [INT32_MIN, INT32_MAX].
+ * Other arguments, layouts, alignment rules and status codes are those of
+ * mma_gemm_ex with dtype_in = MMA_I8, dtype_acc = MMA_I32 (A, B: 1-byte
+ * elements; layout_b MMA_COL_MAJOR or MMA_ROW_MAJOR).  Signed x signed
+ * without clamp is exactly mma_gemm_ex; every other combination runs on the
+ * tensor pipe and grows the library's scratch buffer like it
+ * ((M + N) * roundup(K, 8) * 2 bytes; MMA_ERR_NO_MEMORY if it cannot).
+ */
+mma_status_t mma_gemm_i8_ex(int64_t M, int64_t N, int64_t K, const void *A,
+                            int64_t lda, int a_neg, const void *B, int64_t ldb,
+                            int b_neg, int layout_b, const void *C,
+                            int64_t ldc, void *D, int64_t ldd, int clamp,
+                            void *stream);
+
+/*
  * mma_gemm_batched -- `batch` independent M x N x K products with A-block
  * broadcast:
  *

@@ -8,7 +8,7 @@ Python binding over it (argument marshalling only) plus the seeded input
 generator.  The CUDA library is loaded on first use; if it is missing, every
 compute call raises -- there is no CPU fallback.
 """
-from .binding import (gemm, gemm_ex, gemm_batched, library_path, load,  # noqa: F401
+from .binding import (gemm, gemm_ex, gemm_batched, gemm_i8_ex, library_path, load,  # noqa: F401
                       MMAError)
 
-__all__ = ["gemm", "gemm_ex", "gemm_batched", "load", "library_path", "MMAError"]
+__all__ = ["gemm", "gemm_ex", "gemm_batched", "gemm_i8_ex", "load", "library_path", "MMAError"]

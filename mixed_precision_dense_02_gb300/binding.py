@@ -31,6 +31,8 @@ SIGNATURES = {
     "mma_gemm_batched": (_int, [_int, _int, _i64, _i64, _i64, _p, _i64, _p,
                                 _i64, _p, _i64, _p, _i64, _i64, _int, _int,
                                 _p]),
+    "mma_gemm_i8_ex": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64,
+                              _int, _int, _p, _i64, _p, _i64, _int, _p]),
     "mma_gemm_i8_noalloc": (_int, [_i64, _i64, _i64, _p, _i64, _p, _i64, _p,
                                    _i64, _p, _i64, _p]),
     "mma_device_status": (_int, [_p]),
@@ -101,6 +103,13 @@ def mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C, ldc, D,
     return load().mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B,
                                    ldb, C, ldc, D, ldd, batch, group, abid,
                                    stream)
+
+
+def mma_gemm_i8_ex(M, N, K, A, lda, a_neg, B, ldb, b_neg, layout_b, C, ldc,
+                   D, ldd, clamp, stream) -> int:
+    """8-bit integer GEMM, int8 or uint8 per operand, optional saturation."""
+    return load().mma_gemm_i8_ex(M, N, K, A, lda, a_neg, B, ldb, b_neg,
+                                 layout_b, C, ldc, D, ldd, clamp, stream)
 
 
 def mma_gemm_i8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd,
@@ -191,6 +200,44 @@ def gemm_ex(A, B, C=None, D=None, *, b_layout: str = "col", acc=None,
                      0 if C is None else _ld(C), D.data_ptr(), _ld(D),
                      _stream(stream))
     _check("mma_gemm_ex", st)
+    return D
+
+
+def gemm_i8_ex(A, B, C=None, D=None, *, clamp: bool = False,
+               b_layout: str = "col", stream=None):
+    """8-bit integer D = A @ B + C (INT32 C and D) on the GPU.
+
+    Each of ``A`` and ``B`` is a torch.int8 (signed) or torch.uint8
+    (unsigned) tensor; shapes and layouts as in ``gemm_ex``.  With ``clamp``
+    D is the exact result saturated to the INT32 range, else it wraps
+    modulo 2^32.  ``D`` is allocated when not given.  Returns D.
+    """
+    torch = _torch()
+    sign = {torch.int8: 1, torch.uint8: 0}
+    if A.dtype not in sign or B.dtype not in sign:
+        raise TypeError("A and B must be int8 or uint8 tensors")
+    M, K = A.shape
+    if b_layout == "col":
+        N, Kb = B.shape
+        layout = MMA_COL_MAJOR
+    elif b_layout == "row":
+        Kb, N = B.shape
+        layout = MMA_ROW_MAJOR
+    else:
+        raise ValueError(b_layout)
+    if Kb != K:
+        raise ValueError(f"K mismatch: {K} vs {Kb}")
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.int32, device=A.device)
+    for t in (C, D):
+        if t is not None and (t.dtype != torch.int32 or tuple(t.shape) != (M, N)):
+            raise ValueError("C/D must be (M, N) int32")
+    st = mma_gemm_i8_ex(M, N, K, A.data_ptr(), _ld(A), sign[A.dtype],
+                        B.data_ptr(), _ld(B), sign[B.dtype], layout,
+                        None if C is None else C.data_ptr(),
+                        0 if C is None else _ld(C), D.data_ptr(), _ld(D),
+                        int(bool(clamp)), _stream(stream))
+    _check("mma_gemm_i8_ex", st)
     return D
 
 

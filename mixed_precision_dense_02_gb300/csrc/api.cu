@@ -226,13 +226,14 @@ bool pair_sizes(int in, int acc, int64_t* in_b, int64_t* acc_b) {
 
 }  // namespace
 
-extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
-                                    int64_t N, int64_t K, const void* A,
-                                    int64_t lda, const void* B, int64_t ldb,
-                                    int layout_b, const void* C, int64_t ldc,
-                                    void* D, int64_t ldd, void* stream) {
-  int64_t eb = 0, ea = 0;
-  if (!pair_sizes(dtype_in, dtype_acc, &eb, &ea)) return MMA_ERR_UNSUPPORTED;
+namespace {
+
+// Argument checks shared by the dense entry points (element sizes eb of A
+// and B, ea of C and D).  Returns MMA_OK when the call should go ahead.
+mma_status_t check_dense_args(int64_t eb, int64_t ea, int layout_b, int64_t M,
+                              int64_t N, int64_t K, const void* A, int64_t lda,
+                              const void* B, int64_t ldb, const void* C,
+                              int64_t ldc, const void* D, int64_t ldd) {
   if (layout_b != MMA_COL_MAJOR && layout_b != MMA_ROW_MAJOR)
     return MMA_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
@@ -251,6 +252,22 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
   if (!aligned16(D) || !ld_ok(ldd, ea)) return MMA_ERR_MISALIGNED;
   if (C != nullptr && (!aligned16(C) || !ld_ok(ldc, ea)))
     return MMA_ERR_MISALIGNED;
+  return MMA_OK;
+}
+
+}  // namespace
+
+extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
+                                    int64_t N, int64_t K, const void* A,
+                                    int64_t lda, const void* B, int64_t ldb,
+                                    int layout_b, const void* C, int64_t ldc,
+                                    void* D, int64_t ldd, void* stream) {
+  int64_t eb = 0, ea = 0;
+  if (!pair_sizes(dtype_in, dtype_acc, &eb, &ea)) return MMA_ERR_UNSUPPORTED;
+  const mma_status_t chk = check_dense_args(eb, ea, layout_b, M, N, K, A, lda,
+                                            B, ldb, C, ldc, D, ldd);
+  if (chk != MMA_OK || M == 0 || N == 0) return chk;
+  const bool b_row = layout_b == MMA_ROW_MAJOR;
   int dev = -1;
   const DeviceInfo* info = device_info(&dev);
   if (!info) return MMA_ERR_NO_DEVICE;
@@ -282,9 +299,9 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
       if (b_row || double(M) * double(N) * double(K) >= kI8TensorCoreMinWork)
         return with_workspace(ctx, gemm_i8_tc_workspace_bytes(M, N, K),
                               [&](void* ws) {
-                                return launch_gemm_i8_tc(ctx, M, N, K, A8, lda,
-                                                         B8, ldb, Ci, ldc, Di,
-                                                         ldd, ws, b_row);
+                                return launch_gemm_i8_tc(
+                                    ctx, M, N, K, A8, lda, B8, ldb, Ci, ldc,
+                                    Di, ldd, ws, b_row, true, true, false);
                               });
       return launch_gemm_i8_imma(ctx, M, N, K, A8, lda, B8, ldb, Ci, ldc, Di,
                                  ldd);
@@ -297,6 +314,40 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
     default:
       return MMA_ERR_UNSUPPORTED;
   }
+}
+
+extern "C" mma_status_t mma_gemm_i8_ex(int64_t M, int64_t N, int64_t K,
+                                       const void* A, int64_t lda, int a_neg,
+                                       const void* B, int64_t ldb, int b_neg,
+                                       int layout_b, const void* C,
+                                       int64_t ldc, void* D, int64_t ldd,
+                                       int clamp, void* stream) {
+  const bool a_signed = a_neg != 0, b_signed = b_neg != 0;
+  // signed x signed without saturation is the plain INT8 product
+  if (a_signed && b_signed && clamp == 0)
+    return mma_gemm_ex(MMA_I8, MMA_I32, M, N, K, A, lda, B, ldb, layout_b, C,
+                       ldc, D, ldd, stream);
+  const mma_status_t chk = check_dense_args(1, 4, layout_b, M, N, K, A, lda,
+                                            B, ldb, C, ldc, D, ldd);
+  if (chk != MMA_OK || M == 0 || N == 0) return chk;
+  int dev = -1;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info) return MMA_ERR_NO_DEVICE;
+  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  attach_profile(ctx);
+  if (K == 0) {
+    // D = C: a 32-bit C is in range, so saturation changes nothing
+    return launch_copy_c(ctx, M, N, 4, C, ldc, D, ldd);
+  }
+  const bool b_row = layout_b == MMA_ROW_MAJOR;
+  return with_workspace(
+      ctx, gemm_i8_tc_workspace_bytes(M, N, K), [&](void* ws) {
+        return launch_gemm_i8_tc(ctx, M, N, K, static_cast<const int8_t*>(A),
+                                 lda, static_cast<const int8_t*>(B), ldb,
+                                 static_cast<const int32_t*>(C), ldc,
+                                 static_cast<int32_t*>(D), ldd, ws, b_row,
+                                 a_signed, b_signed, clamp != 0);
+      });
 }
 
 extern "C" mma_status_t mma_gemm(int dtype_in, int dtype_acc, int64_t M,

@@ -55,12 +55,30 @@ constexpr int kGroupM = 16;
 //            the INT32 C and stores INT32 D (wrapping modulo 2^32).
 //   H16      D = acc + C rounded once to the 16-bit input format (FP16 or
 //            BF16 addend and result; FP32 accumulation inside)
-enum class Epi { F32, I32EXACT, H16 };
+//   I32SAT   as I32EXACT, but D is the exact value of A*B + C saturated to
+//            the INT32 range: the chunk sums are gathered without wrapping
+//            (INT32 registers for up to kSatFlush chunks, folded into 64-bit
+//            sums held in spare tensor-memory columns every kSatFlush chunks
+//            and after the last), and each 64-bit sum plus C is clamped
+//            once.  BN = 128 only (the 64-bit sums take the other half of
+//            TMEM).
+enum class Epi { F32, I32EXACT, H16, I32SAT };
 
-// Chunk depth of the exact INT8 mode: |a*b| <= 2^14, so 1024 products keep
-// every partial sum within 2^24, the range where FP32 represents all
-// integers.
+constexpr bool int_mode(Epi e) { return e == Epi::I32EXACT || e == Epi::I32SAT; }
+
+// Chunk depth of the exact 8-bit integer modes: every partial sum must stay
+// within 2^24 in magnitude, the range where FP32 represents all integers.
+// |a*b| <= 2^14 (signed x signed), 128 * 255 (mixed) or 255^2 (unsigned x
+// unsigned), so 1024, 512 or 256 products per chunk.
 constexpr int kI8ChunkK = 1024;
+constexpr int chunk_k(bool a_signed, bool b_signed) {
+  return a_signed && b_signed ? 1024 : (a_signed || b_signed) ? 512 : 256;
+}
+
+// I32SAT: 127 chunk sums of magnitude <= 2^24 stay below 2^31, so the INT32
+// registers hold them exactly; every kSatFlush chunks they are folded into
+// the 64-bit partial sums.
+constexpr int kSatFlush = 127;
 
 // Epilogue staging: each epilogue warp owns NSTG 32-row x 16-column blocks
 // of 4-byte elements (64-byte rows, 64-byte TMA swizzle), a ring through
@@ -152,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    int kb_per_chunk, unsigned* status) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   constexpr int HALF = BN / 2;  // columns per epilogue warp
+  static_assert(EPI != Epi::I32SAT || BN == 128, "I32SAT uses 128-wide tiles");
+  // I32SAT: the two accumulators take columns [0, 256); the 64-bit partial
+  // sums of column half h the 128 columns from 256 + 128 h.
+  constexpr uint32_t TMEM_COLS = EPI == Epi::I32SAT ? 512u : L::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -175,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit_step = gridDim.x / CL;
   const int rank = CL > 1 ? int(cluster_ctarank()) : 0;
   const int num_kb = (K + BK - 1) / BK;
-  // only the exact INT8 mode cuts K into chunks (one accumulator each)
-  const int kpc = EPI == Epi::I32EXACT ? kb_per_chunk : num_kb;
+  // only the exact integer modes cut K into chunks (one accumulator each)
+  const int kpc = int_mode(EPI) ? kb_per_chunk : num_kb;
   const int chunks = (num_kb + kpc - 1) / kpc;
 
   if (threadIdx.x == 0) {
@@ -202,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     if constexpr (CL == 1) {
-      tmem_alloc(tmem_slot, L::TMEM_COLS);
+      tmem_alloc(tmem_slot, TMEM_COLS);
       tmem_relinquish();
     } else {
-      tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
       tmem_relinquish_pair();
     }
   }
@@ -391,6 +413,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[a]), 0));
       }
     };
+    // I32SAT: this warp's 64-bit partial sums, 16 columns per 32-column
+    // group (low words, then high words), in the TMEM columns beyond the
+    // two accumulators.
+    [[maybe_unused]] const uint32_t xaddr =
+        tmem_base + uint32_t(2 * BN + h * 2 * HALF) + (uint32_t(q * 32) << 16);
+    // Add the INT32 chunk sums to the 64-bit partial sums (or start them)
+    // and clear the INT32 sums.
+    [[maybe_unused]] auto fold_partials = [&](bool started,
+                                              uint32_t (&ia)[int_mode(EPI) ? HALF : 1]) {
+      if constexpr (EPI == Epi::I32SAT) {
+#pragma unroll
+        for (int c = 0; c < HALF / 16; ++c) {
+          uint32_t x[32];
+          if (started) {
+            tmem_ld_32x32b_x32(xaddr + uint32_t(c * 32), x);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = 0u;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int64_t v = int64_t((uint64_t(x[16 + e]) << 32) | x[e]) +
+                              int64_t(int32_t(ia[c * 16 + e]));
+            x[e] = uint32_t(uint64_t(v));
+            x[16 + e] = uint32_t(uint64_t(v) >> 32);
+            ia[c * 16 + e] = 0u;
+          }
+          tmem_st_32x32b_x32(xaddr + uint32_t(c * 32), x);
+        }
+        tmem_st_wait();
+      }
+    };
     // Store staging block `buf` to D at (col, row0), or close an empty
     // bulk group when the block lies wholly outside D.
     auto emit_block = [&](uint8_t* buf, int col, int row0) {
@@ -429,9 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = first_unit; u < units && ok; u += unit_step) {
       int row0, colh;
       unit_origin(u, row0, colh);
-      [[maybe_unused]] uint32_t iacc[EPI == Epi::I32EXACT ? HALF : 1];
+      [[maybe_unused]] uint32_t iacc[int_mode(EPI) ? HALF : 1];
+      // I32SAT: whether this unit's 64-bit sums in TMEM hold chunks yet
+      [[maybe_unused]] bool folded = false;
       uint32_t taddr = 0;
-      if constexpr (EPI == Epi::I32EXACT) {
+      if constexpr (int_mode(EPI)) {
 #pragma unroll
         for (int j = 0; j < HALF; ++j) iacc[j] = 0u;
         for (int ch = 0; ch < chunks; ++ch) {
@@ -455,6 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           release_acc(acc);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
+          if constexpr (EPI == Epi::I32SAT) {
+            // every kSatFlush chunks, and after the last one
+            if ((ch + 1) % kSatFlush == 0 || ch + 1 == chunks) {
+              fold_partials(folded, iacc);
+              folded = true;
+            }
+          }
         }
         if (!ok) break;
       } else {
@@ -481,13 +545,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        [[maybe_unused]] uint32_t r[COLS];
+        [[maybe_unused]] uint32_t r[EPI == Epi::I32SAT ? 32 : COLS];
         if constexpr (EPI == Epi::F32) {
           tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
         } else if constexpr (EPI == Epi::H16) {
           tmem_ld_32x32b_x32(taddr + uint32_t(j * 32), r);
+        } else if constexpr (EPI == Epi::I32SAT) {
+          // the 64-bit sums of this block's 16 columns (every chunk folded
+          // in): low words in r[0..15], high words in r[16..31]
+          tmem_ld_32x32b_x32(xaddr + uint32_t(j * 32), r);
+          tmem_ld_wait();
         }
-        if constexpr (EPI != Epi::I32EXACT) {
+        if constexpr (!int_mode(EPI)) {
           tmem_ld_wait();
           // every TMEM read of this accumulator is done: release it
           if (j == NBLK - 1) release_acc(acc);
@@ -521,18 +590,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             o.y = __float_as_uint(__uint_as_float(w.y) + __uint_as_float(r[4 * c + 1]));
             o.z = __float_as_uint(__uint_as_float(w.z) + __uint_as_float(r[4 * c + 2]));
             o.w = __float_as_uint(__uint_as_float(w.w) + __uint_as_float(r[4 * c + 3]));
-          } else {
+          } else if constexpr (EPI == Epi::I32EXACT) {
             // INT32 adds wrap modulo 2^32
             o.x = w.x + iacc[j * 16 + 4 * c + 0];
             o.y = w.y + iacc[j * 16 + 4 * c + 1];
             o.z = w.z + iacc[j * 16 + 4 * c + 2];
             o.w = w.w + iacc[j * 16 + 4 * c + 3];
+          } else {
+            // exact 64-bit sum, saturated once to the INT32 range
+            auto sat = [&](uint32_t cw, int e) {
+              int64_t v = int64_t((uint64_t(r[16 + e]) << 32) | r[e]) +
+                          int64_t(int32_t(cw));
+              v = v < int64_t(INT32_MIN) ? int64_t(INT32_MIN) : v;
+              v = v > int64_t(INT32_MAX) ? int64_t(INT32_MAX) : v;
+              return uint32_t(int32_t(v));
+            };
+            o.x = sat(w.x, 4 * c + 0);
+            o.y = sat(w.y, 4 * c + 1);
+            o.z = sat(w.z, 4 * c + 2);
+            o.w = sat(w.w, 4 * c + 3);
           }
           *p = o;
         }
         emit_block(buf, colh + j * COLS, row0);
       }
-      if constexpr (EPI != Epi::I32EXACT) {
+      if constexpr (!int_mode(EPI)) {
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -550,35 +632,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     if constexpr (CL == 1)
-      tmem_dealloc(tmem_base, L::TMEM_COLS);
+      tmem_dealloc(tmem_base, TMEM_COLS);
     else
-      tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
-// int8 -> bfloat16, exactly (every int8 value has at most 8 significant
-// bits), with full-rate integer/FP32 ALU operations instead of the slower
-// int-to-float conversion unit: for the byte x of v, u = x ^ 0x80 = v + 128
-// (two's complement); the float whose bits are 0x4B0000uu is 2^23 + u, so
-// subtracting 2^23 + 128 leaves v exactly, and its top 16 bits are the
-// bfloat16 of v.
-__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo_byte) {
+// 8-bit integer -> bfloat16, exactly (every int8 and uint8 value has at
+// most 8 significant bits), with full-rate integer/FP32 ALU operations
+// instead of the slower int-to-float conversion unit.  For a byte x, let
+// u = x ^ flip: the byte itself for uint8 (flip = 0), x ^ 0x80 = v + 128
+// for int8 v (flip = 0x80, two's complement).  The float whose bits are
+// 0x4B0000uu is 2^23 + u, so subtracting `bias` (2^23, or 2^23 + 128 for
+// int8) leaves the value exactly, and its top 16 bits are its bfloat16.
+struct ByteCode {
+  uint32_t flip;  // xor applied to all four bytes of a word
+  float bias;
+};
+__device__ __forceinline__ ByteCode byte_code(bool is_signed) {
+  return is_signed ? ByteCode{0x80808080u, 8388736.0f}   // 2^23 + 128
+                   : ByteCode{0u, 8388608.0f};           // 2^23
+}
+
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo_byte,
+                                                   ByteCode bc) {
   // byte_perm picks byte `lo_byte` of w (made unsigned by the xor) into the
   // low byte of 0x4B000000
-  const uint32_t f0 = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u + lo_byte);
-  const uint32_t f1 = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7541u + lo_byte);
-  const float v0 = __uint_as_float(f0) - 8388736.0f;  // 2^23 + 128
-  const float v1 = __uint_as_float(f1) - 8388736.0f;
+  const uint32_t f0 = __byte_perm(w ^ bc.flip, 0x4B000000u, 0x7540u + lo_byte);
+  const uint32_t f1 = __byte_perm(w ^ bc.flip, 0x4B000000u, 0x7541u + lo_byte);
+  const float v0 = __uint_as_float(f0) - bc.bias;
+  const float v1 = __uint_as_float(f1) - bc.bias;
   // high halves of the two floats: (bf16(v1) << 16) | bf16(v0)
   return __byte_perm(__float_as_uint(v0), __float_as_uint(v1), 0x7632);
 }
 
-__device__ __forceinline__ void i8x16_to_bf16(const int4 v, uint4& o0, uint4& o1) {
+// The bfloat16 bit pattern of one 8-bit integer (plain conversion; used
+// for ragged row tails and by the transposing pass).
+__device__ __forceinline__ uint16_t byte_to_bf16(uint8_t x, bool is_signed) {
+  const float f = is_signed ? float(int8_t(x)) : float(x);
+  return uint16_t(__float_as_uint(f) >> 16);
+}
+
+__device__ __forceinline__ void i8x16_to_bf16(const int4 v, ByteCode bc,
+                                              uint4& o0, uint4& o1) {
   const uint32_t w[4] = {uint32_t(v.x), uint32_t(v.y), uint32_t(v.z),
                          uint32_t(v.w)};
   uint32_t o[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) o[j] = i8x2_to_bf16x2(w[j >> 1], 2 * (j & 1));
+  for (int j = 0; j < 8; ++j) o[j] = i8x2_to_bf16x2(w[j >> 1], 2 * (j & 1), bc);
   o0 = make_uint4(o[0], o[1], o[2], o[3]);
   o1 = make_uint4(o[4], o[5], o[6], o[7]);
 }
@@ -593,7 +694,9 @@ constexpr int kConvUnroll = 4;
 __global__ void __launch_bounds__(kConvThreads)
     i8_to_bf16_kernel(const int8_t* __restrict__ A, int64_t lda, int M,
                       const int8_t* __restrict__ B, int64_t ldb, int N, int K,
-                      uint16_t* __restrict__ W, int64_t ldw) {
+                      uint16_t* __restrict__ W, int64_t ldw, bool a_signed,
+                      bool b_signed) {
+  const ByteCode bca = byte_code(a_signed), bcb = byte_code(b_signed);
   const int64_t cpr = (K + 15) / 16;  // chunks per row
   const int64_t total = int64_t(M + N) * cpr;
   constexpr int64_t kSpan = int64_t(kConvThreads) * kConvUnroll;
@@ -620,15 +723,17 @@ __global__ void __launch_bounds__(kConvThreads)
       const int64_t r = i / cpr;
       const int c = int(i - r * cpr) * 16;
       uint16_t* dst = W + r * ldw + c;
+      const bool is_a = r < M;
       if (c + 16 <= K) {
         uint4 o0, o1;
-        i8x16_to_bf16(v[u], o0, o1);
+        i8x16_to_bf16(v[u], is_a ? bca : bcb, o0, o1);
         reinterpret_cast<uint4*>(dst)[0] = o0;
         reinterpret_cast<uint4*>(dst)[1] = o1;
       } else {
-        const int8_t* src = r < M ? A + r * lda + c : B + (r - M) * ldb + c;
+        const int8_t* src = is_a ? A + r * lda + c : B + (r - M) * ldb + c;
+        const bool sgn = is_a ? a_signed : b_signed;
         for (int j = 0; c + j < K; ++j)
-          dst[j] = uint16_t(__float_as_uint(float(src[j])) >> 16);
+          dst[j] = byte_to_bf16(uint8_t(src[j]), sgn);
       }
     }
   }
@@ -694,11 +799,12 @@ bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
 template <int BN, int STAGES, bool BF16, Epi EPI, int CL, int NSTG>
 mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb,
-                 const void* C, int64_t ldc, void* D, int64_t ldd) {
+                 const void* C, int64_t ldc, void* D, int64_t ldd,
+                 int kb_per_chunk) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   static_assert(L::ALLOC <= 232448, "shared memory per CTA");
   const CUtensorMapDataType cd_type =
-      EPI == Epi::I32EXACT ? CU_TENSOR_MAP_DATA_TYPE_INT32
+      int_mode(EPI)        ? CU_TENSOR_MAP_DATA_TYPE_INT32
       : EPI == Epi::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
       : BF16               ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -758,7 +864,7 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   ctx.mark_start();
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, C, ldc, D, ldd, int(M), int(N),
-                         int(K), kI8ChunkK / BK, ctx.status);
+                         int(K), kb_per_chunk, ctx.status);
   ctx.mark_stop();
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -802,25 +908,28 @@ template <bool BF16, Epi EPI>
 mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
                       int64_t N, int64_t K, const void* A, int64_t lda,
                       const void* B, int64_t ldb, const void* C, int64_t ldc,
-                      void* D, int64_t ldd) {
+                      void* D, int64_t ldd, int kb_per_chunk = kI8ChunkK / BK) {
   // Shared memory: operand ring (a pair stages half of B per CTA) plus the
   // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
   // tiles, whose 48 KB stages leave room for only 4 of them).
-  if (bn == 256)
-    return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-                   : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
-  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd)
-                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+  if constexpr (EPI != Epi::I32SAT) {
+    if (bn == 256)
+      return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk)
+                     : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk);
+  }
+  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk)
+                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk);
 }
 
 // Row-major B (K x N, N contiguous) -> K-major copy W (N rows of K, leading
 // dimension ldw) of 16-bit elements, through 64 x 64 shared-memory tiles so
-// that both the reads and the writes are coalesced.  With I8 the int8
-// values are widened to bfloat16 on the way (exactly).
+// that both the reads and the writes are coalesced.  With I8 the 8-bit
+// integers (int8, or uint8 unless b_signed) are widened to bfloat16 on the
+// way (exactly).
 template <bool I8>
 __global__ void __launch_bounds__(256)
     transpose_b_kernel(const void* __restrict__ Bv, int64_t ldb, int K, int N,
-                       uint16_t* __restrict__ W, int64_t ldw) {
+                       uint16_t* __restrict__ W, int64_t ldw, bool b_signed) {
   __shared__ uint16_t tile[64][66];  // [k][n], padded
   const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
@@ -829,7 +938,8 @@ __global__ void __launch_bounds__(256)
     uint16_t v = 0;
     if (k < K && n < N) {
       if constexpr (I8)
-        v = uint16_t(__float_as_uint(float(static_cast<const int8_t*>(Bv)[int64_t(k) * ldb + n])) >> 16);
+        v = byte_to_bf16(static_cast<const uint8_t*>(Bv)[int64_t(k) * ldb + n],
+                         b_signed);
       else
         v = static_cast<const uint16_t*>(Bv)[int64_t(k) * ldb + n];
     }
@@ -846,12 +956,12 @@ __global__ void __launch_bounds__(256)
 template <bool I8>
 mma_status_t launch_transpose_b(const Ctx& ctx, const void* B, int64_t ldb,
                                 int64_t K, int64_t N, uint16_t* W,
-                                int64_t ldw) {
+                                int64_t ldw, bool b_signed = true) {
   const int64_t gy = (K + 63) / 64;
   if (gy > 65535) return MMA_ERR_UNSUPPORTED;
   const dim3 grid{unsigned((N + 63) / 64), unsigned(gy), 1u};
   transpose_b_kernel<I8><<<grid, 256, 0, ctx.stream>>>(B, ldb, int(K), int(N),
-                                                        W, ldw);
+                                                        W, ldw, b_signed);
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }
 
@@ -910,14 +1020,16 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
                                int64_t K, const int8_t* A, int64_t lda,
                                const int8_t* B, int64_t ldb, const int32_t* C,
                                int64_t ldc, int32_t* D, int64_t ldd,
-                               void* workspace, bool b_row_major) {
+                               void* workspace, bool b_row_major,
+                               bool a_signed, bool b_signed, bool clamp) {
   const int64_t ldw = (K + 7) / 8 * 8;
   uint16_t* W = static_cast<uint16_t*>(workspace);
   uint16_t* Bw = W + M * ldw;
   if (b_row_major) {
     // B widened while transposed; the A pass below then runs last, so the
     // GEMM's programmatic dependency is on it (and on B by stream order).
-    const mma_status_t st = launch_transpose_b<true>(ctx, B, ldb, K, N, Bw, ldw);
+    const mma_status_t st =
+        launch_transpose_b<true>(ctx, B, ldb, K, N, Bw, ldw, b_signed);
     if (st != MMA_OK) return st;
   }
   const int64_t rows = b_row_major ? M : M + N;
@@ -926,11 +1038,17 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
   int64_t blocks = (chunks + span - 1) / span;
   if (blocks > int64_t(ctx.num_sms) * 8) blocks = int64_t(ctx.num_sms) * 8;
   i8_to_bf16_kernel<<<int(blocks), kConvThreads, 0, ctx.stream>>>(
-      A, lda, int(M), B, ldb, b_row_major ? 0 : int(N), int(K), W, ldw);
+      A, lda, int(M), B, ldb, b_row_major ? 0 : int(N), int(K), W, ldw,
+      a_signed, b_signed);
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
+  const int kpc = chunk_k(a_signed, b_signed) / BK;
+  if (clamp)
+    return dispatch<true, Epi::I32SAT>(ctx, true, 128, cluster_size(M, N, K),
+                                       M, N, K, W, ldw, Bw, ldw, C, ldc, D,
+                                       ldd, kpc);
   return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N),
                                        cluster_size(M, N, K), M, N, K, W, ldw,
-                                       Bw, ldw, C, ldc, D, ldd);
+                                       Bw, ldw, C, ldc, D, ldd, kpc);
 }
 
 }  // namespace mmagb

@@ -35,15 +35,18 @@ mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, bool out16,
                                 const void* C, int64_t ldc, void* D,
                                 int64_t ldd);
 
-// Exact INT8 GEMM on the tcgen05 BF16 pipe.  `workspace` holds
+// Exact 8-bit integer GEMM on the tcgen05 BF16 pipe.  `workspace` holds
 // gemm_i8_tc_workspace_bytes(M, N, K) bytes of device scratch for the BF16
-// copies of A and B (B is transposed into it when b_row_major).
+// copies of A and B (B is transposed into it when b_row_major).  A and B
+// hold int8 (a_signed / b_signed) or uint8 values; D wraps modulo 2^32, or
+// with `clamp` is the exact result saturated to the INT32 range.
 size_t gemm_i8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
                                int64_t K, const int8_t* A, int64_t lda,
                                const int8_t* B, int64_t ldb, const int32_t* C,
                                int64_t ldc, int32_t* D, int64_t ldd,
-                               void* workspace, bool b_row_major);
+                               void* workspace, bool b_row_major,
+                               bool a_signed, bool b_signed, bool clamp);
 
 // tcgen05 FP16/BF16 GEMM with row-major B: B is transposed into
 // `workspace` (gemm_tc_rowb_workspace_bytes(N, K) bytes) first.

@@ -108,5 +108,6 @@ extern "C" mma_status_t mma_gemm_i8_noalloc(int64_t M, int64_t N, int64_t K,
                            static_cast<const int8_t*>(B), ldb,
                            static_cast<const int32_t*>(C), ldc,
                            static_cast<int32_t*>(D), ldd, scratch,
-                           /*b_row_major=*/false);
+                           /*b_row_major=*/false, /*a_signed=*/true,
+                           /*b_signed=*/true, /*clamp=*/false);
 }

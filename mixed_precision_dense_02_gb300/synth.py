@@ -13,6 +13,7 @@ distribution code:
 * N(0, 1):          Box-Muller, u1 in (0, 1], u2 in [0, 1):
                     r = sqrt(-2 ln u1), (r cos 2 pi u2, r sin 2 pi u2)
 * int8 over [-128, 127] inclusive: one raw byte per value (exactly uniform)
+* uint8 over [0, 255] inclusive: the same bytes read unsigned
 * int32 over [-b, b] inclusive: rejection sampling on the smallest power-of-
   two range covering 2b + 1 values (exactly uniform)
 * rounding to FP16 / BF16: round to nearest, ties to even, from the double.
@@ -73,6 +74,11 @@ def int8_uniform(seed: int, stream: int, n: int) -> np.ndarray:
     return raw_u64(seed, stream, words).view(np.int8)[:n].copy()
 
 
+def uint8_uniform(seed: int, stream: int, n: int) -> np.ndarray:
+    """n uint8 values uniform over the integers [0, 255]."""
+    return int8_uniform(seed, stream, n).view(np.uint8)
+
+
 def int_uniform(seed: int, stream: int, n: int, lo: int, hi: int) -> np.ndarray:
     """n int64 values uniform over the integers [lo, hi] (rejection sampling)."""
     span = hi - lo + 1
@@ -122,7 +128,8 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 @dataclass
 class GemmInputs:
-    dtype_in: str          # "f16" | "bf16" | "i8" | "f64"
+    dtype_in: str          # "f16" | "bf16" | "i8" | "f64" ("i8": A and B
+                           # are int8 or uint8 arrays, see gemm_inputs)
     M: int
     N: int
     K: int
@@ -147,13 +154,16 @@ def _floats(dist: str, seed: int, stream: int, n: int) -> np.ndarray:
 def gemm_inputs(workload: str, dtype_in: str, M: int, N: int, K: int, *,
                 dist: str = "normal", c_dist: str = "normal", seed: int = 0,
                 b_layout: str = "col", c_int_bound: int = 1 << 20,
-                acc16: bool = False) -> GemmInputs:
+                c_int_range: tuple | None = None, acc16: bool = False,
+                a_signed: bool = True, b_signed: bool = True) -> GemmInputs:
     """Inputs of one D = A*B + C problem.
 
     ``dist`` is the A/B distribution ("uniform" on [-1, 1) or "normal"),
     rounded to the input type; ``c_dist`` the C distribution (FP32/FP64:
-    normal; INT32: uniform over [-c_int_bound, c_int_bound]).  With
-    ``acc16`` (FP16/BF16 only) C is rounded to the input's 16-bit type.
+    normal; INT32: uniform over [-c_int_bound, c_int_bound], or over the
+    inclusive ``c_int_range`` when given).  With ``acc16`` (FP16/BF16 only)
+    C is rounded to the input's 16-bit type.  For "i8", ``a_signed`` /
+    ``b_signed`` False draw that operand as uint8 over [0, 255].
     """
     sA, sB, sC = (stream_id(workload, t) for t in "ABC")
     bshape = (N, K) if b_layout == "col" else (K, N)
@@ -164,9 +174,10 @@ def gemm_inputs(workload: str, dtype_in: str, M: int, N: int, K: int, *,
         C = _floats(c_dist, seed, sC, M * N)
         C = (rnd(C) if acc16 else C.astype(np.float32)).reshape(M, N)
     elif dtype_in == "i8":
-        A = int8_uniform(seed, sA, M * K).reshape(M, K)
-        B = int8_uniform(seed, sB, N * K).reshape(bshape)
-        C = int_uniform(seed, sC, M * N, -c_int_bound, c_int_bound).astype(np.int32).reshape(M, N)
+        A = (int8_uniform if a_signed else uint8_uniform)(seed, sA, M * K).reshape(M, K)
+        B = (int8_uniform if b_signed else uint8_uniform)(seed, sB, N * K).reshape(bshape)
+        lo, hi = c_int_range if c_int_range else (-c_int_bound, c_int_bound)
+        C = int_uniform(seed, sC, M * N, lo, hi).astype(np.int32).reshape(M, N)
     elif dtype_in == "f64":
         A = _floats(dist, seed, sA, M * K).reshape(M, K)
         B = _floats(dist, seed, sB, N * K).reshape(bshape)
@@ -237,4 +248,23 @@ WORKLOADS = {
     # BF16 -> BF16 accumulate (16-bit addend and result), large square shape
     "gemm_bf16_acc16_8192": dict(kind="gemm", dtype_in="bf16", M=8192, N=8192,
                                  K=8192, dist="normal", acc16=True),
+    # unsigned x unsigned 8-bit inputs with INT32 saturation; C spans the
+    # whole INT32 range, so the outputs whose C lies within the product sum
+    # of the top (about 1.6% of them) saturate
+    "gemm_u8_4096_clamp": dict(kind="gemm", dtype_in="i8", M=4096, N=4096,
+                               K=4096, a_signed=False, b_signed=False,
+                               clamp=True,
+                               c_int_range=(-(1 << 31), (1 << 31) - 1)),
 }
+
+
+def workload_gemm_inputs(name: str, seed: int = 0) -> GemmInputs:
+    """The inputs of a named GEMM workload."""
+    w = WORKLOADS[name]
+    return gemm_inputs(name, w["dtype_in"], w["M"], w["N"], w["K"],
+                       dist=w.get("dist", "normal"),
+                       b_layout=w.get("b_layout", "col"), seed=seed,
+                       acc16=w.get("acc16", False),
+                       c_int_range=w.get("c_int_range"),
+                       a_signed=w.get("a_signed", True),
+                       b_signed=w.get("b_signed", True))

@@ -28,7 +28,7 @@ def header_functions():
 
 def test_header_declares_the_boundary():
     fns = header_functions()
-    for f in ("mma_gemm", "mma_gemm_ex", "mma_gemm_batched",
+    for f in ("mma_gemm", "mma_gemm_ex", "mma_gemm_batched", "mma_gemm_i8_ex",
               "mma_device_status", "mma_status_string", "mma_version"):
         assert f in fns
 
@@ -112,6 +112,43 @@ def test_valid_arguments_reach_the_device_check(lib):
     assert g(din=BF16, dacc=BF16, ldd=68) == MISAL   # 68 * 2 bytes
     assert g(K=0, A=0, B=0) == NODEV
     assert g(C=0) == NODEV
+
+
+def i8x(*, M=64, N=64, K=64, A=P, lda=64, an=0, B=P, ldb=64, bn=0, layout=0,
+        C=P, ldc=64, D=Q, ldd=64, clamp=1):
+    return binding.mma_gemm_i8_ex(M, N, K, A, lda, an, B, ldb, bn, layout, C,
+                                  ldc, D, ldd, clamp, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), INVALID), (dict(K=-1), INVALID), (dict(layout=3), INVALID),
+    (dict(lda=32), INVALID), (dict(ldb=60), INVALID), (dict(ldc=8), INVALID),
+    (dict(D=0), INVALID), (dict(A=0), INVALID), (dict(B=0), INVALID),
+    (dict(C=P, D=P, ldc=64, ldd=128), INVALID),
+    (dict(A=P + 1), MISAL), (dict(B=P + 8), MISAL), (dict(C=P + 4), MISAL),
+    (dict(D=Q + 4), MISAL),
+    (dict(lda=72), MISAL),           # 72 bytes is not a 16-byte multiple
+    (dict(ldd=66), MISAL),           # 66 * 4 bytes
+    # signed x signed without clamp is the plain INT8 product: same checks
+    (dict(an=1, bn=1, clamp=0, lda=72), MISAL),
+])
+def test_i8_ex_argument_errors(lib, kw, code):
+    assert i8x(**kw) == code
+
+
+def test_i8_ex_empty_and_device_check(lib):
+    assert i8x(M=0, A=0, B=0, C=0, D=0) == OK
+    assert i8x(N=0, A=0, B=0, C=0, D=0, an=1, bn=1, clamp=0) == OK
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    for an in (0, 1):
+        for bn in (0, 1):
+            for clamp in (0, 1):
+                assert i8x(an=an, bn=bn, clamp=clamp) == NODEV
+    assert i8x(layout=1) == NODEV
+    assert i8x(K=0, A=0, B=0) == NODEV
+    assert i8x(C=0) == NODEV
 
 
 def b(*, din=BF16, dacc=F32, M=16, N=16, K=16, A=P, B=P, C=P, D=Q, ld=16,

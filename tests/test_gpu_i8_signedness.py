@@ -1,0 +1,191 @@
+"""Parity of mma_gemm_i8_ex (8-bit integer inputs, each int8 or uint8, with
+optional INT32 saturation) with the CPU oracle, bit for bit.
+
+The operation is the iu8 builtin of "RDNA3 dense WMMA builtins" (sections
+"INT32-accumulate builtins" and "INT8 and UINT8 inputs"): a_neg / b_neg pick
+signed or unsigned inputs, `clamp` saturates the INT32 result on overflow.
+On the tensor pipe, K is cut into chunks of 1024 (signed x signed), 512
+(mixed) or 256 (unsigned x unsigned) products so that each FP32 partial sum
+stays exact; the cases below cover single and many chunks, ragged tails,
+the largest partial sums each chunk depth allows, results beyond INT32 in
+both directions (wrapped and saturated), and K long enough that the
+saturating mode folds its chunk sums into 64-bit sums several times.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_dense_02_gb300 import binding, synth
+
+from helpers import check, dev_padded, to_dev
+
+pytestmark = pytest.mark.gpu
+
+I32_MIN, I32_MAX = -(1 << 31), (1 << 31) - 1
+SIGNS = [(True, True), (True, False), (False, True), (False, False)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mixed_precision_dense_02_gb300 import build
+    build.build()
+    binding.load()
+    yield
+    binding.device_status()
+
+
+def _tag(sa, sb):
+    return ("s" if sa else "u") + ("s" if sb else "u")
+
+
+def run_i8x(A, B, C, *, clamp, b_layout="col", pad=0):
+    import torch
+    Ad = dev_padded(A, extra=pad)
+    Bd = dev_padded(B, extra=pad)
+    Cd = None if C is None else dev_padded(C, extra=pad)
+    M, N = A.shape[0], (B.shape[0] if b_layout == "col" else B.shape[1])
+    Dd = dev_padded(np.full((M, N), 0x3C3C3C3C, np.int32), extra=pad + 1)
+    out = binding.gemm_i8_ex(Ad, Bd, Cd, Dd, clamp=clamp, b_layout=b_layout)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+SHAPES = [(1, 1, 1), (16, 16, 16), (127, 129, 65), (200, 300, 600),
+          (333, 257, 1000), (130, 17, 3), (257, 384, 2100)]
+
+
+@pytest.mark.parametrize("sa,sb", SIGNS, ids=[_tag(*s) for s in SIGNS])
+@pytest.mark.parametrize("clamp", [False, True])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_small_shapes(sa, sb, clamp, M, N, K):
+    g = synth.gemm_inputs(f"i8x_{M}_{N}_{K}", "i8", M, N, K, a_signed=sa,
+                          b_signed=sb)
+    want, ov = oracle.gemm_i8_ex(g.A, g.B, g.C, clamp=clamp)
+    assert ov == 0
+    got = run_i8x(g.A, g.B, g.C, clamp=clamp, pad=1)
+    check("i8", got, want, None, f"{_tag(sa, sb)} clamp={clamp} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("sa,sb", SIGNS, ids=[_tag(*s) for s in SIGNS])
+def test_row_major_b_and_no_c(sa, sb):
+    M, N, K = 190, 136, 777
+    g = synth.gemm_inputs("i8x_row", "i8", M, N, K, a_signed=sa, b_signed=sb,
+                          b_layout="row")
+    for clamp in (False, True):
+        want, _ = oracle.gemm_i8_ex(g.A, g.B, g.C, clamp=clamp, b_layout="row")
+        got = run_i8x(g.A, g.B, g.C, clamp=clamp, b_layout="row")
+        check("i8", got, want, None, f"{_tag(sa, sb)} row-major B clamp={clamp}")
+        want0, _ = oracle.gemm_i8_ex(g.A, g.B, None, clamp=clamp, b_layout="row")
+        got0 = run_i8x(g.A, g.B, None, clamp=clamp, b_layout="row")
+        check("i8", got0, want0, None, f"{_tag(sa, sb)} C=None clamp={clamp}")
+
+
+@pytest.mark.parametrize("sa,sb", SIGNS, ids=[_tag(*s) for s in SIGNS])
+def test_largest_partial_sums_per_chunk(sa, sb):
+    """Every product at its largest magnitude for the signedness: each
+    chunk's FP32 sum reaches the top of the exact range (2^24 for signed,
+    512 * 32640 mixed, 256 * 65025 unsigned)."""
+    M, N, K = 160, 144, 4096 + 17
+    a = -128 if sa else 255
+    b = -128 if sb else 255
+    A = np.full((M, K), a, np.int8 if sa else np.uint8)
+    B = np.full((N, K), b, np.int8 if sb else np.uint8)
+    # a few rows of smaller values so that not every output is the same
+    A[::9, : K // 3] = 1
+    C = synth.int_uniform(0, 17, M * N, -(1 << 20), 1 << 20).astype(np.int32).reshape(M, N)
+    for clamp in (False, True):
+        want, _ = oracle.gemm_i8_ex(A, B, C, clamp=clamp)
+        got = run_i8x(A, B, C, clamp=clamp)
+        check("i8", got, want, None, f"{_tag(sa, sb)} extreme products clamp={clamp}")
+
+
+@pytest.mark.parametrize("sa,sb", SIGNS, ids=[_tag(*s) for s in SIGNS])
+def test_overflow_wraps_or_saturates(sa, sb):
+    """C near both ends of INT32 with large products: outputs beyond the
+    range wrap without clamp and stick at INT32_MIN / INT32_MAX with it."""
+    M, N, K = 136, 264, 3000
+    g = synth.gemm_inputs("i8x_ovf", "i8", M, N, K, a_signed=sa, b_signed=sb,
+                          c_int_range=(I32_MIN, I32_MAX))
+    A, B = g.A.copy(), g.B.copy()
+    # rows with large same-sign products and rows with large opposite-sign
+    # products, so that both ends of the range are crossed
+    A[: M // 2] = 127
+    B[: N // 2] = 127
+    if sa:
+        A[M // 2:] = -128
+    n_total = 0
+    for clamp in (False, True):
+        want, ov = oracle.gemm_i8_ex(A, B, g.C, clamp=clamp)
+        n_total += ov
+        got = run_i8x(A, B, g.C, clamp=clamp)
+        check("i8", got, want, None, f"{_tag(sa, sb)} overflow clamp={clamp}")
+        if clamp:
+            assert np.any(got == I32_MAX)
+            if sa:
+                assert np.any(got == I32_MIN)
+    assert n_total > 0
+
+
+@pytest.mark.parametrize("sa,sb", [(False, False), (False, True), (True, True)],
+                         ids=["uu", "us", "ss"])
+def test_long_k_folds_and_saturates_once(sa, sb):
+    """K long enough for several 64-bit folds of the chunk sums (one every
+    127 chunks).  With signed B the running sum of the constant rows rises
+    past 2^31 in the first half of K and falls back in the second, so
+    saturating once at the end gives the exact in-range value, not a clamped
+    intermediate; with unsigned B it stays beyond 2^31 and saturates."""
+    M, N = 72, 80
+    chunk = 1024 if (sa and sb) else (512 if (sa or sb) else 256)
+    K = 2 * 130 * chunk + 77
+    rng = np.random.default_rng(7)
+    A = np.full((M, K), 127 if sa else 255, np.int8 if sa else np.uint8)
+    if sb:
+        B = np.full((N, K), 127, np.int8)
+        B[:, K // 2:] = -128
+    else:
+        B = np.full((N, K), 255, np.uint8)
+        B[:, K // 2:] = 0
+    # half of the rows/columns random, so that sums are varied
+    A[M // 2:] = rng.integers(0 if not sa else -128, 128 if sa else 256,
+                              (M - M // 2, K)).astype(A.dtype)
+    B[N // 2:] = rng.integers(0 if not sb else -128, 128 if sb else 256,
+                              (N - N // 2, K)).astype(B.dtype)
+    C = synth.int_uniform(0, 19, M * N, -(1 << 30), 1 << 30).astype(np.int32).reshape(M, N)
+    for clamp in (False, True):
+        want, _ = oracle.gemm_i8_ex(A, B, C, clamp=clamp)
+        got = run_i8x(A, B, C, clamp=clamp)
+        check("i8", got, want, None, f"{_tag(sa, sb)} K={K} clamp={clamp}")
+
+
+def test_full_size_u8_clamp_workload():
+    """The 4096^3 unsigned saturating workload: sampled blocks against the
+    oracle, and at every output the properties that hold at any size for
+    nonnegative products: C <= D, and D - C <= K * 255^2 unless D saturated."""
+    import torch
+    name = "gemm_u8_4096_clamp"
+    g = synth.workload_gemm_inputs(name)
+    A, B, C = to_dev(g.A), to_dev(g.B), to_dev(g.C)
+    D = binding.gemm_i8_ex(A, B, C, clamp=True)
+    torch.cuda.synchronize()
+    d64, c64 = D.long(), C.long()
+    assert bool((d64 >= c64).all())
+    assert bool(((d64 == I32_MAX) | (d64 - c64 <= g.K * 255 * 255)).all())
+    assert int((d64 == I32_MAX).sum()) > 0
+    rng = np.random.default_rng(4321)
+    rows = np.unique(np.append(rng.choice(g.M, 95, replace=False), g.M - 1))
+    cols = np.unique(np.append(rng.choice(g.N, 95, replace=False), g.N - 1))
+    # add some saturated outputs to the sample
+    sat = torch.nonzero(D == I32_MAX)[:24].cpu().numpy()
+    rows = np.unique(np.concatenate([rows, sat[:, 0]]))
+    cols = np.unique(np.concatenate([cols, sat[:, 1]]))
+    want, ov = oracle.gemm_i8_ex(np.ascontiguousarray(g.A[rows]),
+                                 np.ascontiguousarray(g.B[cols]),
+                                 np.ascontiguousarray(g.C[np.ix_(rows, cols)]),
+                                 clamp=True)
+    got = D[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    check("i8", got, want, None, name)
+    assert ov > 0
