@@ -68,12 +68,9 @@ constexpr bool int_mode(Epi e) { return e == Epi::I32EXACT || e == Epi::I32SAT; 
 
 // Chunk depth of the exact 8-bit integer modes: every partial sum must stay
 // within 2^24 in magnitude, the range where FP32 represents all integers.
-// |a*b| <= 2^14 (signed x signed), 128 * 255 (mixed) or 255^2 (unsigned x
-// unsigned), so 1024, 512 or 256 products per chunk.
+// The stored values lie in [-128, 127] (unsigned inputs are shifted by -128,
+// see widen_rows_kernel), so |a*b| <= 2^14 and 1024 products per chunk.
 constexpr int kI8ChunkK = 1024;
-constexpr int chunk_k(bool a_signed, bool b_signed) {
-  return a_signed && b_signed ? 1024 : (a_signed || b_signed) ? 512 : 256;
-}
 
 // I32SAT: 127 chunk sums of magnitude <= 2^24 stay below 2^31, so the INT32
 // registers hold them exactly; every kSatFlush chunks they are folded into
@@ -167,7 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmD,
                    const void* __restrict__ Cv, int64_t ldc,
                    void* __restrict__ Dv, int64_t ldd, int M, int N, int K,
-                   int kb_per_chunk, unsigned* status) {
+                   int kb_per_chunk,
+                   const int64_t* __restrict__ row_term,
+                   const int64_t* __restrict__ col_term, unsigned* status) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   constexpr int HALF = BN / 2;  // columns per epilogue warp
   static_assert(EPI != Epi::I32SAT || BN == 128, "I32SAT uses 128-wide tiles");
@@ -413,15 +412,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[a]), 0));
       }
     };
+    // Integer modes with an unsigned operand: the correction terms are
+    // written by the widening pass this kernel may overlap (programmatic
+    // launch), so wait for it before reading them.
+    const bool has_terms = int_mode(EPI) && (row_term || col_term);
+    if (has_terms) grid_dependency_wait();
+    // Correction terms of a unit: this lane's row term, and the column
+    // terms of the warp's HALF columns, one per lane per group of 32 (each
+    // lane loads one; shuffles hand them to the others).  Zero when absent
+    // or outside the problem.
+    constexpr int TG = HALF / 32;
+    [[maybe_unused]] auto load_terms = [&](int r0, int c0, int64_t& rt,
+                                           int64_t (&ct)[TG]) {
+      const int row = r0 + lane;
+      rt = (row_term && row < M) ? __ldg(row_term + row) : 0;
+#pragma unroll
+      for (int g = 0; g < TG; ++g) {
+        const int col = c0 + g * 32 + lane;
+        ct[g] = (col_term && col < N) ? __ldg(col_term + col) : 0;
+      }
+    };
+    // The term of column c0 + jj of the unit whose terms are in ct.
+    [[maybe_unused]] auto col_term_of = [&](const int64_t (&ct)[TG], int jj) {
+      return __shfl_sync(0xffffffffu, ct[jj / 32], jj % 32);
+    };
     // I32SAT: this warp's 64-bit partial sums, 16 columns per 32-column
     // group (low words, then high words), in the TMEM columns beyond the
     // two accumulators.
     [[maybe_unused]] const uint32_t xaddr =
         tmem_base + uint32_t(2 * BN + h * 2 * HALF) + (uint32_t(q * 32) << 16);
-    // Add the INT32 chunk sums to the 64-bit partial sums (or start them)
-    // and clear the INT32 sums.
-    [[maybe_unused]] auto fold_partials = [&](bool started,
-                                              uint32_t (&ia)[int_mode(EPI) ? HALF : 1]) {
+    // Add the INT32 chunk sums to the 64-bit partial sums (or start them,
+    // from the unit's correction terms rt, ct) and clear the INT32 sums.
+    [[maybe_unused]] auto fold_partials =
+        [&](bool started, uint32_t (&ia)[int_mode(EPI) ? HALF : 1], int64_t rt,
+            const int64_t (&ct)[TG]) {
       if constexpr (EPI == Epi::I32SAT) {
 #pragma unroll
         for (int c = 0; c < HALF / 16; ++c) {
@@ -431,7 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = 0u;
+            for (int e = 0; e < 16; ++e) {
+              const uint64_t t0 =
+                  has_terms ? uint64_t(rt + col_term_of(ct, c * 16 + e)) : 0u;
+              x[e] = uint32_t(t0);
+              x[16 + e] = uint32_t(t0 >> 32);
+            }
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -488,9 +517,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // I32SAT: whether this unit's 64-bit sums in TMEM hold chunks yet
       [[maybe_unused]] bool folded = false;
       uint32_t taddr = 0;
+      [[maybe_unused]] int64_t rt = 0;
+      [[maybe_unused]] int64_t ct[TG];
       if constexpr (int_mode(EPI)) {
+        // I32EXACT starts from the correction terms modulo 2^32; I32SAT
+        // adds them in 64 bits at its first fold.
+        if (has_terms) load_terms(row0, colh, rt, ct);
+        if (EPI == Epi::I32EXACT && has_terms) {
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) iacc[j] = 0u;
+          for (int j = 0; j < HALF; ++j)
+            iacc[j] = uint32_t(uint64_t(rt + col_term_of(ct, j)));
+        } else {
+#pragma unroll
+          for (int j = 0; j < HALF; ++j) iacc[j] = 0u;
+        }
         for (int ch = 0; ch < chunks; ++ch) {
           ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
           if (!__all_sync(0xffffffffu, ok)) {
@@ -515,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (EPI == Epi::I32SAT) {
             // every kSatFlush chunks, and after the last one
             if ((ch + 1) % kSatFlush == 0 || ch + 1 == chunks) {
-              fold_partials(folded, iacc);
+              fold_partials(folded, iacc, rt, ct);
               folded = true;
             }
           }
@@ -638,65 +678,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// 8-bit integer -> bfloat16, exactly (every int8 and uint8 value has at
-// most 8 significant bits), with full-rate integer/FP32 ALU operations
-// instead of the slower int-to-float conversion unit.  For a byte x, let
-// u = x ^ flip: the byte itself for uint8 (flip = 0), x ^ 0x80 = v + 128
-// for int8 v (flip = 0x80, two's complement).  The float whose bits are
-// 0x4B0000uu is 2^23 + u, so subtracting `bias` (2^23, or 2^23 + 128 for
-// int8) leaves the value exactly, and its top 16 bits are its bfloat16.
-struct ByteCode {
-  uint32_t flip;  // xor applied to all four bytes of a word
-  float bias;
-};
-__device__ __forceinline__ ByteCode byte_code(bool is_signed) {
-  return is_signed ? ByteCode{0x80808080u, 8388736.0f}   // 2^23 + 128
-                   : ByteCode{0u, 8388608.0f};           // 2^23
-}
+// 8-bit integer -> bfloat16, exactly.  Each input byte x is stored as the
+// value (x ^ flip) - 128: for int8 (flip = 0x80) that is the value itself,
+// for uint8 u (flip = 0) it is u - 128, shifted into the int8 range so that
+// every product keeps the signed bound |a*b| <= 2^14 (the exact sum is
+// restored by the correction terms of widen_rows_kernel).  Both lie in
+// [-128, 127] and have at most 8 significant bits.  Full-rate integer/FP32
+// ALU operations replace the slower int-to-float conversion unit: with
+// u = x ^ flip, the float whose bits are 0x4B0000uu is 2^23 + u, so
+// subtracting 2^23 + 128 leaves the stored value exactly, and its top 16
+// bits are its bfloat16.
+constexpr uint32_t kFlipSigned = 0x80808080u;
 
-__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo_byte,
-                                                   ByteCode bc) {
-  // byte_perm picks byte `lo_byte` of w (made unsigned by the xor) into the
-  // low byte of 0x4B000000
-  const uint32_t f0 = __byte_perm(w ^ bc.flip, 0x4B000000u, 0x7540u + lo_byte);
-  const uint32_t f1 = __byte_perm(w ^ bc.flip, 0x4B000000u, 0x7541u + lo_byte);
-  const float v0 = __uint_as_float(f0) - bc.bias;
-  const float v1 = __uint_as_float(f1) - bc.bias;
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t u, int lo_byte) {
+  // byte_perm picks byte `lo_byte` of u (already flipped) into the low byte
+  // of 0x4B000000
+  const uint32_t f0 = __byte_perm(u, 0x4B000000u, 0x7540u + lo_byte);
+  const uint32_t f1 = __byte_perm(u, 0x4B000000u, 0x7541u + lo_byte);
+  const float v0 = __uint_as_float(f0) - 8388736.0f;  // 2^23 + 128
+  const float v1 = __uint_as_float(f1) - 8388736.0f;
   // high halves of the two floats: (bf16(v1) << 16) | bf16(v0)
   return __byte_perm(__float_as_uint(v0), __float_as_uint(v1), 0x7632);
 }
 
-// The bfloat16 bit pattern of one 8-bit integer (plain conversion; used
-// for ragged row tails and by the transposing pass).
-__device__ __forceinline__ uint16_t byte_to_bf16(uint8_t x, bool is_signed) {
-  const float f = is_signed ? float(int8_t(x)) : float(x);
-  return uint16_t(__float_as_uint(f) >> 16);
+// The bfloat16 bit pattern of one stored value u - 128 (u = x ^ flip; plain
+// conversion, for ragged row tails and the transposing pass).
+__device__ __forceinline__ uint16_t flipped_byte_to_bf16(uint32_t u) {
+  return uint16_t(__float_as_uint(float(int(u) - 128)) >> 16);
 }
 
-__device__ __forceinline__ void i8x16_to_bf16(const int4 v, ByteCode bc,
+// 16 bytes (already flipped) -> 16 bfloat16 values.
+__device__ __forceinline__ void u8x16_to_bf16(const uint32_t (&u)[4],
                                               uint4& o0, uint4& o1) {
-  const uint32_t w[4] = {uint32_t(v.x), uint32_t(v.y), uint32_t(v.z),
-                         uint32_t(v.w)};
   uint32_t o[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) o[j] = i8x2_to_bf16x2(w[j >> 1], 2 * (j & 1), bc);
+  for (int j = 0; j < 8; ++j) o[j] = i8x2_to_bf16x2(u[j >> 1], 2 * (j & 1));
   o0 = make_uint4(o[0], o[1], o[2], o[3]);
   o1 = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// One flat index over the 16-byte chunks of the rows of A then of B.  Each
-// block takes 4 x 256 consecutive chunks, thread t the chunks t, t + 256,
-// t + 512 and t + 768 of them: the four loads are in flight together and
-// every warp-wide load and store covers one contiguous run of memory.
+__device__ __forceinline__ void flip4(const int4 v, uint32_t flip,
+                                      uint32_t (&u)[4]) {
+  u[0] = uint32_t(v.x) ^ flip;
+  u[1] = uint32_t(v.y) ^ flip;
+  u[2] = uint32_t(v.z) ^ flip;
+  u[3] = uint32_t(v.w) ^ flip;
+}
+
+// Signed x signed inputs (no correction terms): one flat index over the
+// 16-byte chunks of the rows of A then of B.  Each block takes 4 x 256
+// consecutive chunks, thread t the chunks t, t + 256, t + 512 and t + 768 of
+// them: the four loads are in flight together and every warp-wide load and
+// store covers one contiguous run of memory.
 constexpr int kConvThreads = 256;
 constexpr int kConvUnroll = 4;
 
 __global__ void __launch_bounds__(kConvThreads)
     i8_to_bf16_kernel(const int8_t* __restrict__ A, int64_t lda, int M,
                       const int8_t* __restrict__ B, int64_t ldb, int N, int K,
-                      uint16_t* __restrict__ W, int64_t ldw, bool a_signed,
-                      bool b_signed) {
-  const ByteCode bca = byte_code(a_signed), bcb = byte_code(b_signed);
+                      uint16_t* __restrict__ W, int64_t ldw) {
   const int64_t cpr = (K + 15) / 16;  // chunks per row
   const int64_t total = int64_t(M + N) * cpr;
   constexpr int64_t kSpan = int64_t(kConvThreads) * kConvUnroll;
@@ -723,17 +763,107 @@ __global__ void __launch_bounds__(kConvThreads)
       const int64_t r = i / cpr;
       const int c = int(i - r * cpr) * 16;
       uint16_t* dst = W + r * ldw + c;
-      const bool is_a = r < M;
       if (c + 16 <= K) {
+        uint32_t w[4];
+        flip4(v[u], kFlipSigned, w);
         uint4 o0, o1;
-        i8x16_to_bf16(v[u], is_a ? bca : bcb, o0, o1);
+        u8x16_to_bf16(w, o0, o1);
         reinterpret_cast<uint4*>(dst)[0] = o0;
         reinterpret_cast<uint4*>(dst)[1] = o1;
       } else {
-        const int8_t* src = is_a ? A + r * lda + c : B + (r - M) * ldb + c;
-        const bool sgn = is_a ? a_signed : b_signed;
+        const int8_t* src = r < M ? A + r * lda + c : B + (r - M) * ldb + c;
         for (int j = 0; c + j < K; ++j)
-          dst[j] = byte_to_bf16(uint8_t(src[j]), sgn);
+          dst[j] = flipped_byte_to_bf16(uint32_t(uint8_t(src[j])) ^ 0x80u);
+      }
+    }
+  }
+}
+
+// Inputs with an unsigned operand.  With oa, ob = 128 for an unsigned A, B
+// (else 0) and A', B' the stored (shifted) values, A = A' + oa and
+// B = B' + ob elementwise, so
+//   (A B)_ij = (A' B')_ij + ob * r_i + oa * c_j + oa * ob * K,
+//   r_i = sum_k A'_ik,  c_j = sum_k B'_kj,
+// exactly; the GEMM computes A' B' with the signed chunk depth and its
+// epilogue adds the per-row term row_term[i] = ob * r_i + oa * ob * K and the
+// per-column term col_term[j] = oa * c_j (each array only when nonzero).
+//
+// This pass widens rows [0, M) of A and then rows [0, nb) of column-major B
+// (nb = 0 when B is row-major and transposed separately) and writes those
+// terms.  G lanes share a row (G a power of two <= 32): lane t of the group
+// takes the row's 16-byte chunks t, t + G, ... (G * 16 contiguous bytes per
+// warp access), four in flight, and the group adds its sums by shuffles.
+constexpr int kRowThreads = 256;
+
+__global__ void __launch_bounds__(kRowThreads)
+    widen_rows_kernel(const uint8_t* __restrict__ A, int64_t lda, int M,
+                      const uint8_t* __restrict__ B, int64_t ldb, int nb,
+                      int K, uint16_t* __restrict__ W, int64_t ldw,
+                      uint32_t flip_a, uint32_t flip_b, int G,
+                      int64_t* __restrict__ row_term, int64_t a_mul,
+                      int64_t a_add, int64_t* __restrict__ col_term,
+                      int64_t b_mul) {
+  const int64_t rows = int64_t(M) + nb;
+  const int64_t cpr = (K + 15) / 16;
+  const int lane = threadIdx.x & 31;
+  const int t = lane & (G - 1);
+  const int64_t rows_per_warp = 32 / G;
+  const int64_t warp0 =
+      (int64_t(blockIdx.x) * kRowThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kRowThreads) >> 5;
+  for (int64_t base = warp0 * rows_per_warp; base < rows;
+       base += nwarps * rows_per_warp) {
+    const int64_t r = base + lane / G;
+    const bool live = r < rows;
+    const bool is_a = r < M;
+    uint64_t s = 0;  // sum over this lane's bytes of (x ^ flip)
+    if (live) {
+      const uint8_t* src = is_a ? A + r * lda : B + (r - M) * ldb;
+      uint16_t* dst = W + r * ldw;
+      const uint32_t flip = is_a ? flip_a : flip_b;
+      for (int64_t c0 = t; c0 < cpr; c0 += 4 * G) {
+        int4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t c = c0 + int64_t(u) * G;
+          v[u] = make_int4(0, 0, 0, 0);
+          if (c < cpr && c * 16 + 16 <= K)
+            v[u] = __ldcs(reinterpret_cast<const int4*>(src + c * 16));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t c = c0 + int64_t(u) * G;
+          if (c >= cpr) continue;
+          if (c * 16 + 16 <= K) {
+            uint32_t w[4];
+            flip4(v[u], flip, w);
+            uint4 o0, o1;
+            u8x16_to_bf16(w, o0, o1);
+            reinterpret_cast<uint4*>(dst + c * 16)[0] = o0;
+            reinterpret_cast<uint4*>(dst + c * 16)[1] = o1;
+            // the 16 bytes' unsigned sum, four at a time
+            const unsigned ones = 0x01010101u;
+            s += __dp4a(w[0], ones, __dp4a(w[1], ones,
+                        __dp4a(w[2], ones, __dp4a(w[3], ones, 0u))));
+          } else {
+            for (int64_t k = c * 16; k < K; ++k) {
+              const uint32_t x = uint32_t(src[k]) ^ (flip & 0xFFu);
+              dst[k] = flipped_byte_to_bf16(x);
+              s += x;
+            }
+          }
+        }
+      }
+    }
+    for (int off = G >> 1; off > 0; off >>= 1)
+      s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (live && t == 0) {
+      // the sum of the row's stored values (x ^ flip) - 128
+      const int64_t sum = int64_t(s) - 128 * int64_t(K);
+      if (is_a) {
+        if (row_term) row_term[r] = a_mul * sum + a_add;
+      } else if (col_term) {
+        col_term[r - M] = b_mul * sum;
       }
     }
   }
@@ -800,7 +930,8 @@ template <int BN, int STAGES, bool BF16, Epi EPI, int CL, int NSTG>
 mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd,
-                 int kb_per_chunk) {
+                 int kb_per_chunk, const int64_t* row_term,
+                 const int64_t* col_term) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   static_assert(L::ALLOC <= 232448, "shared memory per CTA");
   const CUtensorMapDataType cd_type =
@@ -864,7 +995,7 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   ctx.mark_start();
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, C, ldc, D, ldd, int(M), int(N),
-                         int(K), kb_per_chunk, ctx.status);
+                         int(K), kb_per_chunk, row_term, col_term, ctx.status);
   ctx.mark_stop();
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -908,42 +1039,64 @@ template <bool BF16, Epi EPI>
 mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
                       int64_t N, int64_t K, const void* A, int64_t lda,
                       const void* B, int64_t ldb, const void* C, int64_t ldc,
-                      void* D, int64_t ldd, int kb_per_chunk = kI8ChunkK / BK) {
+                      void* D, int64_t ldd, const int64_t* row_term = nullptr,
+                      const int64_t* col_term = nullptr) {
+  constexpr int kpc = kI8ChunkK / BK;
   // Shared memory: operand ring (a pair stages half of B per CTA) plus the
   // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
   // tiles, whose 48 KB stages leave room for only 4 of them).
   if constexpr (EPI != Epi::I32SAT) {
     if (bn == 256)
-      return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk)
-                     : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk);
+      return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term)
+                     : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term);
   }
-  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk)
-                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kb_per_chunk);
+  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term)
+                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term);
 }
 
 // Row-major B (K x N, N contiguous) -> K-major copy W (N rows of K, leading
 // dimension ldw) of 16-bit elements, through 64 x 64 shared-memory tiles so
 // that both the reads and the writes are coalesced.  With I8 the 8-bit
-// integers (int8, or uint8 unless b_signed) are widened to bfloat16 on the
-// way (exactly).
+// inputs are widened to their stored bfloat16 values on the way (exactly;
+// x -> (x ^ flip) - 128, as in i8x2_to_bf16x2), and with col_term each
+// column's sum of stored values times b_mul is added to col_term[n]
+// (64-bit atomics; col_term starts at zero).
 template <bool I8>
 __global__ void __launch_bounds__(256)
     transpose_b_kernel(const void* __restrict__ Bv, int64_t ldb, int K, int N,
-                       uint16_t* __restrict__ W, int64_t ldw, bool b_signed) {
+                       uint16_t* __restrict__ W, int64_t ldw, uint32_t flip,
+                       int64_t* __restrict__ col_term, int64_t b_mul) {
   __shared__ uint16_t tile[64][66];  // [k][n], padded
+  __shared__ int psum[4][64];        // per column, one per thread row
   const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
+  int part = 0;  // this thread's column is threadIdx.x & 63 throughout
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int kk = i >> 6, nn = i & 63;
     const int k = k0 + kk, n = n0 + nn;
     uint16_t v = 0;
     if (k < K && n < N) {
-      if constexpr (I8)
-        v = byte_to_bf16(static_cast<const uint8_t*>(Bv)[int64_t(k) * ldb + n],
-                         b_signed);
-      else
+      if constexpr (I8) {
+        const uint32_t x =
+            uint32_t(static_cast<const uint8_t*>(Bv)[int64_t(k) * ldb + n]) ^
+            (flip & 0xFFu);
+        v = flipped_byte_to_bf16(x);
+        part += int(x) - 128;
+      } else {
         v = static_cast<const uint16_t*>(Bv)[int64_t(k) * ldb + n];
+      }
     }
     tile[kk][nn] = v;
+  }
+  if (I8 && col_term != nullptr) {
+    psum[threadIdx.x >> 6][threadIdx.x & 63] = part;
+    __syncthreads();
+    if (threadIdx.x < 64 && n0 + int(threadIdx.x) < N) {
+      const int64_t c = int64_t(psum[0][threadIdx.x]) + psum[1][threadIdx.x] +
+                        psum[2][threadIdx.x] + psum[3][threadIdx.x];
+      atomicAdd(reinterpret_cast<unsigned long long*>(col_term + n0 +
+                                                      threadIdx.x),
+                static_cast<unsigned long long>(b_mul * c));
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
@@ -956,12 +1109,14 @@ __global__ void __launch_bounds__(256)
 template <bool I8>
 mma_status_t launch_transpose_b(const Ctx& ctx, const void* B, int64_t ldb,
                                 int64_t K, int64_t N, uint16_t* W,
-                                int64_t ldw, bool b_signed = true) {
+                                int64_t ldw, uint32_t flip = kFlipSigned,
+                                int64_t* col_term = nullptr,
+                                int64_t b_mul = 0) {
   const int64_t gy = (K + 63) / 64;
   if (gy > 65535) return MMA_ERR_UNSUPPORTED;
   const dim3 grid{unsigned((N + 63) / 64), unsigned(gy), 1u};
-  transpose_b_kernel<I8><<<grid, 256, 0, ctx.stream>>>(B, ldb, int(K), int(N),
-                                                        W, ldw, b_signed);
+  transpose_b_kernel<I8><<<grid, 256, 0, ctx.stream>>>(
+      B, ldb, int(K), int(N), W, ldw, flip, col_term, b_mul);
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }
 
@@ -1013,7 +1168,8 @@ mma_status_t launch_gemm_tc_f16_rowb(const Ctx& ctx, bool bf16, bool out16,
 
 size_t gemm_i8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const int64_t ldw = (K + 7) / 8 * 8;
-  return size_t(M + N) * size_t(ldw) * 2;
+  // BF16 copies of A and B, then the 64-bit correction terms
+  return size_t(M + N) * size_t(ldw) * 2 + size_t(M + N) * 8;
 }
 
 mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
@@ -1025,30 +1181,56 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
   const int64_t ldw = (K + 7) / 8 * 8;
   uint16_t* W = static_cast<uint16_t*>(workspace);
   uint16_t* Bw = W + M * ldw;
+  // Offsets of the stored values (128 for an unsigned operand) and the
+  // correction terms they need (see widen_rows_kernel).
+  const int64_t oa = a_signed ? 0 : 128, ob = b_signed ? 0 : 128;
+  int64_t* terms = reinterpret_cast<int64_t*>(W + (M + N) * ldw);
+  int64_t* row_term = ob ? terms : nullptr;
+  int64_t* col_term = oa ? terms + M : nullptr;
+  const uint32_t flip_a = a_signed ? kFlipSigned : 0u;
+  const uint32_t flip_b = b_signed ? kFlipSigned : 0u;
   if (b_row_major) {
-    // B widened while transposed; the A pass below then runs last, so the
-    // GEMM's programmatic dependency is on it (and on B by stream order).
-    const mma_status_t st =
-        launch_transpose_b<true>(ctx, B, ldb, K, N, Bw, ldw, b_signed);
+    // B widened while transposed (its column sums gathered by atomics into
+    // a zeroed col_term); the A pass below then runs last, so the GEMM's
+    // programmatic dependency is on it (and on B by stream order).
+    if (col_term &&
+        cudaMemsetAsync(col_term, 0, size_t(N) * 8, ctx.stream) != cudaSuccess)
+      return MMA_ERR_LAUNCH;
+    const mma_status_t st = launch_transpose_b<true>(ctx, B, ldb, K, N, Bw,
+                                                     ldw, flip_b, col_term, oa);
     if (st != MMA_OK) return st;
   }
-  const int64_t rows = b_row_major ? M : M + N;
-  const int64_t chunks = rows * ((K + 15) / 16);
-  const int64_t span = int64_t(kConvThreads) * kConvUnroll;
-  int64_t blocks = (chunks + span - 1) / span;
-  if (blocks > int64_t(ctx.num_sms) * 8) blocks = int64_t(ctx.num_sms) * 8;
-  i8_to_bf16_kernel<<<int(blocks), kConvThreads, 0, ctx.stream>>>(
-      A, lda, int(M), B, ldb, b_row_major ? 0 : int(N), int(K), W, ldw,
-      a_signed, b_signed);
+  const int64_t nb = b_row_major ? 0 : N;
+  if (oa == 0 && ob == 0) {
+    const int64_t chunks = (M + nb) * ((K + 15) / 16);
+    const int64_t span = int64_t(kConvThreads) * kConvUnroll;
+    int64_t blocks = (chunks + span - 1) / span;
+    if (blocks > int64_t(ctx.num_sms) * 8) blocks = int64_t(ctx.num_sms) * 8;
+    i8_to_bf16_kernel<<<int(blocks), kConvThreads, 0, ctx.stream>>>(
+        A, lda, int(M), B, ldb, int(nb), int(K), W, ldw);
+  } else {
+    // lanes per row: enough that each lane has about four 16-byte chunks
+    const int64_t cpr = (K + 15) / 16;
+    int G = 1;
+    while (G < 32 && int64_t(G) * 4 < cpr) G *= 2;
+    const int64_t warps = ((M + nb) * G + 31) / 32;
+    int64_t blocks = (warps + kRowThreads / 32 - 1) / (kRowThreads / 32);
+    if (blocks > int64_t(ctx.num_sms) * 8) blocks = int64_t(ctx.num_sms) * 8;
+    widen_rows_kernel<<<int(blocks), kRowThreads, 0, ctx.stream>>>(
+        reinterpret_cast<const uint8_t*>(A), lda, int(M),
+        reinterpret_cast<const uint8_t*>(B), ldb, int(nb), int(K), W, ldw,
+        flip_a, flip_b, G, row_term, ob, oa * ob * K,
+        b_row_major ? nullptr : col_term, oa);
+  }
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
-  const int kpc = chunk_k(a_signed, b_signed) / BK;
   if (clamp)
     return dispatch<true, Epi::I32SAT>(ctx, true, 128, cluster_size(M, N, K),
                                        M, N, K, W, ldw, Bw, ldw, C, ldc, D,
-                                       ldd, kpc);
+                                       ldd, row_term, col_term);
   return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N),
                                        cluster_size(M, N, K), M, N, K, W, ldw,
-                                       Bw, ldw, C, ldc, D, ldd, kpc);
+                                       Bw, ldw, C, ldc, D, ldd, row_term,
+                                       col_term);
 }
 
 }  // namespace mmagb

@@ -4,11 +4,13 @@ optional INT32 saturation) with the CPU oracle, bit for bit.
 The operation is the iu8 builtin of "RDNA3 dense WMMA builtins" (sections
 "INT32-accumulate builtins" and "INT8 and UINT8 inputs"): a_neg / b_neg pick
 signed or unsigned inputs, `clamp` saturates the INT32 result on overflow.
-On the tensor pipe, K is cut into chunks of 1024 (signed x signed), 512
-(mixed) or 256 (unsigned x unsigned) products so that each FP32 partial sum
-stays exact; the cases below cover single and many chunks, ragged tails,
-the largest partial sums each chunk depth allows, results beyond INT32 in
-both directions (wrapped and saturated), and K long enough that the
+On the tensor pipe an unsigned operand is stored shifted by -128 (so every
+product keeps the signed bound and K is cut into 1024-deep chunks whose FP32
+partial sums stay exact) and the exact product is restored by per-row and
+per-column correction terms.  The cases below cover single and many chunks,
+ragged tails, the largest stored products of every signedness, results
+beyond INT32 in both directions (wrapped and saturated), row-major B (whose
+column sums come from the transposing pass), and K long enough that the
 saturating mode folds its chunk sums into 64-bit sums several times.
 """
 from __future__ import annotations
@@ -85,22 +87,29 @@ def test_row_major_b_and_no_c(sa, sb):
 
 
 @pytest.mark.parametrize("sa,sb", SIGNS, ids=[_tag(*s) for s in SIGNS])
-def test_largest_partial_sums_per_chunk(sa, sb):
-    """Every product at its largest magnitude for the signedness: each
-    chunk's FP32 sum reaches the top of the exact range (2^24 for signed,
-    512 * 32640 mixed, 256 * 65025 unsigned)."""
+@pytest.mark.parametrize("b_layout", ["col", "row"])
+def test_extreme_values(sa, sb, b_layout):
+    """Rows and columns held at the ends of each type's range (-128 and 127
+    for int8, 0 and 255 for uint8): the stored products reach 2^14, so each
+    1024-deep chunk's FP32 sum reaches 2^24, and the correction terms take
+    their largest values."""
     M, N, K = 160, 144, 4096 + 17
-    a = -128 if sa else 255
-    b = -128 if sb else 255
-    A = np.full((M, K), a, np.int8 if sa else np.uint8)
-    B = np.full((N, K), b, np.int8 if sb else np.uint8)
+    lo_a, hi_a = (-128, 127) if sa else (0, 255)
+    lo_b, hi_b = (-128, 127) if sb else (0, 255)
+    A = np.full((M, K), lo_a, np.int8 if sa else np.uint8)
+    A[1::2] = hi_a
+    B = np.full((N, K), lo_b, np.int8 if sb else np.uint8)
+    B[1::2] = hi_b
     # a few rows of smaller values so that not every output is the same
     A[::9, : K // 3] = 1
+    if b_layout == "row":
+        B = np.ascontiguousarray(B.T)
     C = synth.int_uniform(0, 17, M * N, -(1 << 20), 1 << 20).astype(np.int32).reshape(M, N)
     for clamp in (False, True):
-        want, _ = oracle.gemm_i8_ex(A, B, C, clamp=clamp)
-        got = run_i8x(A, B, C, clamp=clamp)
-        check("i8", got, want, None, f"{_tag(sa, sb)} extreme products clamp={clamp}")
+        want, _ = oracle.gemm_i8_ex(A, B, C, clamp=clamp, b_layout=b_layout)
+        got = run_i8x(A, B, C, clamp=clamp, b_layout=b_layout)
+        check("i8", got, want, None,
+              f"{_tag(sa, sb)} extreme values B {b_layout} clamp={clamp}")
 
 
 @pytest.mark.parametrize("sa,sb", SIGNS, ids=[_tag(*s) for s in SIGNS])
@@ -139,8 +148,7 @@ def test_long_k_folds_and_saturates_once(sa, sb):
     saturating once at the end gives the exact in-range value, not a clamped
     intermediate; with unsigned B it stays beyond 2^31 and saturates."""
     M, N = 72, 80
-    chunk = 1024 if (sa and sb) else (512 if (sa or sb) else 256)
-    K = 2 * 130 * chunk + 77
+    K = 2 * 130 * 1024 + 77      # 261 chunks: folds after 127, 254 and 261
     rng = np.random.default_rng(7)
     A = np.full((M, K), 127 if sa else 255, np.int8 if sa else np.uint8)
     if sb:
