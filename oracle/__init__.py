@@ -79,7 +79,9 @@ def lib() -> ctypes.CDLL:
         L.oracle_gemm_batched.restype = _i64
         L.oracle_gemm_batched.argtypes = [_int, _i64, _i64, _i64, _p, _i64, _p,
                                           _i64, _int, _p, _i64, _p, _i64, _i64,
-                                          _i64, _i64]
+                                          _i64, _i64, _int]
+        L.oracle_blgp_source.restype = _int
+        L.oracle_blgp_source.argtypes = [_int, _int]
         _lib = L
     return _lib
 
@@ -241,14 +243,23 @@ def gemm_acc16(dtype_in: str, A, B, C=None, *, b_layout: str = "col",
     return (D, ab) if want_absab else D
 
 
+def blgp_source(blgp: int, q: int) -> int:
+    """Quarter whose B the entry at quarter q of a group of four reads under
+    B lane-group pattern ``blgp`` ("Common MFMA parameters" -- Dense MFMA
+    parameters, blgp), or -1 for an invalid pattern."""
+    return int(lib().oracle_blgp_source(int(blgp), int(q)))
+
+
 def gemm_batched(dtype_in: str, A, B, C, *, group: int = 1, abid: int = 0,
-                 b_layout: str = "col"):
+                 b_layout: str = "col", blgp: int = 0):
     """Batched tiles with A-block broadcast ("Common MFMA parameters" --
-    Shared parameters, cbsz/abid).
+    Shared parameters, cbsz/abid) and B-group pattern (Dense MFMA
+    parameters, blgp, read at matrix level).
 
     ``A``: (batch, M, K); ``B``: (batch, N, K) column-major tiles or
     (batch, K, N) row-major tiles; ``C``: (batch, M, N) or None.  Entry b
-    uses A tile ``(b // group) * group + abid``.  All arrays contiguous.
+    uses A tile ``(b // group) * group + abid`` and B tile
+    ``(b // 4) * 4 + blgp_source(blgp, b % 4)``.  All arrays contiguous.
     """
     batch, M, K = A.shape
     if b_layout == "col":
@@ -274,7 +285,7 @@ def gemm_batched(dtype_in: str, A, B, C, *, group: int = 1, abid: int = 0,
     rc = lib().oracle_gemm_batched(_DT[dtype_in], M, N, K, _ptr(A), K, _ptr(B),
                                    K if b_layout == "col" else N,
                                    _LAYOUT[b_layout], _ptr(Cc), N, _ptr(D), N,
-                                   batch, group, abid)
+                                   batch, group, abid, int(blgp))
     if rc < 0:
         raise ValueError("oracle_gemm_batched rejected its arguments")
     if rc > 0:
@@ -282,6 +293,6 @@ def gemm_batched(dtype_in: str, A, B, C, *, group: int = 1, abid: int = 0,
     return D
 
 
-__all__ = ["gemm", "gemm_i8_ex", "gemm_acc16", "gemm_batched", "num_threads",
+__all__ = ["gemm", "gemm_i8_ex", "gemm_acc16", "blgp_source", "gemm_batched", "num_threads",
            "f16_to_double", "bf16_to_double", "double_to_f16",
            "double_to_bf16", "lib"]

@@ -348,15 +348,38 @@ int oracle_gemm_f64(int64_t M, int64_t N, int64_t K, const double *A,
  * while B, C and D are never broadcast.  G is 1, 2, 4, 8 or 16, G must
  * divide batch and 0 <= abid < G.  Returns 0 (or the INT8 overflow count), -1 on bad
  * arguments.                                                            */
+/* B-group source of an entry, read from "Common MFMA parameters", section
+ * "Dense MFMA parameters" (blgp): the page swizzles B between the four
+ * 16-lane quarters of a 64-lane operand.  At matrix level the batch is cut
+ * into groups of four consecutive entries, entry q of a group playing lane
+ * quarter q; returns the quarter whose B the entry at quarter q reads, or
+ * -1 for a pattern outside 0..7.                                          */
+int oracle_blgp_source(int blgp, int q) {
+  switch (blgp) {
+    case 0: return q;                  /* no swizzling                     */
+    case 1: return q & 1;              /* lanes 0-31 copied into 32-63     */
+    case 2: return 2 + (q & 1);        /* lanes 32-63 copied into 0-31     */
+    case 3: return (q + 1) & 3;        /* rotated down by 16 lanes: lane 16
+                                          feeds lane 0, lane 0 lane 48     */
+    case 4: return 0;                  /* lanes 0-15 to all quarters       */
+    case 5: return 1;                  /* lanes 16-31 to all quarters      */
+    case 6: return 2;                  /* lanes 32-47 to all quarters      */
+    case 7: return 3;                  /* lanes 48-63 to all quarters      */
+    default: return -1;
+  }
+}
+
 int64_t oracle_gemm_batched(int dtype_in, int64_t M, int64_t N, int64_t K,
                             const void *A, int64_t lda, const void *B,
                             int64_t ldb, int b_layout, const void *C,
                             int64_t ldc, void *D, int64_t ldd, int64_t batch,
-                            int64_t G, int64_t abid) {
+                            int64_t G, int64_t abid, int blgp) {
   if (M < 0 || N < 0 || K < 0) return -1;
   /* G = 2^cbsz with cbsz in 0..4 ("Common MFMA parameters", cbsz row) */
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return -1;
   if (batch < 0 || abid < 0 || abid >= G || batch % G != 0) return -1;
+  if (oracle_blgp_source(blgp, 0) < 0) return -1;
+  if (blgp != 0 && batch % 4 != 0) return -1;
   if (dtype_in != OR_F16 && dtype_in != OR_BF16 && dtype_in != OR_I8 &&
       dtype_in != OR_F64)
     return -1;
@@ -370,20 +393,22 @@ int64_t oracle_gemm_batched(int dtype_in, int64_t M, int64_t N, int64_t K,
 #pragma omp parallel for schedule(dynamic, 64) reduction(+ : overflow)
   for (int64_t b = 0; b < batch; ++b) {
     const int64_t src = (b / G) * G + abid;
+    /* (pattern 0 maps every entry to itself, whatever the batch) */
+    const int64_t bs = (b / 4) * 4 + oracle_blgp_source(blgp, (int)(b % 4));
     for (int64_t i = 0; i < M; ++i) {
       if (dtype_in == OR_I8)
         overflow += i8_row(i, N, K, (const int8_t *)A + src * M * lda, lda,
-                           (const int8_t *)B + b * b_tile, ldb, b_layout,
+                           (const int8_t *)B + bs * b_tile, ldb, b_layout,
                            C ? (const int32_t *)C + b * M * ldc : NULL, ldc,
                            (int32_t *)D + b * M * ldd, ldd);
       else if (dtype_in == OR_F64)
         f64_row(i, N, K, (const double *)A + src * M * lda, lda,
-                (const double *)B + b * b_tile, ldb, b_layout,
+                (const double *)B + bs * b_tile, ldb, b_layout,
                 C ? (const double *)C + b * M * ldc : NULL, ldc,
                 (double *)D + b * M * ldd, ldd, NULL, 0);
       else
         f16_row(tab, i, N, K, (const uint16_t *)A + src * M * lda, lda,
-                (const uint16_t *)B + b * b_tile, ldb, b_layout,
+                (const uint16_t *)B + bs * b_tile, ldb, b_layout,
                 C ? (const float *)C + b * M * ldc : NULL, ldc,
                 (float *)D + b * M * ldd, ldd, NULL, 0);
     }

@@ -512,3 +512,84 @@ def test_i8_ex_extremes_and_clamp(oracle_mod):
     D1, _ = oracle_mod.gemm_i8_ex(neg, v, None)
     D2, _ = oracle_mod.gemm_i8_ex(neg, v, None, clamp=True)
     assert np.array_equal(D1, D2) and np.all(D1 == -128 * 255 * K)
+
+
+# ------------------------------------------------ B lane-group pattern
+
+def _golden_blgp():
+    """{pattern: {dest quarter: source quarter}} from the lane-level moves
+    transcribed in the golden file (16 lanes = one quarter = one entry of a
+    group of four)."""
+    out = {}
+    with open(os.path.join(HERE, "golden", "blgp_lane_patterns.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if not line:
+                continue
+            p = int(line[0])
+            d0, d1 = map(int, line[1].split("-"))
+            s0, s1 = map(int, line[2].split("-"))
+            assert d1 - d0 == s1 - s0 and d0 % 16 == 0 and s0 % 16 == 0
+            for off in range(0, d1 - d0 + 1, 16):
+                out.setdefault(p, {})[(d0 + off) // 16] = (s0 + off) // 16
+    return out
+
+
+def test_blgp_patterns_follow_the_page(oracle_mod):
+    table = _golden_blgp()
+    assert sorted(table) == list(range(8))
+    for p, m in table.items():
+        assert sorted(m) == [0, 1, 2, 3], f"pattern {p} must cover all quarters"
+        for q, src in m.items():
+            assert oracle_mod.blgp_source(p, q) == src, (p, q)
+    assert oracle_mod.blgp_source(8, 0) == -1
+
+
+@pytest.mark.parametrize("blgp", range(8))
+def test_batched_blgp_reads_the_mapped_b_tile(oracle_mod, blgp):
+    """B tile t = (t+1) * I, A = I, C = 0: D_b = (srcB(b) + 1) * I, read off
+    D for two groups of four entries (the group offset is checked too)."""
+    table = _golden_blgp()[blgp]
+    batch, n = 8, 16
+    eye = np.eye(n, dtype=bool)
+    one = 0x3F80
+    A = np.broadcast_to(np.where(eye, one, 0).astype(np.uint16), (batch, n, n)).copy()
+    B = np.zeros((batch, n, n), np.uint16)
+    for t in range(batch):
+        B[t] = np.where(eye, synth.round_bf16_bits(np.array([t + 1.0]))[0], 0)
+    C = np.zeros((batch, n, n), np.float32)
+    D = oracle_mod.gemm_batched("bf16", A, B, C, group=1, abid=0, blgp=blgp)
+    for b in range(batch):
+        src = (b // 4) * 4 + table[b % 4]
+        assert np.array_equal(D[b], (src + 1) * np.eye(n, dtype=np.float32)), (blgp, b)
+
+
+def test_batched_blgp_with_a_broadcast_and_rejections(oracle_mod):
+    """cbsz/abid on A and blgp on B act independently: equal to a plain
+    batch whose A and B tiles were gathered by the two source maps."""
+    batch = 16
+    bi = synth.batched_inputs("blgp_pin", "bf16", batch, M=24, N=40, K=32,
+                              group=4, abid=2)
+    D = oracle_mod.gemm_batched("bf16", bi.A, bi.B, bi.C, group=4, abid=2, blgp=3)
+    srcA = [(b // 4) * 4 + 2 for b in range(batch)]
+    srcB = [(b // 4) * 4 + (b + 1) % 4 for b in range(batch)]
+    D2 = oracle_mod.gemm_batched("bf16", np.ascontiguousarray(bi.A[srcA]),
+                                 np.ascontiguousarray(bi.B[srcB]), bi.C)
+    assert np.array_equal(D, D2)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_batched("bf16", bi.A[:6], bi.B[:6], bi.C[:6], blgp=1)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_batched("bf16", bi.A, bi.B, bi.C, blgp=8)
+
+
+@pytest.mark.parametrize("M,N,K", [(24, 40, 32), (1, 7, 3), (130, 9, 70)])
+def test_batched_generic_shapes_are_independent_products(oracle_mod, M, N, K):
+    """Any M x N x K: a batch without broadcast is the independent products
+    of its entries (each checked against the single-problem oracle, itself
+    pinned above by brute force)."""
+    batch = 8
+    bi = synth.batched_inputs(f"gen_pin_{M}_{N}_{K}", "bf16", batch, M=M, N=N, K=K,
+                              group=1, abid=0)
+    D = oracle_mod.gemm_batched("bf16", bi.A, bi.B, bi.C)
+    for b in range(batch):
+        assert np.array_equal(D[b], oracle_mod.gemm("bf16", bi.A[b], bi.B[b], bi.C[b]))
