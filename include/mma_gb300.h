@@ -44,9 +44,12 @@
  *
  * Device memory owned by the library: some paths first rewrite an operand
  * into a scratch buffer -- INT8 products with M*N*K >= 2^24 (and every INT8
- * product with row-major B) widen A and B to BF16 for the tensor pipe,
- * (M + N) * roundup(K, 8) * 2 bytes; FP16/BF16 products with row-major B
- * transpose B, N * roundup(K, 8) * 2 bytes.  That buffer is allocated once
+ * product with row-major B, and every mma_gemm_i8_ex product other than
+ * signed x signed without clamp) widen A and B to BF16 for the tensor pipe,
+ * (M + N) * roundup(K, 8) * 2 bytes, plus (M + N) * 8 bytes of correction
+ * terms; batched INT8 products widen every tile, batch * (M + N) *
+ * roundup(K, 8) * 2 bytes; FP16/BF16 products with row-major B transpose
+ * B, N * roundup(K, 8) * 2 bytes.  That buffer is allocated once
  * per device by the first such call, grown (cudaMalloc, after the previous
  * user finishes) only when a larger problem arrives, and kept until the
  * process exits; calls on different streams are ordered on it by an event.
@@ -181,12 +184,16 @@ mma_status_t mma_gemm_i8_ex(int64_t M, int64_t N, int64_t K, const void *A,
  * Storage: tiles are contiguous, tile b of A at A + b*M*lda, of B at
  * B + b*N*ldb (column-major tiles), of C and D at b*M*ldc and b*M*ldd
  * (elements).  A holds `batch` tiles; only tile src(b) is read for entry b.
- * B, C and D are never broadcast.
+ * B, C and D are never broadcast here (see mma_gemm_batched_ex for B).
+ * Pairs: the four of mma_gemm plus 16-bit accumulate; any M, N, K >= 0;
+ * leading dimensions and alignment as for mma_gemm (each tile is one
+ * mma_gemm problem).  16 x 16 x 16 FP16/BF16 -> FP32 tiles with all leading
+ * dimensions 16 take an HBM-streaming kernel; other shapes run on the
+ * tensor-core GEMM kernels (INT8: through BF16 copies of every tile in the
+ * library's scratch buffer, grown like mma_gemm's).
  * Constraints: a_broadcast_group in {1, 2, 4, 8, 16}; 0 <= a_broadcast_id
  * < a_broadcast_group; batch % a_broadcast_group == 0 (else
- * MMA_ERR_INVALID_ARG).  Provided shapes: M = N = K = 16 with
- * (MMA_F16 | MMA_BF16, MMA_F32) and lda = ldb = ldc = ldd = 16; other
- * shapes or pairs (16-bit accumulate included) return MMA_ERR_UNSUPPORTED.
+ * MMA_ERR_INVALID_ARG); batch < 2^31 (else MMA_ERR_UNSUPPORTED).
  */
 mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc, int64_t M,
                               int64_t N, int64_t K, const void *A, int64_t lda,
@@ -194,6 +201,34 @@ mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc, int64_t M,
                               int64_t ldc, void *D, int64_t ldd, int64_t batch,
                               int a_broadcast_group, int a_broadcast_id,
                               void *stream);
+
+/*
+ * mma_gemm_batched_ex -- mma_gemm_batched with a B-group pattern as well:
+ *
+ *     D_b = A_{src(b)} * B_{bsrc(b)} + C_b,
+ *     bsrc(b) = (b / 4) * 4 + P[b_lane_group_pattern][b % 4]
+ *
+ * Passage: "Common MFMA parameters", section "Dense MFMA parameters"
+ * (blgp: a constrained swizzle of B between the lanes of the 64-lane
+ * operand).  Read at matrix level: consecutive groups of four batch entries
+ * play the four 16-lane quarters, and P[p][q] is the quarter whose B the
+ * entry at quarter q reads:
+ *   p = 0  q            (no swizzling)
+ *   p = 1  q & 1        (lanes 0-31 broadcast into lanes 32-63)
+ *   p = 2  2 + (q & 1)  (lanes 32-63 broadcast into lanes 0-31)
+ *   p = 3  (q + 1) % 4  (all lanes rotated down by 16)
+ *   p = 4..7  p - 4     (one quarter broadcast into the other three)
+ * b_lane_group_pattern in 0..7, and batch % 4 == 0 when it is nonzero (else
+ * MMA_ERR_INVALID_ARG).  Everything else is as for mma_gemm_batched, which
+ * is this call with b_lane_group_pattern = 0.
+ */
+mma_status_t mma_gemm_batched_ex(int dtype_in, int dtype_acc, int64_t M,
+                                 int64_t N, int64_t K, const void *A,
+                                 int64_t lda, const void *B, int64_t ldb,
+                                 const void *C, int64_t ldc, void *D,
+                                 int64_t ldd, int64_t batch,
+                                 int a_broadcast_group, int a_broadcast_id,
+                                 int b_lane_group_pattern, void *stream);
 
 /*
  * mma_device_status -- synchronise `stream`, then read and clear the

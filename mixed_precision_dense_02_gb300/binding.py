@@ -31,6 +31,9 @@ SIGNATURES = {
     "mma_gemm_batched": (_int, [_int, _int, _i64, _i64, _i64, _p, _i64, _p,
                                 _i64, _p, _i64, _p, _i64, _i64, _int, _int,
                                 _p]),
+    "mma_gemm_batched_ex": (_int, [_int, _int, _i64, _i64, _i64, _p, _i64, _p,
+                                   _i64, _p, _i64, _p, _i64, _i64, _int, _int,
+                                   _int, _p]),
     "mma_gemm_i8_ex": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64,
                               _int, _int, _p, _i64, _p, _i64, _int, _p]),
     "mma_gemm_i8_noalloc": (_int, [_i64, _i64, _i64, _p, _i64, _p, _i64, _p,
@@ -103,6 +106,13 @@ def mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C, ldc, D,
     return load().mma_gemm_batched(dtype_in, dtype_acc, M, N, K, A, lda, B,
                                    ldb, C, ldc, D, ldd, batch, group, abid,
                                    stream)
+
+
+def mma_gemm_batched_ex(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C, ldc,
+                        D, ldd, batch, group, abid, blgp, stream) -> int:
+    return load().mma_gemm_batched_ex(dtype_in, dtype_acc, M, N, K, A, lda, B,
+                                      ldb, C, ldc, D, ldd, batch, group, abid,
+                                      blgp, stream)
 
 
 def mma_gemm_i8_ex(M, N, K, A, lda, a_neg, B, ldb, b_neg, layout_b, C, ldc,
@@ -247,14 +257,22 @@ def gemm(A, B, C=None, D=None, *, acc=None, stream=None):
 
 
 def gemm_batched(A, B, C=None, D=None, *, group: int = 1, abid: int = 0,
-                 stream=None):
-    """Batched D_b = A_{(b//group)*group + abid} @ B_b + C_b.
+                 blgp: int = 0, acc=None, stream=None):
+    """Batched D_b = A_{(b//group)*group + abid} @ B_{bsrc(b)} + C_b with
+    bsrc(b) = (b//4)*4 + (quarter read under lane-group pattern ``blgp``).
 
     ``A``: (batch, M, K); ``B``: (batch, N, K) column-major tiles;
-    ``C``/``D``: (batch, M, N); all contiguous.
+    ``C``/``D``: (batch, M, N); all contiguous.  Dtypes as in ``gemm_ex``
+    (FP16/BF16 accumulate into their own type with ``acc="same"`` or a C/D
+    of that type).
     """
     torch = _torch()
     dt_in, dt_acc, out_dtype = _dtypes(A)
+    if A.dtype in (torch.float16, torch.bfloat16):
+        given = D if D is not None else C
+        if acc == "same" or (acc is None and given is not None
+                             and given.dtype == A.dtype):
+            dt_acc, out_dtype = dt_in, A.dtype
     batch, M, K = A.shape
     _, N, Kb = B.shape
     if Kb != K or B.shape[0] != batch:
@@ -264,11 +282,12 @@ def gemm_batched(A, B, C=None, D=None, *, group: int = 1, abid: int = 0,
             raise ValueError("batched operands must be contiguous")
     if D is None:
         D = torch.empty((batch, M, N), dtype=out_dtype, device=A.device)
-    st = mma_gemm_batched(dt_in, dt_acc, M, N, K, A.data_ptr(), K,
-                          B.data_ptr(), K, None if C is None else C.data_ptr(),
-                          N, D.data_ptr(), N, batch, group, abid,
-                          _stream(stream))
-    _check("mma_gemm_batched", st)
+    st = mma_gemm_batched_ex(dt_in, dt_acc, M, N, K, A.data_ptr(), K,
+                             B.data_ptr(), K,
+                             None if C is None else C.data_ptr(), N,
+                             D.data_ptr(), N, batch, group, abid, blgp,
+                             _stream(stream))
+    _check("mma_gemm_batched_ex", st)
     return D
 
 

@@ -359,6 +359,73 @@ extern "C" mma_status_t mma_gemm(int dtype_in, int dtype_acc, int64_t M,
                      MMA_COL_MAJOR, C, ldc, D, ldd, stream);
 }
 
+extern "C" mma_status_t mma_gemm_batched_ex(
+    int dtype_in, int dtype_acc, int64_t M, int64_t N, int64_t K,
+    const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+    int64_t ldc, void* D, int64_t ldd, int64_t batch, int a_broadcast_group,
+    int a_broadcast_id, int b_lane_group_pattern, void* stream) {
+  int64_t eb = 0, ea = 0;
+  if (!pair_sizes(dtype_in, dtype_acc, &eb, &ea)) return MMA_ERR_UNSUPPORTED;
+  const int G = a_broadcast_group;
+  const int blgp = b_lane_group_pattern;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return MMA_ERR_INVALID_ARG;
+  if (a_broadcast_id < 0 || a_broadcast_id >= G) return MMA_ERR_INVALID_ARG;
+  if (blgp < 0 || blgp > 7) return MMA_ERR_INVALID_ARG;
+  if (batch < 0 || batch % G != 0) return MMA_ERR_INVALID_ARG;
+  if (blgp != 0 && batch % 4 != 0) return MMA_ERR_INVALID_ARG;
+  if (batch > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
+  if (M < 0 || N < 0 || K < 0) return MMA_ERR_INVALID_ARG;
+  if (batch == 0) return MMA_OK;
+  // each tile is checked as a single column-major-B problem
+  const mma_status_t chk = check_dense_args(eb, ea, MMA_COL_MAJOR, M, N, K, A,
+                                            lda, B, ldb, C, ldc, D, ldd);
+  if (chk != MMA_OK || batch == 0 || M == 0 || N == 0) return chk;
+  int dev = -1;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info) return MMA_ERR_NO_DEVICE;
+  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  attach_profile(ctx);
+  // K == 0: D = C tile by tile; the tiles are contiguous, so batch * M rows
+  if (K == 0) return launch_copy_c(ctx, batch * M, N, int(ea), C, ldc, D, ldd);
+  const int abid = a_broadcast_id;
+  switch (dtype_in) {
+    case MMA_F16:
+    case MMA_BF16: {
+      const bool bf16 = dtype_in == MMA_BF16;
+      const bool out16 = dtype_acc != MMA_F32;
+      // 16 x 16 x 16 FP32-accumulate tiles stored densely: the HBM-streaming
+      // kernel; every other shape: the tcgen05 kernel over 3-D tensor maps
+      if (!out16 && M == 16 && N == 16 && K == 16 && lda == 16 && ldb == 16 &&
+          ldd == 16 && (C == nullptr || ldc == 16))
+        return launch_batched16(ctx, bf16, batch, G, abid, blgp, A, B,
+                                static_cast<const float*>(C),
+                                static_cast<float*>(D));
+      return launch_gemm_tc_batched(ctx, bf16, out16, M, N, K, A, lda, B, ldb,
+                                    C, ldc, D, ldd, batch, G, abid, blgp);
+    }
+    case MMA_I8:
+      return with_workspace(
+          ctx, gemm_i8_tc_batched_workspace_bytes(M, N, K, batch),
+          [&](void* ws) {
+            return launch_gemm_i8_tc_batched(
+                ctx, M, N, K, static_cast<const int8_t*>(A), lda,
+                static_cast<const int8_t*>(B), ldb,
+                static_cast<const int32_t*>(C), ldc, static_cast<int32_t*>(D),
+                ldd, batch, G, abid, blgp, ws);
+          });
+    case MMA_F64:
+      return launch_gemm_f64_batched(ctx, M, N, K,
+                                     static_cast<const double*>(A), lda,
+                                     static_cast<const double*>(B), ldb,
+                                     static_cast<const double*>(C), ldc,
+                                     static_cast<double*>(D), ldd, batch, G,
+                                     abid, blgp);
+    default:
+      return MMA_ERR_UNSUPPORTED;
+  }
+}
+
 extern "C" mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc,
                                          int64_t M, int64_t N, int64_t K,
                                          const void* A, int64_t lda,
@@ -367,32 +434,9 @@ extern "C" mma_status_t mma_gemm_batched(int dtype_in, int dtype_acc,
                                          int64_t ldd, int64_t batch,
                                          int a_broadcast_group,
                                          int a_broadcast_id, void* stream) {
-  int64_t eb = 0, ea = 0;
-  if (!pair_sizes(dtype_in, dtype_acc, &eb, &ea)) return MMA_ERR_UNSUPPORTED;
-  const int G = a_broadcast_group;
-  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
-    return MMA_ERR_INVALID_ARG;
-  if (a_broadcast_id < 0 || a_broadcast_id >= G) return MMA_ERR_INVALID_ARG;
-  if (batch < 0 || M < 0 || N < 0 || K < 0) return MMA_ERR_INVALID_ARG;
-  if (batch % G != 0) return MMA_ERR_INVALID_ARG;
-  if (!(M == 16 && N == 16 && K == 16)) return MMA_ERR_UNSUPPORTED;
-  if ((dtype_in != MMA_F16 && dtype_in != MMA_BF16) || dtype_acc != MMA_F32)
-    return MMA_ERR_UNSUPPORTED;
-  if (lda != 16 || ldb != 16 || ldd != 16 || (C != nullptr && ldc != 16))
-    return MMA_ERR_UNSUPPORTED;
-  if (batch == 0) return MMA_OK;
-  if (A == nullptr || B == nullptr || D == nullptr) return MMA_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(D) ||
-      (C != nullptr && !aligned16(C)))
-    return MMA_ERR_MISALIGNED;
-  int dev = -1;
-  const DeviceInfo* info = device_info(&dev);
-  if (!info) return MMA_ERR_NO_DEVICE;
-  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
-  attach_profile(ctx);
-  return launch_batched16(ctx, dtype_in == MMA_BF16, batch, G, a_broadcast_id,
-                          A, B, static_cast<const float*>(C),
-                          static_cast<float*>(D));
+  return mma_gemm_batched_ex(dtype_in, dtype_acc, M, N, K, A, lda, B, ldb, C,
+                             ldc, D, ldd, batch, a_broadcast_group,
+                             a_broadcast_id, 0, stream);
 }
 
 extern "C" mma_status_t mma_device_status(void* stream) {
@@ -466,4 +510,4 @@ extern "C" const char* mma_status_string(int status) {
   }
 }
 
-extern "C" int mma_version(void) { return 100; }
+extern "C" int mma_version(void) { return 200; }

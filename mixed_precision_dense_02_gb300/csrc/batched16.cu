@@ -1,5 +1,9 @@
 // Batched 16x16x16 FP16/BF16 -> FP32 multiply-accumulate with A-block
-// broadcast:  D_b = A_{src(b)} * B_b + C_b,  src(b) = (b / G) * G + abid.
+// broadcast:  D_b = A_{src(b)} * B_{bsrc(b)} + C_b,  src(b) = (b / G) * G +
+// abid, bsrc(b) = (b / 4) * 4 + (quarter read under lane-group pattern blgp;
+// page "Common MFMA parameters", section "Dense MFMA parameters", read at
+// matrix level with the four entries of a group as the four 16-lane
+// quarters of the B operand; blgp = 0 gives bsrc(b) = b).
 //
 // Semantics: page "Common MFMA parameters", section "Shared parameters"
 // (cbsz broadcasts the A values of block abid of each group of G = 2^cbsz
@@ -43,7 +47,7 @@ __global__ void __launch_bounds__(kThreads)
     batched16_kernel(const uint16_t* __restrict__ A,
                      const uint16_t* __restrict__ B,
                      const float* __restrict__ C, float* __restrict__ D,
-                     int64_t batch, int abid) {
+                     int64_t batch, int abid, int blgp) {
   constexpr int NA = G >= 4 ? 1 : 4 / G;  // distinct A tiles per unit
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
@@ -76,7 +80,14 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = 0; e < 4; ++e) {
       const int64_t b = b0 + e;
       if (b < batch) {
-        const uint16_t* bt = B + b * 256;
+        // quarter e of the group of four whose first entry is b0: the
+        // quarter it reads under pattern blgp (a unit is one such group)
+        const int qs = blgp == 0   ? e
+                       : blgp == 1 ? (e & 1)
+                       : blgp == 2 ? (2 | (e & 1))
+                       : blgp == 3 ? ((e + 1) & 3)
+                                   : blgp - 4;
+        const uint16_t* bt = B + (b0 + qs) * 256;
         bf[e][0] = __ldcs(reinterpret_cast<const uint2*>(bt + g * 16 + t4));
         bf[e][1] = __ldcs(reinterpret_cast<const uint2*>(bt + (g + 8) * 16 + t4));
         const float* ct = C ? C + b * 256 : nullptr;
@@ -113,8 +124,8 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <int G, bool BF16>
-mma_status_t run(const Ctx& ctx, int64_t batch, int abid, const void* A,
-                 const void* B, const float* C, float* D) {
+mma_status_t run(const Ctx& ctx, int64_t batch, int abid, int blgp,
+                 const void* A, const void* B, const float* C, float* D) {
   const int64_t units = (batch + 3) / 4;
   const int64_t warps_per_block = kThreads / 32;
   int64_t blocks = (units + warps_per_block - 1) / warps_per_block;
@@ -123,21 +134,21 @@ mma_status_t run(const Ctx& ctx, int64_t batch, int abid, const void* A,
   ctx.mark_start();
   batched16_kernel<G, BF16><<<int(blocks), kThreads, 0, ctx.stream>>>(
       static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), C, D,
-      batch, abid);
+      batch, abid, blgp);
   ctx.mark_stop();
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }
 
 template <bool BF16>
 mma_status_t dispatch_group(const Ctx& ctx, int64_t batch, int group, int abid,
-                            const void* A, const void* B, const float* C,
-                            float* D) {
+                            int blgp, const void* A, const void* B,
+                            const float* C, float* D) {
   switch (group) {
-    case 1: return run<1, BF16>(ctx, batch, abid, A, B, C, D);
-    case 2: return run<2, BF16>(ctx, batch, abid, A, B, C, D);
-    case 4: return run<4, BF16>(ctx, batch, abid, A, B, C, D);
-    case 8: return run<8, BF16>(ctx, batch, abid, A, B, C, D);
-    case 16: return run<16, BF16>(ctx, batch, abid, A, B, C, D);
+    case 1: return run<1, BF16>(ctx, batch, abid, blgp, A, B, C, D);
+    case 2: return run<2, BF16>(ctx, batch, abid, blgp, A, B, C, D);
+    case 4: return run<4, BF16>(ctx, batch, abid, blgp, A, B, C, D);
+    case 8: return run<8, BF16>(ctx, batch, abid, blgp, A, B, C, D);
+    case 16: return run<16, BF16>(ctx, batch, abid, blgp, A, B, C, D);
     default: return MMA_ERR_INVALID_ARG;
   }
 }
@@ -145,10 +156,11 @@ mma_status_t dispatch_group(const Ctx& ctx, int64_t batch, int group, int abid,
 }  // namespace
 
 mma_status_t launch_batched16(const Ctx& ctx, bool bf16, int64_t batch,
-                              int group, int abid, const void* A,
+                              int group, int abid, int blgp, const void* A,
                               const void* B, const float* C, float* D) {
-  return bf16 ? dispatch_group<true>(ctx, batch, group, abid, A, B, C, D)
-              : dispatch_group<false>(ctx, batch, group, abid, A, B, C, D);
+  return bf16 ? dispatch_group<true>(ctx, batch, group, abid, blgp, A, B, C, D)
+              : dispatch_group<false>(ctx, batch, group, abid, blgp, A, B, C,
+                                      D);
 }
 
 }  // namespace mmagb

@@ -20,12 +20,12 @@ constexpr int TM = 64, TN = 64, TK = 16;
 constexpr int kThreads = 128;
 constexpr int LDS = TK + 4;  // padded row (doubles) of the shared tiles
 
+// One 64 x 64 tile of D = A * B + C (block tile (blockIdx.y, blockIdx.x)).
 template <bool B_ROW>
-__global__ void __launch_bounds__(kThreads)
-    gemm_f64_kernel(const double* __restrict__ A, int64_t lda,
-                    const double* __restrict__ B, int64_t ldb,
-                    const double* __restrict__ C, int64_t ldc,
-                    double* __restrict__ D, int64_t ldd, int M, int N, int K) {
+__device__ __forceinline__ void gemm_f64_tile(
+    const double* __restrict__ A, int64_t lda, const double* __restrict__ B,
+    int64_t ldb, const double* __restrict__ C, int64_t ldc,
+    double* __restrict__ D, int64_t ldd, int M, int N, int K) {
   __shared__ double As[TM * LDS];
   __shared__ double Bs[TN * LDS];  // Bs[n][k]
 
@@ -120,6 +120,34 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Grid z walks the batch entries (one problem: batch = 1).  Entry b reads
+// the A tile (b / group) * group + abid and the B tile of lane-group
+// pattern blgp (see launch_gemm_f64_batched); tiles are contiguous, tile t
+// of A at A + t*M*lda, of B at B + t*(B_ROW ? K : N)*ldb, of C and D at
+// t*M*ldc and t*M*ldd.
+template <bool B_ROW>
+__global__ void __launch_bounds__(kThreads)
+    gemm_f64_kernel(const double* __restrict__ A, int64_t lda,
+                    const double* __restrict__ B, int64_t ldb,
+                    const double* __restrict__ C, int64_t ldc,
+                    double* __restrict__ D, int64_t ldd, int M, int N, int K,
+                    int batch, int group, int abid, int blgp) {
+  const int64_t b_tile = int64_t(B_ROW ? K : N) * ldb;
+  for (int b = blockIdx.z; b < batch; b += gridDim.z) {
+    const int za = (b / group) * group + abid;
+    const int q = b & 3;
+    const int zb = (b & ~3) + (blgp == 0   ? q
+                               : blgp == 1 ? (q & 1)
+                               : blgp == 2 ? (2 | (q & 1))
+                               : blgp == 3 ? ((q + 1) & 3)
+                                           : blgp - 4);
+    gemm_f64_tile<B_ROW>(A + int64_t(za) * M * lda, lda, B + zb * b_tile, ldb,
+                         C ? C + int64_t(b) * M * ldc : nullptr, ldc,
+                         D + int64_t(b) * M * ldd, ldd, M, N, K);
+    __syncthreads();  // the shared tiles are reused by the next entry
+  }
+}
+
 }  // namespace
 
 mma_status_t launch_gemm_f64(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
@@ -132,10 +160,29 @@ mma_status_t launch_gemm_f64(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   ctx.mark_start();
   if (b_row_major)
     gemm_f64_kernel<true><<<grid, kThreads, 0, ctx.stream>>>(
-        A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K));
+        A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K), 1, 1, 0, 0);
   else
     gemm_f64_kernel<false><<<grid, kThreads, 0, ctx.stream>>>(
-        A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K));
+        A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K), 1, 1, 0, 0);
+  ctx.mark_stop();
+  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}
+
+// Batched FP64 (column-major B tiles): grid z covers the entries.
+mma_status_t launch_gemm_f64_batched(const Ctx& ctx, int64_t M, int64_t N,
+                                     int64_t K, const double* A, int64_t lda,
+                                     const double* B, int64_t ldb,
+                                     const double* C, int64_t ldc, double* D,
+                                     int64_t ldd, int64_t batch, int group,
+                                     int abid, int blgp) {
+  const int64_t gx = (N + TN - 1) / TN, gy = (M + TM - 1) / TM;
+  if (gy > 65535 || batch > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
+  const int64_t gz = batch < 65535 ? batch : 65535;
+  const dim3 grid{unsigned(gx), unsigned(gy), unsigned(gz)};
+  ctx.mark_start();
+  gemm_f64_kernel<false><<<grid, kThreads, 0, ctx.stream>>>(
+      A, lda, B, ldb, C, ldc, D, ldd, int(M), int(N), int(K), int(batch),
+      group, abid, blgp);
   ctx.mark_stop();
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
 }

@@ -98,6 +98,34 @@ struct Layout {
       2 * BN <= 256 ? 256u : 512u;
 };
 
+// Batched problems: `batch` entries of the same M x N x K shape, each tile
+// of A, B, C and D contiguous (the batch entry is the third tensor-map
+// coordinate).  Entry b reads the A tile (b / group) * group + abid (the
+// cbsz/abid broadcast of "Common MFMA parameters", section "Shared
+// parameters", group = 2^cbsz) and the B tile (b / 4) * 4 + blgp_source(q)
+// for q = b % 4 (the blgp lane-group patterns of section "Dense MFMA
+// parameters", read at matrix level: the four entries of a group play the
+// four 16-lane quarters of a 64-lane B operand).  A single problem is
+// batch = 1, group = 1, abid = 0, blgp = 0.
+struct BatchArgs {
+  int batch;
+  int group;
+  int abid;
+  int blgp;
+};
+
+// The quarter whose B data quarter q receives under lane-group pattern p:
+// 0 none moved; 1 lanes 0-31 copied to 32-63; 2 lanes 32-63 copied to 0-31;
+// 3 all lanes rotated down by 16 (lane 16 -> lane 0, lane 0 -> lane 48);
+// 4..7 the quarter p - 4 copied to the other three.
+__device__ __forceinline__ int blgp_source(int p, int q) {
+  if (p == 0) return q;
+  if (p == 1) return q & 1;
+  if (p == 2) return 2 | (q & 1);
+  if (p == 3) return (q + 1) & 3;
+  return p - 4;
+}
+
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n,
                                             int& mb, int& nb) {
   const int per_group = kGroupM * num_n;
@@ -164,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmD,
                    const void* __restrict__ Cv, int64_t ldc,
                    void* __restrict__ Dv, int64_t ldd, int M, int N, int K,
-                   int kb_per_chunk,
+                   int kb_per_chunk, BatchArgs bat,
                    const int64_t* __restrict__ row_term,
                    const int64_t* __restrict__ col_term, unsigned* status) {
   using L = Layout<BN, STAGES, CL, NSTG>;
@@ -188,10 +216,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;
-  // Work units: CL vertically adjacent tiles per cluster.  The CTA of rank
-  // r in its cluster takes m-block (unit row) * CL + r.
+  // Work units: CL vertically adjacent tiles per cluster, of one batch entry
+  // (entries in order, tiles M-grouped within an entry).  The CTA of rank r
+  // in its cluster takes m-block (unit row) * CL + r.
   const int unit_m = (num_m + CL - 1) / CL;
-  const int units = unit_m * num_n;
+  const int per_entry = unit_m * num_n;
+  const int units = per_entry * bat.batch;
+  // Tile coordinates of unit u and the tensor-map batch coordinates of its
+  // A, B and C/D tiles.
+  auto decode = [&](int u, int& mu, int& nb, int& za, int& zb, int& zc) {
+    const int b = u / per_entry;
+    tile_coords(u - b * per_entry, unit_m, num_n, mu, nb);
+    za = (b / bat.group) * bat.group + bat.abid;
+    zb = (b & ~3) + blgp_source(bat.blgp, b & 3);
+    zc = b;
+  };
   const int first_unit = blockIdx.x / CL;
   const int unit_step = gridDim.x / CL;
   const int rank = CL > 1 ? int(cluster_ctarank()) : 0;
@@ -254,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the epilogue's C prefetch overlap its tail.
       grid_dependency_wait();
       for (int u = first_unit; u < units && ok; u += unit_step) {
-        int mu, nb;
-        tile_coords(u, unit_m, num_n, mu, nb);
+        int mu, nb, za, zb, zc;
+        decode(u, mu, nb, za, zb, zc);
         const int mb = mu * CL + rank;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
@@ -265,16 +304,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * L::STAGE_BYTES;
           if constexpr (CL == 1) {
             mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-            tma_load_2d(&tmA, &full[stage], sa, kb * BK, mb * BM);
-            tma_load_2d(&tmB, &full[stage], sa + L::A_BYTES, kb * BK, nb * BN);
+            tma_load_3d(&tmA, &full[stage], sa, kb * BK, mb * BM, za);
+            tma_load_3d(&tmB, &full[stage], sa + L::A_BYTES, kb * BK, nb * BN,
+                        zb);
           } else {
             // the leader expects the bytes of both CTAs' stage
             if (rank == 0)
               mbar_arrive_expect_tx(&full[stage], CL * L::STAGE_BYTES);
             const uint32_t fb = full_lead + uint32_t(stage) * 8u;
-            tma_load_2d_pair(&tmA, fb, sa, kb * BK, mb * BM);
-            tma_load_2d_pair(&tmB, fb, sa + L::A_BYTES, kb * BK,
-                             nb * BN + rank * (BN / CL));
+            tma_load_3d_pair(&tmA, fb, sa, kb * BK, mb * BM, za);
+            tma_load_3d_pair(&tmB, fb, sa + L::A_BYTES, kb * BK,
+                             nb * BN + rank * (BN / CL), zb);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -475,34 +515,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
     };
-    // Store staging block `buf` to D at (col, row0), or close an empty
-    // bulk group when the block lies wholly outside D.
-    auto emit_block = [&](uint8_t* buf, int col, int row0) {
+    // Store staging block `buf` to D at (col, row0) of entry z, or close an
+    // empty bulk group when the block lies wholly outside D.
+    auto emit_block = [&](uint8_t* buf, int col, int row0, int z) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        if (col < N && row0 < M) tma_store_2d(&tmD, buf, col, row0);
+        if (col < N && row0 < M) tma_store_3d(&tmD, buf, col, row0, z);
         bulk_commit_group();
       }
       __syncwarp();
     };
-    // This warp's first row and first column in work unit u.
-    auto unit_origin = [&](int u, int& row0, int& colh) {
-      int mu, nb;
-      tile_coords(u, unit_m, num_n, mu, nb);
+    // This warp's first row and first column in work unit u, and the
+    // unit's batch entry.
+    auto unit_origin = [&](int u, int& row0, int& colh, int& z) {
+      int mu, nb, za, zb;
+      decode(u, mu, nb, za, zb, z);
       row0 = (mu * CL + rank) * BM + q * 32;
       colh = nb * BN + h * HALF;
     };
     // (lane 0) Request the C of block gg, which is block jj of unit u.
     auto request_c = [&](uint32_t gg, int u, int jj) {
       const uint32_t b = gg % NSTG;
-      int row0, colh;
-      unit_origin(u, row0, colh);
+      int row0, colh, z;
+      unit_origin(u, row0, colh, z);
       bulk_wait_group_read<WAITN>();
       if (row0 < M && colh + jj * COLS < N) {
         mbar_arrive_expect_tx(&wbar[b], kStgBytes);
-        tma_load_2d(&tmC, &wbar[b], stg + b * kStgBytes, colh + jj * COLS,
-                    row0);
+        tma_load_3d(&tmC, &wbar[b], stg + b * kStgBytes, colh + jj * COLS,
+                    row0, z);
       } else {
         mbar_arrive(&wbar[b]);  // wholly outside C and D: nothing to load
       }
@@ -511,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int jj = 0; jj < PF; ++jj) request_c(uint32_t(jj), first_unit, jj);
     __syncwarp();
     for (int u = first_unit; u < units && ok; u += unit_step) {
-      int row0, colh;
-      unit_origin(u, row0, colh);
+      int row0, colh, zc;
+      unit_origin(u, row0, colh, zc);
       [[maybe_unused]] uint32_t iacc[int_mode(EPI) ? HALF : 1];
       // I32SAT: whether this unit's 64-bit sums in TMEM hold chunks yet
       [[maybe_unused]] bool folded = false;
@@ -652,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *p = o;
         }
-        emit_block(buf, colh + j * COLS, row0);
+        emit_block(buf, colh + j * COLS, row0, zc);
       }
       if constexpr (!int_mode(EPI)) {
         acc ^= 1;
@@ -886,38 +927,47 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D K-major operand: inner dim K (contiguous), outer dim rows, box
-// 64 x box_rows, 128-byte swizzle, zero fill out of bounds.
+// K-major operand: `count` tiles of `rows` rows of K contiguous 16-bit
+// elements (leading dimension ld_elems; tile t starts rows * ld_elems
+// elements after tile t - 1).  Inner dim K, then rows, then the tile; box
+// 64 x box_rows x 1, 128-byte swizzle, zero fill out of bounds (so a box
+// overhanging a tile's last row or K reads zeros, never the next tile).
 bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t K,
-                     int64_t rows, int64_t ld_elems, int box_rows, bool bf16) {
+                     int64_t rows, int64_t ld_elems, int box_rows, bool bf16,
+                     int64_t count = 1) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(ld_elems) * 2};
-  cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
+  cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(rows), cuuint64_t(count)};
+  cuuint64_t strides[2] = {cuuint64_t(ld_elems) * 2,
+                           cuuint64_t(rows) * cuuint64_t(ld_elems) * 2};
+  cuuint32_t box[3] = {cuuint32_t(BK), cuuint32_t(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map,
                    bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   2, const_cast<void*>(base), dims, strides, box, estr,
+                   3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// 2-D row-major C/D map: 64-byte (16 x 4-byte or 32 x 2-byte) x 32-row box,
-// 64-byte swizzle, matching the epilogue's staging blocks.
+// Row-major C/D map over `count` M x N tiles (tile t starts M * ld_elems
+// elements after tile t - 1): 64-byte (16 x 4-byte or 32 x 2-byte) x 32-row
+// x 1 box, 64-byte swizzle, matching the epilogue's staging blocks.
 bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
-                 int64_t ld_elems, CUtensorMapDataType dt, int elem_bytes) {
+                 int64_t ld_elems, CUtensorMapDataType dt, int elem_bytes,
+                 int64_t count = 1) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(M)};
-  cuuint64_t strides[1] = {cuuint64_t(ld_elems) * cuuint64_t(elem_bytes)};
-  cuuint32_t box[2] = {cuuint32_t(64 / elem_bytes), 32};
-  cuuint32_t estr[2] = {1, 1};
+  cuuint64_t dims[3] = {cuuint64_t(N), cuuint64_t(M), cuuint64_t(count)};
+  cuuint64_t strides[2] = {
+      cuuint64_t(ld_elems) * cuuint64_t(elem_bytes),
+      cuuint64_t(M) * cuuint64_t(ld_elems) * cuuint64_t(elem_bytes)};
+  cuuint32_t box[3] = {cuuint32_t(64 / elem_bytes), 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, dt,
-                   2, const_cast<void*>(base), dims, strides, box, estr,
+                   3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -930,7 +980,7 @@ template <int BN, int STAGES, bool BF16, Epi EPI, int CL, int NSTG>
 mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd,
-                 int kb_per_chunk, const int64_t* row_term,
+                 int kb_per_chunk, BatchArgs bat, const int64_t* row_term,
                  const int64_t* col_term) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   static_assert(L::ALLOC <= 232448, "shared memory per CTA");
@@ -941,12 +991,14 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int cd_bytes = EPI == Epi::H16 ? 2 : 4;
   CUtensorMap ta, tb, tc, td;
-  if (!make_kmajor_map(&ta, A, K, M, lda, BM, BF16) ||
-      !make_kmajor_map(&tb, B, K, N, ldb, BN / CL, BF16) ||
-      !make_cd_map(&td, D, N, M, ldd, cd_type, cd_bytes))
+  const int64_t nt = bat.batch;  // tiles of each operand
+  if (!make_kmajor_map(&ta, A, K, M, lda, BM, BF16, nt) ||
+      !make_kmajor_map(&tb, B, K, N, ldb, BN / CL, BF16, nt) ||
+      !make_cd_map(&td, D, N, M, ldd, cd_type, cd_bytes, nt))
     return MMA_ERR_LAUNCH;
   if (C != nullptr) {
-    if (!make_cd_map(&tc, C, N, M, ldc, cd_type, cd_bytes)) return MMA_ERR_LAUNCH;
+    if (!make_cd_map(&tc, C, N, M, ldc, cd_type, cd_bytes, nt))
+      return MMA_ERR_LAUNCH;
   } else {
     tc = td;  // never read: the kernel loads C only when it is given
   }
@@ -958,7 +1010,9 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
       return MMA_ERR_LAUNCH;
     smem_set[ctx.device & 63] = true;
   }
-  const int64_t units = ((M + BM * CL - 1) / (BM * CL)) * ((N + BN - 1) / BN);
+  const int64_t units =
+      ((M + BM * CL - 1) / (BM * CL)) * ((N + BN - 1) / BN) * bat.batch;
+  if (units > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::ALLOC;
@@ -995,7 +1049,8 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   ctx.mark_start();
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, C, ldc, D, ldd, int(M), int(N),
-                         int(K), kb_per_chunk, row_term, col_term, ctx.status);
+                         int(K), kb_per_chunk, bat, row_term, col_term,
+                         ctx.status);
   ctx.mark_stop();
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -1008,14 +1063,14 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
 // enough to keep many pairs busy (at least two m-blocks); single CTAs
 // otherwise.
 // MMA_GB300_CLUSTER (1 or 2) overrides the choice, for tuning.
-int cluster_size(int64_t M, int64_t N, int64_t K) {
+int cluster_size(int64_t M, int64_t N, int64_t K, int64_t batch = 1) {
   static const int forced = [] {
     const char* e = getenv("MMA_GB300_CLUSTER");
     const int v = e ? atoi(e) : 0;
     return (v == 1 || v == 2) ? v : 0;
   }();
   if (forced) return forced;
-  const double work = double(M) * double(N) * double(K);
+  const double work = double(M) * double(N) * double(K) * double(batch);
   return (M > BM && work >= 1073741824.0) ? 2 : 1;
 }
 
@@ -1024,14 +1079,14 @@ int cluster_size(int64_t M, int64_t N, int64_t K) {
 // INT8 4096^3, BF16 8192^3 and 16384 x 128 x 4096 workloads, 256-wide tiles
 // beat 192 and 128 wherever they fill the chip.  MMA_GB300_TILE_N (128 or
 // 256) overrides the choice, for tuning.
-int tile_n(const Ctx& ctx, int64_t M, int64_t N) {
+int tile_n(const Ctx& ctx, int64_t M, int64_t N, int64_t batch = 1) {
   static const int forced = [] {
     const char* e = getenv("MMA_GB300_TILE_N");
     const int v = e ? atoi(e) : 0;
     return (v == 128 || v == 256) ? v : 0;
   }();
   if (forced) return forced;
-  const int64_t wide_tiles = ((M + BM - 1) / BM) * ((N + 255) / 256);
+  const int64_t wide_tiles = ((M + BM - 1) / BM) * ((N + 255) / 256) * batch;
   return (N > 128 && wide_tiles >= ctx.num_sms) ? 256 : 128;
 }
 
@@ -1040,18 +1095,19 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
                       int64_t N, int64_t K, const void* A, int64_t lda,
                       const void* B, int64_t ldb, const void* C, int64_t ldc,
                       void* D, int64_t ldd, const int64_t* row_term = nullptr,
-                      const int64_t* col_term = nullptr) {
+                      const int64_t* col_term = nullptr,
+                      BatchArgs bat = BatchArgs{1, 1, 0, 0}) {
   constexpr int kpc = kI8ChunkK / BK;
   // Shared memory: operand ring (a pair stages half of B per CTA) plus the
   // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
   // tiles, whose 48 KB stages leave room for only 4 of them).
   if constexpr (EPI != Epi::I32SAT) {
     if (bn == 256)
-      return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term)
-                     : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term);
+      return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
+                     : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
   }
-  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term)
-                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, row_term, col_term);
+  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
+                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
 }
 
 // Row-major B (K x N, N contiguous) -> K-major copy W (N rows of K, leading
@@ -1231,6 +1287,67 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
                                        cluster_size(M, N, K), M, N, K, W, ldw,
                                        Bw, ldw, C, ldc, D, ldd, row_term,
                                        col_term);
+}
+
+mma_status_t launch_gemm_tc_batched(const Ctx& ctx, bool bf16, bool out16,
+                                    int64_t M, int64_t N, int64_t K,
+                                    const void* A, int64_t lda, const void* B,
+                                    int64_t ldb, const void* C, int64_t ldc,
+                                    void* D, int64_t ldd, int64_t batch,
+                                    int group, int abid, int blgp) {
+  if (batch > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
+  const BatchArgs bat{int(batch), group, abid, blgp};
+  const int bn = tile_n(ctx, M, N, batch);
+  const int cl = cluster_size(M, N, K, batch);
+  if (out16)
+    return bf16 ? dispatch<true, Epi::H16>(ctx, false, bn, cl, M, N, K, A, lda,
+                                           B, ldb, C, ldc, D, ldd, nullptr,
+                                           nullptr, bat)
+                : dispatch<false, Epi::H16>(ctx, false, bn, cl, M, N, K, A,
+                                            lda, B, ldb, C, ldc, D, ldd,
+                                            nullptr, nullptr, bat);
+  return bf16 ? dispatch<true, Epi::F32>(ctx, false, bn, cl, M, N, K, A, lda, B,
+                                         ldb, C, ldc, D, ldd, nullptr, nullptr,
+                                         bat)
+              : dispatch<false, Epi::F32>(ctx, false, bn, cl, M, N, K, A, lda,
+                                          B, ldb, C, ldc, D, ldd, nullptr,
+                                          nullptr, bat);
+}
+
+size_t gemm_i8_tc_batched_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                          int64_t batch) {
+  const int64_t ldw = (K + 7) / 8 * 8;
+  return size_t(batch) * size_t(M + N) * size_t(ldw) * 2;
+}
+
+mma_status_t launch_gemm_i8_tc_batched(const Ctx& ctx, int64_t M, int64_t N,
+                                       int64_t K, const int8_t* A, int64_t lda,
+                                       const int8_t* B, int64_t ldb,
+                                       const int32_t* C, int64_t ldc,
+                                       int32_t* D, int64_t ldd, int64_t batch,
+                                       int group, int abid, int blgp,
+                                       void* workspace) {
+  // The tiles of A (and of B) are contiguous, so `batch` tiles of M rows
+  // are one matrix of batch * M rows with leading dimension lda; every tile
+  // is widened (the kernel then reads the broadcast sources among them).
+  if (batch * (M + N) > int64_t(INT32_MAX) || batch > int64_t(INT32_MAX))
+    return MMA_ERR_UNSUPPORTED;
+  const int64_t ldw = (K + 7) / 8 * 8;
+  uint16_t* W = static_cast<uint16_t*>(workspace);
+  uint16_t* Bw = W + batch * M * ldw;
+  const int64_t rows_a = batch * M, rows_b = batch * N;
+  const int64_t chunks = (rows_a + rows_b) * ((K + 15) / 16);
+  const int64_t span = int64_t(kConvThreads) * kConvUnroll;
+  int64_t blocks = (chunks + span - 1) / span;
+  if (blocks > int64_t(ctx.num_sms) * 8) blocks = int64_t(ctx.num_sms) * 8;
+  i8_to_bf16_kernel<<<int(blocks), kConvThreads, 0, ctx.stream>>>(
+      A, lda, int(rows_a), B, ldb, int(rows_b), int(K), W, ldw);
+  if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
+  const BatchArgs bat{int(batch), group, abid, blgp};
+  return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N, batch),
+                                       cluster_size(M, N, K, batch), M, N, K,
+                                       W, ldw, Bw, ldw, C, ldc, D, ldd,
+                                       nullptr, nullptr, bat);
 }
 
 }  // namespace mmagb

@@ -48,6 +48,35 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
                                void* workspace, bool b_row_major,
                                bool a_signed, bool b_signed, bool clamp);
 
+// Batched tcgen05 GEMMs: `batch` entries of contiguous M x N x K tiles
+// (tile b of A at A + b*M*lda, of B at B + b*N*ldb, of C/D at b*M*ldc,
+// b*M*ldd elements); entry b reads A tile (b/group)*group + abid and the B
+// tile of lane-group pattern blgp (0..7; batch % 4 == 0 when nonzero).
+mma_status_t launch_gemm_tc_batched(const Ctx& ctx, bool bf16, bool out16,
+                                    int64_t M, int64_t N, int64_t K,
+                                    const void* A, int64_t lda, const void* B,
+                                    int64_t ldb, const void* C, int64_t ldc,
+                                    void* D, int64_t ldd, int64_t batch,
+                                    int group, int abid, int blgp);
+// INT8 -> INT32 (exact), through BF16 copies of every tile in `workspace`.
+size_t gemm_i8_tc_batched_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                          int64_t batch);
+mma_status_t launch_gemm_i8_tc_batched(const Ctx& ctx, int64_t M, int64_t N,
+                                       int64_t K, const int8_t* A, int64_t lda,
+                                       const int8_t* B, int64_t ldb,
+                                       const int32_t* C, int64_t ldc,
+                                       int32_t* D, int64_t ldd, int64_t batch,
+                                       int group, int abid, int blgp,
+                                       void* workspace);
+
+// Batched FP64 (DMMA), same tile conventions.
+mma_status_t launch_gemm_f64_batched(const Ctx& ctx, int64_t M, int64_t N,
+                                     int64_t K, const double* A, int64_t lda,
+                                     const double* B, int64_t ldb,
+                                     const double* C, int64_t ldc, double* D,
+                                     int64_t ldd, int64_t batch, int group,
+                                     int abid, int blgp);
+
 // tcgen05 FP16/BF16 GEMM with row-major B: B is transposed into
 // `workspace` (gemm_tc_rowb_workspace_bytes(N, K) bytes) first.
 size_t gemm_tc_rowb_workspace_bytes(int64_t N, int64_t K);
@@ -72,7 +101,7 @@ mma_status_t launch_gemm_f64(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
 
 // Batched 16x16x16 FP16/BF16 -> FP32 with A-block broadcast.
 mma_status_t launch_batched16(const Ctx& ctx, bool bf16, int64_t batch,
-                              int group, int abid, const void* A,
+                              int group, int abid, int blgp, const void* A,
                               const void* B, const float* C, float* D);
 
 // Launch context for the current device (false if it is not a usable

@@ -155,69 +155,45 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
                : "memory");
 }
 
-// 2-D tiled load of one box into shared memory, completing on `bar`.
-// x is the innermost (contiguous) coordinate.
-__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map,
+// 3-D tiled load of one box into shared memory, completing on `bar`.
+// x is the innermost (contiguous) coordinate, z the batch entry (0 for a
+// single problem).  Elements outside the tensor are filled with zero.
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map,
                                             uint64_t* bar, void* dst, int x,
-                                            int y) {
+                                            int y, int z) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
-      "complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-// As tma_load_2d, but the box is written to the same shared-memory offset
-// in every CTA of the cluster named in cta_mask, and each destination CTA's
-// mbarrier at the offset of `bar` receives the completed bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(const CUtensorMap* map,
-                                                      uint64_t* bar, void* dst,
-                                                      int x, int y,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
-      "complete_tx::bytes.multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(
-          smem_u32(dst)),
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y),
-      "h"(cta_mask)
+      "r"(z)
       : "memory");
 }
 
-// As tma_load_2d, for a CTA pair: the box lands in this CTA's shared
+// As tma_load_3d, for a CTA pair: the box lands in this CTA's shared
 // memory and its bytes complete on the mbarrier at `bar_cluster` (a
 // shared::cluster address, in this CTA or its peer).
-__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map,
+__device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* map,
                                                  uint32_t bar_cluster,
-                                                 void* dst, int x, int y) {
+                                                 void* dst, int x, int y,
+                                                 int z) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
-      "mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile."
+      "mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
           smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y),
+      "r"(z)
       : "memory");
 }
 
-// 2-D tiled store of one box from shared memory (bulk-group completion).
+// 3-D tiled store of one box from shared memory (bulk-group completion).
 // Out-of-bounds parts of the box are not written.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map,
-                                             const void* src, int x, int y) {
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map,
+                                             const void* src, int x, int y,
+                                             int z) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], "
-      "[%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y)
-      : "memory");
-}
-
-// 2-D tiled reduction of one box from shared memory into global memory:
-// element-wise atomic add (element type from the tensor map; INT32 adds
-// wrap modulo 2^32).  Out-of-bounds parts of the box are skipped.
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map,
-                                                  const void* src, int x,
-                                                  int y) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group "
-      "[%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group "
+      "[%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 

@@ -199,24 +199,32 @@ class BatchedInputs:
     A: np.ndarray          # (batch, M, K); entry b reads tile (b//G)*G + abid
     B: np.ndarray          # (batch, N, K) column-major tiles
     C: np.ndarray          # (batch, M, N)
+    blgp: int = 0          # B lane-group pattern (groups of four entries)
 
     def algorithmic_bytes(self) -> int:
-        """A read once per group, B and C read once, D written once."""
+        """A read once per group, the B tiles that are read once, C read
+        once, D written once."""
         a_tile = self.M * self.K * self.A.itemsize
-        return ((self.batch // self.group) * a_tile + self.B.nbytes
+        b_tile = self.N * self.K * self.B.itemsize
+        b_read = {0: 4, 1: 2, 2: 2, 3: 4}.get(self.blgp, 1)  # per group of 4
+        n_b = self.batch if self.blgp == 0 else (self.batch // 4) * b_read
+        return ((self.batch // self.group) * a_tile + n_b * b_tile
                 + self.C.nbytes + self.C.nbytes)
 
 
 def batched_inputs(workload: str, dtype_in: str, batch: int, M: int = 16,
                    N: int = 16, K: int = 16, *, group: int = 4, abid: int = 1,
-                   dist: str = "uniform", seed: int = 0) -> BatchedInputs:
-    """Contiguous per-tile batched inputs (A allocated with ``batch`` tiles)."""
+                   dist: str = "uniform", seed: int = 0, blgp: int = 0,
+                   acc16: bool = False) -> BatchedInputs:
+    """Contiguous per-tile batched inputs (A allocated with ``batch`` tiles).
+    With ``acc16`` (FP16/BF16) C is rounded to the input's 16-bit type."""
     sA, sB, sC = (stream_id(workload, t) for t in "ABC")
     if dtype_in in ("f16", "bf16"):
         rnd = round_f16_bits if dtype_in == "f16" else round_bf16_bits
         A = rnd(_floats(dist, seed, sA, batch * M * K)).reshape(batch, M, K)
         B = rnd(_floats(dist, seed, sB, batch * N * K)).reshape(batch, N, K)
-        C = normal(seed, sC, batch * M * N).astype(np.float32).reshape(batch, M, N)
+        C = normal(seed, sC, batch * M * N)
+        C = (rnd(C) if acc16 else C.astype(np.float32)).reshape(batch, M, N)
     elif dtype_in == "i8":
         A = int8_uniform(seed, sA, batch * M * K).reshape(batch, M, K)
         B = int8_uniform(seed, sB, batch * N * K).reshape(batch, N, K)
@@ -227,7 +235,7 @@ def batched_inputs(workload: str, dtype_in: str, batch: int, M: int = 16,
         C = normal(seed, sC, batch * M * N).reshape(batch, M, N)
     else:
         raise ValueError(dtype_in)
-    return BatchedInputs(dtype_in, batch, M, N, K, group, abid, A, B, C)
+    return BatchedInputs(dtype_in, batch, M, N, K, group, abid, A, B, C, blgp)
 
 
 # The five workloads, by what they are.

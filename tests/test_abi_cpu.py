@@ -43,7 +43,7 @@ def test_status_strings(lib):
     for code, name in binding.STATUS.items():
         assert binding.mma_status_string(code) == name
     assert binding.mma_status_string(99) == "MMA_ERR_UNKNOWN"
-    assert binding.load().mma_version() == 100
+    assert binding.load().mma_version() == 200
 
 
 F16, BF16, I8, F64, F32, I32 = 1, 2, 3, 4, 5, 6
@@ -152,24 +152,27 @@ def test_i8_ex_empty_and_device_check(lib):
 
 
 def b(*, din=BF16, dacc=F32, M=16, N=16, K=16, A=P, B=P, C=P, D=Q, ld=16,
-      batch=64, G=4, abid=1):
-    return binding.mma_gemm_batched(din, dacc, M, N, K, A, ld, B, ld, C, ld, D,
-                                    ld, batch, G, abid, None)
+      batch=64, G=4, abid=1, blgp=None):
+    if blgp is None:
+        return binding.mma_gemm_batched(din, dacc, M, N, K, A, ld, B, ld, C, ld,
+                                        D, ld, batch, G, abid, None)
+    return binding.mma_gemm_batched_ex(din, dacc, M, N, K, A, ld, B, ld, C, ld,
+                                       D, ld, batch, G, abid, blgp, None)
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(G=3), INVALID), (dict(G=32), INVALID), (dict(G=0), INVALID),
     (dict(abid=4), INVALID), (dict(abid=-1), INVALID),
     (dict(batch=6), INVALID), (dict(batch=-4), INVALID),
-    (dict(M=32), UNSUP), (dict(K=8), UNSUP),
-    (dict(din=I8, dacc=I32), UNSUP), (dict(din=F64, dacc=F64), UNSUP),
+    (dict(blgp=8), INVALID), (dict(blgp=-1), INVALID),
+    (dict(blgp=3, batch=6, G=2), INVALID),    # patterns need groups of four
     (dict(din=BF16, dacc=I32), UNSUP),
-    (dict(din=BF16, dacc=F16), UNSUP),
     (dict(din=F16, dacc=BF16), UNSUP),
     (dict(din=I8, dacc=I8), UNSUP),
-    (dict(ld=32), UNSUP),
+    (dict(M=-1), INVALID), (dict(ld=8), INVALID),
     (dict(A=0), INVALID), (dict(D=0), INVALID),
     (dict(A=P + 8), MISAL), (dict(C=P + 4), MISAL),
+    (dict(M=20, N=20, K=20, ld=20), MISAL),   # 20 * 2 bytes
 ])
 def test_batched_argument_errors(lib, kw, code):
     assert b(**kw) == code
@@ -177,10 +180,17 @@ def test_batched_argument_errors(lib, kw, code):
 
 def test_batched_empty_and_device_check(lib):
     assert b(batch=0, A=0, B=0, C=0, D=0) == OK
+    assert b(M=0, A=0, B=0, C=0, D=0) == OK
     import torch
     if not torch.cuda.is_available():
         assert b() == NODEV
         assert b(C=0, G=1, abid=0, batch=5) == NODEV
+        # generic shapes and every pair are provided
+        assert b(M=32, N=48, K=64, ld=64) == NODEV
+        assert b(din=I8, dacc=I32, M=32, N=32, K=32, ld=32) == NODEV
+        assert b(din=F64, dacc=F64) == NODEV
+        assert b(din=BF16, dacc=BF16, blgp=3) == NODEV
+        assert b(blgp=7) == NODEV
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -1,0 +1,166 @@
+"""Parity of the batched products of any M x N x K (mma_gemm_batched_ex)
+with the CPU oracle: A-block broadcast (cbsz/abid of "Common MFMA
+parameters", section "Shared parameters") and the B lane-group pattern
+(blgp, section "Dense MFMA parameters", read at matrix level) on every
+dtype pair.
+
+Shapes span one and several tiles per entry, ragged M/N/K edges inside each
+entry (the tensor maps' batch coordinate keeps a tile's overhang from
+reading the next entry), the CTA-pair path (M > 128 with enough work), and
+16 x 16 x 16 tiles on the HBM-streaming kernel with every blgp pattern.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_dense_02_gb300 import binding, synth
+
+from helpers import check, check16, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mixed_precision_dense_02_gb300 import build
+    build.build()
+    binding.load()
+    yield
+    binding.device_status()
+
+
+def run(bi, *, use_c=True, acc=None):
+    import torch
+    D = binding.gemm_batched(to_dev(bi.A, bi.dtype_in), to_dev(bi.B, bi.dtype_in),
+                             to_dev(bi.C, bi.dtype_in) if use_c else None,
+                             group=bi.group, abid=bi.abid, blgp=bi.blgp, acc=acc)
+    torch.cuda.synchronize()
+    if D.dtype in (torch.float16, torch.bfloat16):   # 16-bit results as bits
+        return D.view(torch.int16).cpu().numpy().view(np.uint16)
+    return D.cpu().numpy()
+
+
+def absab(bi):
+    """(|A| |B|) per output, the scale of the floating-point tolerance."""
+    if bi.dtype_in in ("f16", "bf16"):
+        a, b = bi.A & 0x7FFF, bi.B & 0x7FFF
+    else:
+        a, b = np.abs(bi.A), np.abs(bi.B)
+    return oracle.gemm_batched(bi.dtype_in, a, b, None, group=bi.group,
+                               abid=bi.abid, blgp=bi.blgp).astype(np.float64)
+
+
+def want(bi, use_c=True):
+    return oracle.gemm_batched(bi.dtype_in, bi.A, bi.B, bi.C if use_c else None,
+                               group=bi.group, abid=bi.abid, blgp=bi.blgp)
+
+
+# (M, N, K): K a multiple of 8 (16-bit rows of 16 bytes), N of 4 (FP32 rows)
+SHAPES = [(24, 40, 32), (128, 128, 64), (130, 200, 136), (64, 264, 520),
+          (1, 8, 8), (200, 4, 1000)]
+GROUPS = [(1, 0, 0), (4, 1, 0), (2, 1, 3), (16, 15, 5), (8, 3, 1), (4, 2, 7)]
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("G,abid,blgp", GROUPS)
+def test_generic_f16_bf16(dtype_in, M, N, K, G, abid, blgp):
+    bi = synth.batched_inputs(f"bg_{M}_{N}_{K}", dtype_in, 16, M=M, N=N, K=K,
+                              group=G, abid=abid, blgp=blgp)
+    check(dtype_in, run(bi), want(bi), absab(bi),
+          f"{dtype_in} {M}x{N}x{K} G={G} abid={abid} blgp={blgp}")
+
+
+def test_generic_no_c_and_pair_path():
+    """C = None, and entries with M > 128 and 2^30 multiply-adds in all
+    (the CTA-pair kernel): 64 entries of 256 x 256 x 256."""
+    bi = synth.batched_inputs("bg_pair", "bf16", 64, M=256, N=256, K=256,
+                              group=4, abid=3, blgp=3)
+    check("bf16", run(bi, use_c=False), want(bi, use_c=False), absab(bi),
+          "bf16 256^3 x 64, pair path, no C")
+    bi = synth.batched_inputs("bg_pair_r", "f16", 16, M=300, N=136, K=264,
+                              group=2, abid=0, blgp=6)
+    check("f16", run(bi), want(bi), absab(bi), "f16 300x136x264, ragged pair")
+
+
+@pytest.mark.parametrize("M,N,K,G,abid,blgp", [(24, 40, 32, 4, 1, 0),
+                                               (130, 200, 1040, 2, 1, 3),
+                                               (256, 128, 2048, 4, 0, 4)])
+def test_generic_i8_exact(M, N, K, G, abid, blgp):
+    bi = synth.batched_inputs(f"bg_i8_{M}", "i8", 16, M=M, N=N, K=K, group=G,
+                              abid=abid, blgp=blgp)
+    check("i8", run(bi), want(bi), None, f"i8 {M}x{N}x{K} G={G} blgp={blgp}")
+
+
+@pytest.mark.parametrize("M,N,K,G,abid,blgp", [(24, 40, 32, 4, 1, 0),
+                                               (130, 66, 70, 2, 1, 3),
+                                               (64, 64, 64, 16, 7, 5)])
+def test_generic_f64(M, N, K, G, abid, blgp):
+    bi = synth.batched_inputs(f"bg_f64_{M}", "f64", 16, M=M, N=N, K=K, group=G,
+                              abid=abid, blgp=blgp)
+    got, w = run(bi), want(bi)
+    ab = absab(bi)
+    check("f64", got, w, ab, f"f64 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K,G,abid,blgp", [(24, 40, 32, 4, 1, 2),
+                                               (136, 264, 200, 8, 6, 3)])
+def test_generic_16bit_accumulate(dtype_in, M, N, K, G, abid, blgp):
+    """FP16->FP16 / BF16->BF16: each entry against the single-problem
+    16-bit-accumulate oracle on the tiles the source maps select."""
+    bi = synth.batched_inputs(f"bg_h_{M}", dtype_in, 16, M=M, N=N, K=K,
+                              group=G, abid=abid, blgp=blgp, acc16=True)
+    got = run(bi, acc="same")
+    for b in range(bi.batch):
+        sa = (b // G) * G + abid
+        sb = (b // 4) * 4 + oracle.blgp_source(blgp, b % 4)
+        w, ab = oracle.gemm_acc16(dtype_in, bi.A[sa], bi.B[sb], bi.C[b],
+                                  want_absab=True)
+        check16(dtype_in, got[b], w, ab, f"{dtype_in}->16 entry {b}")
+
+
+@pytest.mark.parametrize("blgp", range(8))
+def test_16x16x16_every_blgp(blgp):
+    """16^3 tiles take the HBM-streaming kernel; every lane-group pattern,
+    with an A broadcast at the same time."""
+    bi = synth.batched_inputs(f"b16_blgp_{blgp}", "bf16", 1024, group=4, abid=2,
+                              blgp=blgp)
+    check("bf16", run(bi), want(bi), absab(bi), f"16^3 blgp={blgp}")
+
+
+@pytest.mark.parametrize("path", ["stream", "tcgen05"])
+def test_blgp_identifies_source_tiles(path):
+    """B tile t = (t+1) I, A = I, C = 0: D_b = (bsrc(b)+1) I, read off D,
+    for the rotation pattern (3) on both batched kernels."""
+    import torch
+    n = 16 if path == "stream" else 24
+    batch = 8
+    eye = np.eye(n, dtype=bool)
+    A = np.broadcast_to(np.where(eye, np.uint16(0x3F80), np.uint16(0)),
+                        (batch, n, n)).copy()
+    B = np.zeros((batch, n, n), np.uint16)
+    for t in range(batch):
+        B[t] = np.where(eye, synth.round_bf16_bits(np.array([t + 1.0]))[0], 0)
+    D = binding.gemm_batched(to_dev(A, "bf16"), to_dev(B, "bf16"), None, blgp=3)
+    torch.cuda.synchronize()
+    D = D.cpu().numpy()
+    for b in range(batch):
+        src = (b // 4) * 4 + (b + 1) % 4
+        assert np.array_equal(D[b], (src + 1) * np.eye(n, dtype=np.float32)), b
+
+
+def test_k_zero_and_empty():
+    import torch
+    bi = synth.batched_inputs("bg_k0", "bf16", 8, M=24, N=40, K=8, group=2, abid=1)
+    dev = torch.device("cuda:0")
+    A = torch.zeros((8, 24, 0), dtype=torch.bfloat16, device=dev)
+    B = torch.zeros((8, 40, 0), dtype=torch.bfloat16, device=dev)
+    C = to_dev(bi.C)
+    D = binding.gemm_batched(A, B, C, group=2, abid=1)
+    torch.cuda.synchronize()
+    assert torch.equal(D, C)
