@@ -232,7 +232,9 @@ def roofline_bound(name, w):
 
 def kernel_source(w):
     if w["kind"] == "batched":
-        return "mixed_precision_dense_02_gb300/csrc/batched16.cu"
+        if (w["M"], w["N"], w["K"]) == (16, 16, 16):
+            return "mixed_precision_dense_02_gb300/csrc/batched16.cu"
+        return "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu"
     if w["dtype_in"] == "i8" and not i8_on_tensor_pipe(w):
         return "mixed_precision_dense_02_gb300/csrc/gemm_i8.cu"
     return {"f16": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",

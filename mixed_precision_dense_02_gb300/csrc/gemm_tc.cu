@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // terms of the warp's HALF columns, one per lane per group of 32 (each
     // lane loads one; shuffles hand them to the others).  Zero when absent
     // or outside the problem.
-    constexpr int TG = HALF / 32;
+    constexpr int TG = (HALF + 31) / 32;
     [[maybe_unused]] auto load_terms = [&](int r0, int c0, int64_t& rt,
                                            int64_t (&ct)[TG]) {
       const int row = r0 + lane;
@@ -1074,20 +1074,35 @@ int cluster_size(int64_t M, int64_t N, int64_t K, int64_t batch = 1) {
   return (M > BM && work >= 1073741824.0) ? 2 : 1;
 }
 
-// Tile width (columns of D per CTA): 256 when there are enough such tiles
-// to occupy every SM, else 128 (more, smaller tiles).  Measured on the
-// INT8 4096^3, BF16 8192^3 and 16384 x 128 x 4096 workloads, 256-wide tiles
-// beat 192 and 128 wherever they fill the chip.  MMA_GB300_TILE_N (128 or
-// 256) overrides the choice, for tuning.
-int tile_n(const Ctx& ctx, int64_t M, int64_t N, int64_t batch = 1) {
+// Tile width (columns of D per CTA or CTA pair): 256 when there are enough
+// such tiles to occupy every SM, else 128 (more, smaller tiles).  CTA pairs
+// with FP32 or exact-INT32 results may also take 224-wide tiles: the width
+// with the smaller wave cost ceil(units / pairs) * width wins (ties go to
+// 256).  Measured: at 4096^3 the 224-wide tiles fill exactly four waves of
+// the 76 pairs (304 units) where 256-wide ones leave the fourth wave 37 %
+// full, 6 % faster for INT8 and BF16; at 8192^3 both need the same waves
+// and 256 is 6 % faster.  MMA_GB300_TILE_N (128, 224 or 256) overrides the
+// choice, for tuning.
+int tile_n(const Ctx& ctx, int64_t M, int64_t N, int64_t batch = 1,
+           int cl = 1, bool allow224 = false) {
   static const int forced = [] {
     const char* e = getenv("MMA_GB300_TILE_N");
     const int v = e ? atoi(e) : 0;
-    return (v == 128 || v == 256) ? v : 0;
+    return (v == 128 || v == 224 || v == 256) ? v : 0;
   }();
   if (forced) return forced;
   const int64_t wide_tiles = ((M + BM - 1) / BM) * ((N + 255) / 256) * batch;
-  return (N > 128 && wide_tiles >= ctx.num_sms) ? 256 : 128;
+  if (!(N > 128 && wide_tiles >= ctx.num_sms)) return 128;
+  if (cl == 2 && allow224) {
+    const int64_t pairs = ctx.num_sms / 2;
+    const int64_t m_units = (M + 2 * BM - 1) / (2 * BM) * batch;
+    auto cost = [&](int64_t bn) {
+      const int64_t units = m_units * ((N + bn - 1) / bn);
+      return (units + pairs - 1) / pairs * bn;
+    };
+    if (cost(224) < cost(256)) return 224;
+  }
+  return 256;
 }
 
 template <bool BF16, Epi EPI>
@@ -1102,7 +1117,13 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
   // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
   // tiles, whose 48 KB stages leave room for only 4 of them).
   if constexpr (EPI != Epi::I32SAT) {
-    if (bn == 256)
+    // 224-wide pair tiles (FP32 and exact-INT32 results: 112 columns per
+    // epilogue warp, seven 16-column blocks)
+    if constexpr (EPI == Epi::F32 || EPI == Epi::I32EXACT) {
+      if (bn == 224 && cl == 2)
+        return run<224, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+    }
+    if (bn >= 224)
       return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
                      : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
   }
@@ -1183,8 +1204,8 @@ mma_status_t dispatch_f16(const Ctx& ctx, bool pdl, bool bf16, int64_t M,
                           int64_t N, int64_t K, const void* A, int64_t lda,
                           const void* B, int64_t ldb, const void* C,
                           int64_t ldc, void* D, int64_t ldd) {
-  const int bn = tile_n(ctx, M, N);
   const int cl = cluster_size(M, N, K);
+  const int bn = tile_n(ctx, M, N, 1, cl, EPI == Epi::F32);
   return bf16 ? dispatch<true, EPI>(ctx, pdl, bn, cl, M, N, K, A, lda, B, ldb,
                                     C, ldc, D, ldd)
               : dispatch<false, EPI>(ctx, pdl, bn, cl, M, N, K, A, lda, B,
@@ -1283,10 +1304,10 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
     return dispatch<true, Epi::I32SAT>(ctx, true, 128, cluster_size(M, N, K),
                                        M, N, K, W, ldw, Bw, ldw, C, ldc, D,
                                        ldd, row_term, col_term);
-  return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N),
-                                       cluster_size(M, N, K), M, N, K, W, ldw,
-                                       Bw, ldw, C, ldc, D, ldd, row_term,
-                                       col_term);
+  const int cl = cluster_size(M, N, K);
+  return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N, 1, cl, true),
+                                       cl, M, N, K, W, ldw, Bw, ldw, C, ldc, D,
+                                       ldd, row_term, col_term);
 }
 
 mma_status_t launch_gemm_tc_batched(const Ctx& ctx, bool bf16, bool out16,
@@ -1297,8 +1318,8 @@ mma_status_t launch_gemm_tc_batched(const Ctx& ctx, bool bf16, bool out16,
                                     int group, int abid, int blgp) {
   if (batch > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
   const BatchArgs bat{int(batch), group, abid, blgp};
-  const int bn = tile_n(ctx, M, N, batch);
   const int cl = cluster_size(M, N, K, batch);
+  const int bn = tile_n(ctx, M, N, batch, cl, !out16);
   if (out16)
     return bf16 ? dispatch<true, Epi::H16>(ctx, false, bn, cl, M, N, K, A, lda,
                                            B, ldb, C, ldc, D, ldd, nullptr,
@@ -1344,9 +1365,10 @@ mma_status_t launch_gemm_i8_tc_batched(const Ctx& ctx, int64_t M, int64_t N,
       A, lda, int(rows_a), B, ldb, int(rows_b), int(K), W, ldw);
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
   const BatchArgs bat{int(batch), group, abid, blgp};
-  return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N, batch),
-                                       cluster_size(M, N, K, batch), M, N, K,
-                                       W, ldw, Bw, ldw, C, ldc, D, ldd,
+  const int cl = cluster_size(M, N, K, batch);
+  return dispatch<true, Epi::I32EXACT>(ctx, true,
+                                       tile_n(ctx, M, N, batch, cl, true), cl,
+                                       M, N, K, W, ldw, Bw, ldw, C, ldc, D, ldd,
                                        nullptr, nullptr, bat);
 }
 

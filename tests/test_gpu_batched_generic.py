@@ -164,3 +164,27 @@ def test_k_zero_and_empty():
     D = binding.gemm_batched(A, B, C, group=2, abid=1)
     torch.cuda.synchronize()
     assert torch.equal(D, C)
+
+
+def test_full_size_generic_batched_workload():
+    """8192 entries of 128 x 128 x 128 BF16 with groups of 4 (source 1):
+    sampled entries (and the last) against the oracle on those entries'
+    tiles; every output finite."""
+    import torch
+    name = "batched_bf16_128x128x128_b8192_g4_abid1"
+    w = synth.WORKLOADS[name]
+    bi = synth.batched_inputs(name, "bf16", w["batch"], M=w["M"], N=w["N"],
+                              K=w["K"], group=w["group"], abid=w["abid"],
+                              dist=w["dist"])
+    D = binding.gemm_batched(to_dev(bi.A, "bf16"), to_dev(bi.B, "bf16"),
+                             to_dev(bi.C), group=bi.group, abid=bi.abid)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(D).all())
+    rng = np.random.default_rng(99)
+    ents = np.unique(np.append(rng.choice(bi.batch, 63, replace=False), bi.batch - 1))
+    src = (ents // bi.group) * bi.group + bi.abid
+    A, B, C = (np.ascontiguousarray(x) for x in (bi.A[src], bi.B[ents], bi.C[ents]))
+    want = oracle.gemm_batched("bf16", A, B, C)
+    ab = oracle.gemm_batched("bf16", A & 0x7FFF, B & 0x7FFF, None).astype(np.float64)
+    got = D[torch.from_numpy(ents).cuda()].cpu().numpy()
+    check("bf16", got, want, ab, name)
