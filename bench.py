@@ -54,12 +54,15 @@ NOMINAL_FP64_TFLOPS = 1.25
 # source makes the figure stale, and it is then reported as null).
 NCU_TRAFFIC: dict = {
     # ncu --set full, one launch after the warm-up launches (profiles/*.md)
-    "gemm_i8_4096": {"sha": "5e3f86df3c1b5816", "bytes": 184445952 + 43882496},
-    "gemm_bf16_8192": {"sha": "5e3f86df3c1b5816", "bytes": 1566695000 + 258763008},
-    "gemm_bf16_skinny_16384x128x4096": {"sha": "5e3f86df3c1b5816",
-                                        "bytes": 143704832 + 3984384},
-    "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "24a0b2e421dd643e",
-                                               "bytes": 436229888 + 226331648},
+    "gemm_i8_4096": {"sha": "5246b09e2a4af693", "bytes": 192796160 + 43637248},
+    "gemm_u8_4096_clamp": {"sha": "5246b09e2a4af693", "bytes": 150888192 + 47247616},
+    "gemm_bf16_8192": {"sha": "5246b09e2a4af693", "bytes": 1566679000 + 257689600},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "5246b09e2a4af693",
+                                        "bytes": 143708928 + 3910656},
+    "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "795afc87d77db152",
+                                               "bytes": 436287232 + 223953408},
+    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "5246b09e2a4af693",
+                                                "bytes": 882545664 + 498531584},
 }
 
 
