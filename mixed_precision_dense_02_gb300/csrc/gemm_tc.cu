@@ -62,9 +62,16 @@ constexpr int kGroupM = 16;
 //            and after the last), and each 64-bit sum plus C is clamped
 //            once.  BN = 128 only (the 64-bit sums take the other half of
 //            TMEM).
-enum class Epi { F32, I32EXACT, H16, I32SAT };
+//   I32SATW  as I32SAT, on any tile width, for problems whose correction
+//            terms plus chunk sums stay inside the INT32 range (checked on
+//            the host; K up to about 32000): the INT32 sums start from the
+//            terms like I32EXACT's, never wrap, and each output is widened
+//            to 64 bits only to add C and clamp; no TMEM folds.
+enum class Epi { F32, I32EXACT, H16, I32SAT, I32SATW };
 
-constexpr bool int_mode(Epi e) { return e == Epi::I32EXACT || e == Epi::I32SAT; }
+constexpr bool int_mode(Epi e) {
+  return e == Epi::I32EXACT || e == Epi::I32SAT || e == Epi::I32SATW;
+}
 
 // Chunk depth of the exact 8-bit integer modes: every partial sum must stay
 // within 2^24 in magnitude, the range where FP32 represents all integers.
@@ -431,6 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int PF = NSTG > 2 ? NSTG - 2 : 1;
     constexpr int WAITN = NSTG - PF - 1;
     static_assert(PF <= NBLK, "C is prefetched at most one tile ahead");
+    // Before the first unit every ring slot is free, so the C of its first
+    // PF0 blocks is requested at once (a CTA with a single tile then has
+    // all of its C in flight while its main loop runs).
+    constexpr int PF0 = NSTG < NBLK ? NSTG : NBLK;
     uint32_t g = 0;  // blocks emitted so far by this warp
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -549,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     if (has_c && lane == 0 && first_unit < units)
-      for (int jj = 0; jj < PF; ++jj) request_c(uint32_t(jj), first_unit, jj);
+      for (int jj = 0; jj < PF0; ++jj) request_c(uint32_t(jj), first_unit, jj);
     __syncwarp();
     for (int u = first_unit; u < units && ok; u += unit_step) {
       int row0, colh, zc;
@@ -561,10 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       [[maybe_unused]] int64_t rt = 0;
       [[maybe_unused]] int64_t ct[TG];
       if constexpr (int_mode(EPI)) {
-        // I32EXACT starts from the correction terms modulo 2^32; I32SAT
-        // adds them in 64 bits at its first fold.
+        // I32EXACT starts from the correction terms modulo 2^32 and
+        // I32SATW from their exact value (in range by the host's check);
+        // I32SAT adds them in 64 bits at its first fold.
         if (has_terms) load_terms(row0, colh, rt, ct);
-        if (EPI == Epi::I32EXACT && has_terms) {
+        if (EPI != Epi::I32SAT && has_terms) {
 #pragma unroll
           for (int j = 0; j < HALF; ++j)
             iacc[j] = uint32_t(uint64_t(rt + col_term_of(ct, j)));
@@ -620,7 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               jj -= NBLK;
               uu = u + unit_step;
             }
-            if (uu < units) request_c(g + PF, uu, jj);
+            if (uu < units && g + PF >= uint32_t(PF0))
+              request_c(g + PF, uu, jj);
           } else {
             bulk_wait_group_read<NSTG - 1>();  // slot's last store has read it
           }
@@ -680,8 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // exact 64-bit sum, saturated once to the INT32 range
             auto sat = [&](uint32_t cw, int e) {
-              int64_t v = int64_t((uint64_t(r[16 + e]) << 32) | r[e]) +
-                          int64_t(int32_t(cw));
+              int64_t v;
+              if constexpr (EPI == Epi::I32SAT)
+                v = int64_t((uint64_t(r[16 + e]) << 32) | r[e]);
+              else  // I32SATW: the exact sum (terms included) in INT32
+                v = int64_t(int32_t(iacc[j * 16 + e]));
+              v += int64_t(int32_t(cw));
               v = v < int64_t(INT32_MIN) ? int64_t(INT32_MIN) : v;
               v = v > int64_t(INT32_MAX) ? int64_t(INT32_MAX) : v;
               return uint32_t(int32_t(v));
@@ -1060,10 +1077,14 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
 }
 
 // Cluster size: CTA pairs sharing one MMA (cta_group::2) for problems large
-// enough to keep many pairs busy (at least two m-blocks); single CTAs
-// otherwise.
+// enough to keep many pairs busy (at least two m-blocks, 2^30 multiply-adds
+// and a full wave of 256 x 256 pair tiles); single CTAs otherwise.  With
+// fewer pair tiles than pairs every SM would hold one tile and the pairs'
+// synchronisation would buy nothing: the 16384 x 128 x 4096 BF16 product
+// (64 pair tiles) ran in 34.6 us as pairs and 32.6 us as 128 single CTAs.
 // MMA_GB300_CLUSTER (1 or 2) overrides the choice, for tuning.
-int cluster_size(int64_t M, int64_t N, int64_t K, int64_t batch = 1) {
+int cluster_size(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
+                 int64_t batch = 1) {
   static const int forced = [] {
     const char* e = getenv("MMA_GB300_CLUSTER");
     const int v = e ? atoi(e) : 0;
@@ -1071,7 +1092,10 @@ int cluster_size(int64_t M, int64_t N, int64_t K, int64_t batch = 1) {
   }();
   if (forced) return forced;
   const double work = double(M) * double(N) * double(K) * double(batch);
-  return (M > BM && work >= 1073741824.0) ? 2 : 1;
+  const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256) * batch;
+  return (M > BM && work >= 1073741824.0 && pair_tiles >= ctx.num_sms / 2)
+             ? 2
+             : 1;
 }
 
 // Tile width (columns of D per CTA or CTA pair): 256 when there are enough
@@ -1119,13 +1143,22 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
   if constexpr (EPI != Epi::I32SAT) {
     // 224-wide pair tiles (FP32 and exact-INT32 results: 112 columns per
     // epilogue warp, seven 16-column blocks)
-    if constexpr (EPI == Epi::F32 || EPI == Epi::I32EXACT) {
+    if constexpr (EPI == Epi::F32 || EPI == Epi::I32EXACT ||
+                  EPI == Epi::I32SATW) {
       if (bn == 224 && cl == 2)
         return run<224, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
     }
     if (bn >= 224)
       return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
                      : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+  }
+  // Single CTAs on 128-wide tiles with at most four K steps per tile (small
+  // or batched small-block problems): the C stream is as large as the
+  // operand stream, so trade a ring stage for two more C staging slots
+  // (a whole tile of C in flight per warp).
+  if constexpr (EPI == Epi::F32) {
+    if (cl == 1 && (K + BK - 1) / BK <= 4)
+      return run<128, 4, BF16, EPI, 1, 6>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
   }
   return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
                  : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
@@ -1204,7 +1237,7 @@ mma_status_t dispatch_f16(const Ctx& ctx, bool pdl, bool bf16, int64_t M,
                           int64_t N, int64_t K, const void* A, int64_t lda,
                           const void* B, int64_t ldb, const void* C,
                           int64_t ldc, void* D, int64_t ldd) {
-  const int cl = cluster_size(M, N, K);
+  const int cl = cluster_size(ctx, M, N, K);
   const int bn = tile_n(ctx, M, N, 1, cl, EPI == Epi::F32);
   return bf16 ? dispatch<true, EPI>(ctx, pdl, bn, cl, M, N, K, A, lda, B, ldb,
                                     C, ldc, D, ldd)
@@ -1300,11 +1333,22 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
         b_row_major ? nullptr : col_term, oa);
   }
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
-  if (clamp)
-    return dispatch<true, Epi::I32SAT>(ctx, true, 128, cluster_size(M, N, K),
-                                       M, N, K, W, ldw, Bw, ldw, C, ldc, D,
-                                       ldd, row_term, col_term);
-  const int cl = cluster_size(M, N, K);
+  const int cl = cluster_size(ctx, M, N, K);
+  if (clamp) {
+    // Largest magnitude of any partial INT32 sum when the sums start from
+    // the correction terms: each chunk adds at most 2^24, and
+    // |row term| + |column term| <= K * (128 ob + 128 oa + oa ob).
+    const double reach = double((K + kI8ChunkK - 1) / kI8ChunkK) * 16777216.0 +
+                         double(K) * double(128 * ob + 128 * oa + oa * ob);
+    if (reach < 2147483647.0)
+      return dispatch<true, Epi::I32SATW>(ctx, true,
+                                          tile_n(ctx, M, N, 1, cl, true), cl,
+                                          M, N, K, W, ldw, Bw, ldw, C, ldc, D,
+                                          ldd, row_term, col_term);
+    return dispatch<true, Epi::I32SAT>(ctx, true, 128, cl, M, N, K, W, ldw,
+                                       Bw, ldw, C, ldc, D, ldd, row_term,
+                                       col_term);
+  }
   return dispatch<true, Epi::I32EXACT>(ctx, true, tile_n(ctx, M, N, 1, cl, true),
                                        cl, M, N, K, W, ldw, Bw, ldw, C, ldc, D,
                                        ldd, row_term, col_term);
@@ -1318,7 +1362,7 @@ mma_status_t launch_gemm_tc_batched(const Ctx& ctx, bool bf16, bool out16,
                                     int group, int abid, int blgp) {
   if (batch > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
   const BatchArgs bat{int(batch), group, abid, blgp};
-  const int cl = cluster_size(M, N, K, batch);
+  const int cl = cluster_size(ctx, M, N, K, batch);
   const int bn = tile_n(ctx, M, N, batch, cl, !out16);
   if (out16)
     return bf16 ? dispatch<true, Epi::H16>(ctx, false, bn, cl, M, N, K, A, lda,
@@ -1365,7 +1409,7 @@ mma_status_t launch_gemm_i8_tc_batched(const Ctx& ctx, int64_t M, int64_t N,
       A, lda, int(rows_a), B, ldb, int(rows_b), int(K), W, ldw);
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
   const BatchArgs bat{int(batch), group, abid, blgp};
-  const int cl = cluster_size(M, N, K, batch);
+  const int cl = cluster_size(ctx, M, N, K, batch);
   return dispatch<true, Epi::I32EXACT>(ctx, true,
                                        tile_n(ctx, M, N, batch, cl, true), cl,
                                        M, N, K, W, ldw, Bw, ldw, C, ldc, D, ldd,

@@ -197,3 +197,24 @@ def test_full_size_u8_clamp_workload():
     got = D[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
     check("i8", got, want, None, name)
     assert ov > 0
+
+
+@pytest.mark.parametrize("K", [32000, 33024])
+def test_saturating_modes_either_side_of_the_int32_reach(K):
+    """Unsigned x unsigned with clamp: up to about K = 32000 the INT32 sums
+    start from the correction terms and never wrap (wide tiles); beyond, the
+    chunk sums are folded into 64-bit sums in tensor memory (128-wide
+    tiles).  Values at both ends of uint8 push the terms and partial sums
+    to their extremes on either side of the switch."""
+    M, N = 136, 200
+    A = np.zeros((M, K), np.uint8)
+    A[1::2] = 255
+    A[::5, : K // 2] = 7
+    B = np.zeros((N, K), np.uint8)
+    B[::2] = 255
+    B[::7, K // 3:] = 128
+    C = synth.int_uniform(0, 23, M * N, I32_MIN, I32_MAX).astype(np.int32).reshape(M, N)
+    for clamp in (False, True):
+        want, _ = oracle.gemm_i8_ex(A, B, C, clamp=clamp)
+        got = run_i8x(A, B, C, clamp=clamp)
+        check("i8", got, want, None, f"uu K={K} clamp={clamp}")
