@@ -54,15 +54,15 @@ NOMINAL_FP64_TFLOPS = 1.25
 # source makes the figure stale, and it is then reported as null).
 NCU_TRAFFIC: dict = {
     # ncu --set full, one launch after the warm-up launches (profiles/*.md)
-    "gemm_i8_4096": {"sha": "5246b09e2a4af693", "bytes": 192796160 + 43637248},
-    "gemm_u8_4096_clamp": {"sha": "5246b09e2a4af693", "bytes": 150888192 + 47247616},
-    "gemm_bf16_8192": {"sha": "5246b09e2a4af693", "bytes": 1566679000 + 257689600},
-    "gemm_bf16_skinny_16384x128x4096": {"sha": "5246b09e2a4af693",
-                                        "bytes": 143708928 + 3910656},
+    "gemm_i8_4096": {"sha": "d4f2c4571a8cf9cb", "bytes": 188936192 + 44193536},
+    "gemm_u8_4096_clamp": {"sha": "d4f2c4571a8cf9cb", "bytes": 189157888 + 43582976},
+    "gemm_bf16_8192": {"sha": "d4f2c4571a8cf9cb", "bytes": 1577342000 + 259705088},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "d4f2c4571a8cf9cb",
+                                        "bytes": 143704832 + 3561472},
     "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "795afc87d77db152",
-                                               "bytes": 436287232 + 223953408},
-    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "5246b09e2a4af693",
-                                                "bytes": 882545664 + 498531584},
+                                               "bytes": 436228352 + 225458688},
+    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "d4f2c4571a8cf9cb",
+                                                "bytes": 876352512 + 496451072},
 }
 
 
