@@ -242,6 +242,23 @@ mma_status_t mma_gemm_batched_ex(int dtype_in, int dtype_acc, int64_t M,
 mma_status_t mma_device_status(void *stream);
 
 /*
+ * mma_selftest_wait_timeout -- exercise the failure-detection path of the
+ * kernels without faulting or hanging the GPU.  The pages have no
+ * counterpart; it backs mma_device_status's contract with a test.
+ *
+ * Every pipeline wait inside the kernels is bounded: when one runs out, the
+ * kernel records MMA_ERR_TIMEOUT in the device status word, drains and
+ * returns.  This call enqueues on `stream` one tiny kernel that performs
+ * that same bounded wait on a barrier that nothing ever signals, with the
+ * limit `limit_ns` (1000 .. 10^10 nanoseconds), so the wait runs out after
+ * about limit_ns and the kernel returns.  A following mma_device_status
+ * (stream) then returns MMA_ERR_TIMEOUT once and clears the word; the
+ * context stays usable.  Returns MMA_ERR_INVALID_ARG for a limit out of
+ * range, MMA_ERR_NO_DEVICE without a device, else MMA_OK.
+ */
+mma_status_t mma_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+/*
  * mma_profile_begin / mma_profile_end -- per-launch timing of the dominant
  * kernel (the contraction kernel of each mma_gemm* call), for measuring it
  * against its roofline.  The pages time each kernel launch after warm-up

@@ -39,6 +39,7 @@ SIGNATURES = {
     "mma_gemm_i8_noalloc": (_int, [_i64, _i64, _i64, _p, _i64, _p, _i64, _p,
                                    _i64, _p, _i64, _p]),
     "mma_device_status": (_int, [_p]),
+    "mma_selftest_wait_timeout": (_int, [_i64, _p]),
     "mma_profile_begin": (_int, []),
     "mma_profile_end": (_int, [ctypes.POINTER(ctypes.c_float), _int,
                                ctypes.POINTER(_int)]),
@@ -131,6 +132,12 @@ def mma_gemm_i8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd,
 
 def mma_device_status(stream) -> int:
     return load().mma_device_status(stream)
+
+
+def mma_selftest_wait_timeout(limit_ns, stream) -> int:
+    """Run one bounded wait that is made to run out (failure-detection
+    self-test); mma_device_status then reports MMA_ERR_TIMEOUT once."""
+    return load().mma_selftest_wait_timeout(limit_ns, stream)
 
 
 def mma_status_string(status: int) -> str:

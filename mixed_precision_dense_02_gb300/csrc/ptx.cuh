@@ -127,11 +127,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns
 // false (without completing) if another role of the CTA has raised `abort`
-// or if the wait exceeded kWaitLimitNs, in which case this call raises
+// or if the wait exceeded limit_ns (kWaitLimitNs unless a caller gives a
+// shorter limit), in which case this call raises
 // `abort` and records the timeout in *status.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag,
-                                          unsigned* status) {
+__device__ __forceinline__ bool mbar_wait(
+    uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* status,
+    unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   unsigned long long t0 = global_timer_ns();
@@ -139,7 +140,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStatusTimeout);
         return false;

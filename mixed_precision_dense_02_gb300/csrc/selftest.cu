@@ -1,0 +1,51 @@
+// mma_selftest_wait_timeout: the failure-detection path of the pipeline
+// kernels, exercised on purpose without faulting or hanging the GPU.
+//
+// Every wait of the tcgen05 pipeline (TMA stage, accumulator hand-off, C
+// block) is mbar_wait from ptx.cuh: bounded by a time limit, after which it
+// raises the CTA's abort flag, records MMA_ERR_TIMEOUT in the library's
+// device status word and returns false, so the kernel drains and exits and
+// the context stays usable.  This kernel runs that same wait on an mbarrier
+// that no thread ever arrives on, with a short caller-chosen limit, so the
+// wait runs out exactly as a stuck pipeline's would.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mmagb {
+namespace {
+
+__global__ void wait_timeout_kernel(unsigned* status,
+                                    unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);  // expects one arrival, which never comes
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // returns false after limit_ns, having recorded the timeout
+    (void)mbar_wait(&bar, 0u, &abort_flag, status, limit_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace mmagb
+
+using namespace mmagb;
+
+extern "C" mma_status_t mma_selftest_wait_timeout(int64_t limit_ns,
+                                                  void* stream) {
+  // 1 us .. 10 s
+  if (limit_ns < 1000 || limit_ns > 10000000000ll) return MMA_ERR_INVALID_ARG;
+  Ctx ctx{};
+  if (!current_ctx(stream, &ctx)) return MMA_ERR_NO_DEVICE;
+  wait_timeout_kernel<<<1, 32, 0, ctx.stream>>>(
+      ctx.status, static_cast<unsigned long long>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}

@@ -198,3 +198,12 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_HERE", str(tmp_path))
     with pytest.raises(RuntimeError, match="not built"):
         binding.load()
+
+
+def test_selftest_wait_timeout_arguments(lib):
+    assert binding.mma_selftest_wait_timeout(0, None) == INVALID
+    assert binding.mma_selftest_wait_timeout(999, None) == INVALID
+    assert binding.mma_selftest_wait_timeout(10 ** 10 + 1, None) == INVALID
+    import torch
+    if not torch.cuda.is_available():
+        assert binding.mma_selftest_wait_timeout(50_000_000, None) == NODEV
