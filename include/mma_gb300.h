@@ -111,7 +111,7 @@ typedef enum {
  * INT32, FP64 -> FP64 with round-to-nearest-even); "RDNA3 dense WMMA
  * builtins", section "Builtin reference" (srcA x srcB + srcC; signed int8).
  *
- * dtype_in, dtype_acc : one of the four pairs in the table above.
+ * dtype_in, dtype_acc : one of the pairs in the table above.
  * M, N, K             : problem size, each >= 0.
  * A, lda              : M x K row-major input, lda >= K.
  * B, ldb              : K x N column-major input (stored as N rows of K

@@ -311,17 +311,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// As umma_commit, arriving on the mbarrier at the offset of `bar` in every
-// CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
-      "multicast::cluster.b64 [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Warp-collective load of 32 consecutive 32-bit TMEM columns; lane i of the
 // warp receives TMEM lane (taddr.lane + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr,

@@ -238,7 +238,7 @@ def batched_inputs(workload: str, dtype_in: str, batch: int, M: int = 16,
     return BatchedInputs(dtype_in, batch, M, N, K, group, abid, A, B, C, blgp)
 
 
-# The five workloads, by what they are.
+# The workloads, by what they are.
 WORKLOADS = {
     "gemm_f16_256": dict(kind="gemm", dtype_in="f16", M=256, N=256, K=256,
                          dist="uniform"),
