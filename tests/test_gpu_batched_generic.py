@@ -76,15 +76,17 @@ def test_generic_f16_bf16(dtype_in, M, N, K, G, abid, blgp):
 
 
 def test_generic_no_c_and_pair_path():
-    """C = None, and entries with M > 128 and 2^30 multiply-adds in all
-    (the CTA-pair kernel): 64 entries of 256 x 256 x 256."""
-    bi = synth.batched_inputs("bg_pair", "bf16", 64, M=256, N=256, K=256,
+    """C = None, and entries with M > 128, more than 2^30 multiply-adds and
+    at least one 256 x 256 pair tile per CTA pair (the CTA-pair kernel):
+    80 entries of 256 x 256 x 256."""
+    bi = synth.batched_inputs("bg_pair", "bf16", 80, M=256, N=256, K=256,
                               group=4, abid=3, blgp=3)
     check("bf16", run(bi, use_c=False), want(bi, use_c=False), absab(bi),
-          "bf16 256^3 x 64, pair path, no C")
-    bi = synth.batched_inputs("bg_pair_r", "f16", 16, M=300, N=136, K=264,
+          "bf16 256^3 x 80, pair path, no C")
+    # ragged M (300 = 256 + 44) on pairs: 100 entries, 2^30 multiply-adds
+    bi = synth.batched_inputs("bg_pair_r", "f16", 100, M=300, N=136, K=264,
                               group=2, abid=0, blgp=6)
-    check("f16", run(bi), want(bi), absab(bi), "f16 300x136x264, ragged pair")
+    check("f16", run(bi), want(bi), absab(bi), "f16 300x136x264 x 100, ragged pair")
 
 
 @pytest.mark.parametrize("M,N,K,G,abid,blgp", [(24, 40, 32, 4, 1, 0),

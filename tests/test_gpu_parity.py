@@ -361,3 +361,27 @@ def test_full_size_batched_workload():
     got = run_batched(bi)
     want = oracle.gemm_batched("bf16", bi.A, bi.B, bi.C, group=bi.group, abid=bi.abid)
     check("bf16", got, want, batched_absab(bi), name)
+
+
+@pytest.mark.parametrize("dtype_in", ["bf16", "f16", "i8"])
+def test_ragged_shapes_on_cta_pairs(dtype_in):
+    """A problem the automatic choice runs on CTA pairs (M > 128, more than
+    2^30 multiply-adds, at least one 256 x 256 pair tile per pair), ragged
+    in every dimension: M = 2000 (= 7 * 256 + 208), N = 2600, K = 1000.
+    Sampled rows (with the last) against the oracle."""
+    import torch
+    M, N, K = 2000, 2600, 1000
+    g = synth.gemm_inputs(f"pair_ragged_{dtype_in}", dtype_in, M, N, K, dist="uniform")
+    D = binding.gemm(dev_padded(g.A, dtype_in), dev_padded(g.B, dtype_in),
+                     dev_padded(g.C))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.append(rng.choice(M, 90, replace=False), [M - 1, M - 208]))
+    A = np.ascontiguousarray(g.A[rows])
+    C = np.ascontiguousarray(g.C[rows])
+    got = D[torch.from_numpy(rows).cuda()].cpu().numpy()
+    if dtype_in == "i8":
+        check("i8", got, oracle.gemm("i8", A, g.B, C), None, "i8 ragged pairs")
+    else:
+        want, ab = oracle.gemm(dtype_in, A, g.B, C, want_absab=True)
+        check(dtype_in, got, want, ab, f"{dtype_in} ragged pairs")
