@@ -237,6 +237,8 @@ def kernel_source(w):
     if w["kind"] == "batched":
         if (w["M"], w["N"], w["K"]) == (16, 16, 16):
             return "mixed_precision_dense_02_gb300/csrc/batched16.cu"
+        if w["M"] * w["N"] * w["K"] <= 96 * 96 * 64:
+            return "mixed_precision_dense_02_gb300/csrc/batched_mma.cu"
         return "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu"
     if w["dtype_in"] == "i8" and not i8_on_tensor_pipe(w):
         return "mixed_precision_dense_02_gb300/csrc/gemm_i8.cu"

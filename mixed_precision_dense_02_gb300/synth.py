@@ -256,6 +256,11 @@ WORKLOADS = {
     # BF16 -> BF16 accumulate (16-bit addend and result), large square shape
     "gemm_bf16_acc16_8192": dict(kind="gemm", dtype_in="bf16", M=8192, N=8192,
                                  K=8192, dist="normal", acc16=True),
+    # batched 32 x 32 x 32 blocks (the warp-level streaming kernel), groups
+    # of 4 with source 1
+    "batched_bf16_32x32x32_b65536_g4_abid1": dict(
+        kind="batched", dtype_in="bf16", batch=65536, M=32, N=32, K=32,
+        group=4, abid=1, dist="uniform"),
     # batched 128 x 128 x 128 tiles (larger blocks than the 16^3 form) with
     # the A block of each group of 4 broadcast from entry 1 of the group
     "batched_bf16_128x128x128_b8192_g4_abid1": dict(

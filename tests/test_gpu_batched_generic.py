@@ -168,12 +168,14 @@ def test_k_zero_and_empty():
     assert torch.equal(D, C)
 
 
-def test_full_size_generic_batched_workload():
-    """8192 entries of 128 x 128 x 128 BF16 with groups of 4 (source 1):
-    sampled entries (and the last) against the oracle on those entries'
-    tiles; every output finite."""
+@pytest.mark.parametrize("name", ["batched_bf16_128x128x128_b8192_g4_abid1",
+                                  "batched_bf16_32x32x32_b65536_g4_abid1"])
+def test_full_size_generic_batched_workload(name):
+    """The batched workloads of 128^3 blocks (tensor-memory GEMM) and 32^3
+    blocks (warp-level streaming kernel), groups of 4 (source 1): sampled
+    entries (and the last) against the oracle on those entries' tiles;
+    every output finite."""
     import torch
-    name = "batched_bf16_128x128x128_b8192_g4_abid1"
     w = synth.WORKLOADS[name]
     bi = synth.batched_inputs(name, "bf16", w["batch"], M=w["M"], N=w["N"],
                               K=w["K"], group=w["group"], abid=w["abid"],
@@ -190,3 +192,40 @@ def test_full_size_generic_batched_workload():
     ab = oracle.gemm_batched("bf16", A & 0x7FFF, B & 0x7FFF, None).astype(np.float64)
     got = D[torch.from_numpy(ents).cuda()].cpu().numpy()
     check("bf16", got, want, ab, name)
+
+
+# Dense blocks with M, N, K multiples of 16 and at most 96 * 96 * 64
+# multiply-adds take the warp-level streaming kernel (32 x 32 warp tiles
+# when M and N are multiples of 32, else 16 x 16; K in 32-deep chunks plus
+# a tail); (128, 128, 128) just beyond the limit takes the tensor-memory
+# GEMM.
+STREAM_SHAPES = [(32, 32, 32), (64, 64, 64), (16, 48, 80), (96, 64, 96),
+                 (64, 64, 144), (48, 16, 16), (32, 96, 16), (128, 128, 128)]
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", STREAM_SHAPES)
+@pytest.mark.parametrize("G,abid,blgp", [(1, 0, 0), (4, 1, 3), (8, 6, 5)])
+def test_streaming_kernel_shapes(dtype_in, M, N, K, G, abid, blgp):
+    bi = synth.batched_inputs(f"bs_{M}_{N}_{K}", dtype_in, 64, M=M, N=N, K=K,
+                              group=G, abid=abid, blgp=blgp)
+    check(dtype_in, run(bi), want(bi), absab(bi),
+          f"{dtype_in} {M}x{N}x{K} G={G} blgp={blgp}")
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(32, 32, 32), (16, 48, 80), (64, 64, 144)])
+def test_streaming_kernel_16bit_and_no_c(dtype_in, M, N, K):
+    bi = synth.batched_inputs(f"bs_h_{M}", dtype_in, 32, M=M, N=N, K=K,
+                              group=2, abid=1, blgp=2, acc16=True)
+    got = run(bi, acc="same")
+    for b in range(bi.batch):
+        sa = (b // 2) * 2 + 1
+        sb = (b // 4) * 4 + oracle.blgp_source(2, b % 4)
+        w, ab = oracle.gemm_acc16(dtype_in, bi.A[sa], bi.B[sb], bi.C[b],
+                                  want_absab=True)
+        check16(dtype_in, got[b], w, ab, f"{dtype_in}->16 {M}x{N}x{K} entry {b}")
+    bf = synth.batched_inputs(f"bs_n_{M}", dtype_in, 32, M=M, N=N, K=K,
+                              group=4, abid=0, blgp=7)
+    check(dtype_in, run(bf, use_c=False), want(bf, use_c=False), absab(bf),
+          f"{dtype_in} {M}x{N}x{K} no C")
