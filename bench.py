@@ -63,6 +63,8 @@ NCU_TRAFFIC: dict = {
                                                "bytes": 436228352 + 225458688},
     "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "d4f2c4571a8cf9cb",
                                                 "bytes": 876352512 + 496451072},
+    "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "ead9532501d7686b",
+                                              "bytes": 436271616 + 215038976},
 }
 
 
