@@ -1167,54 +1167,124 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
 }
 
 // Row-major B (K x N, N contiguous) -> K-major copy W (N rows of K, leading
-// dimension ldw) of 16-bit elements, through 64 x 64 shared-memory tiles so
-// that both the reads and the writes are coalesced.  With I8 the 8-bit
-// inputs are widened to their stored bfloat16 values on the way (exactly;
-// x -> (x ^ flip) - 128, as in i8x2_to_bf16x2), and with col_term each
-// column's sum of stored values times b_mul is added to col_term[n]
-// (64-bit atomics; col_term starts at zero).
+// dimension ldw) of 16-bit elements, through 64 x 64 shared-memory tiles
+// with 16-byte global accesses on both sides:
+//   * load: each thread reads 16 contiguous bytes of one row k of B (16
+//     int8 or 8 16-bit values) into the tile [k][n];
+//   * store: warp w writes the 8-deep K run w of the tile's 64 columns, 32
+//     columns per pass: each thread gathers tile[8w .. 8w+7][n] (a warp
+//     reads 32 consecutive columns of one tile row, conflict-free) and
+//     writes them as one 16-byte run of row n of W.
+// With I8 the 8-bit inputs are widened to their stored bfloat16 values on
+// the way (exactly; x -> (x ^ flip) - 128, as in i8x2_to_bf16x2), and with
+// col_term each column's sum of stored values times b_mul is added to
+// col_term[n] (64-bit atomics, one per column per tile; col_term starts at
+// zero).  Ragged edges fall back to element accesses.
+constexpr int kTrTile = 64;
+constexpr int kTrPad = 8;  // uint16 padding per tile row (16 bytes)
+
 template <bool I8>
 __global__ void __launch_bounds__(256)
     transpose_b_kernel(const void* __restrict__ Bv, int64_t ldb, int K, int N,
                        uint16_t* __restrict__ W, int64_t ldw, uint32_t flip,
                        int64_t* __restrict__ col_term, int64_t b_mul) {
-  __shared__ uint16_t tile[64][66];  // [k][n], padded
-  __shared__ int psum[4][64];        // per column, one per thread row
-  const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
-  int part = 0;  // this thread's column is threadIdx.x & 63 throughout
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int kk = i >> 6, nn = i & 63;
-    const int k = k0 + kk, n = n0 + nn;
-    uint16_t v = 0;
-    if (k < K && n < N) {
-      if constexpr (I8) {
-        const uint32_t x =
-            uint32_t(static_cast<const uint8_t*>(Bv)[int64_t(k) * ldb + n]) ^
-            (flip & 0xFFu);
-        v = flipped_byte_to_bf16(x);
-        part += int(x) - 128;
-      } else {
-        v = static_cast<const uint16_t*>(Bv)[int64_t(k) * ldb + n];
-      }
+  __shared__ __align__(16) uint16_t tile[kTrTile][kTrTile + kTrPad];  // [k][n]
+  __shared__ int psum[8][kTrTile];
+  const int n0 = blockIdx.x * kTrTile, k0 = blockIdx.y * kTrTile;
+  const int tid = threadIdx.x;
+  // ---- load: rows of B into the tile
+  if constexpr (I8) {
+    const uint8_t* B8 = static_cast<const uint8_t*>(Bv);
+    const int kk = tid >> 2, c = (tid & 3) * 16;  // 64 rows x 4 chunks
+    const int k = k0 + kk, n = n0 + c;
+    uint32_t u[16];
+    if (k < K && n + 16 <= N &&
+        (reinterpret_cast<uintptr_t>(B8 + int64_t(k) * ldb + n) & 15) == 0) {
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(B8 + int64_t(k) * ldb + n));
+      const uint32_t w[4] = {v.x ^ flip, v.y ^ flip, v.z ^ flip, v.w ^ flip};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) u[e] = (w[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        u[e] = (k < K && n + e < N)
+                   ? (uint32_t(B8[int64_t(k) * ldb + n + e]) ^ (flip & 0xFFu))
+                   : 128u;  // stored value 0
     }
-    tile[kk][nn] = v;
-  }
-  if (I8 && col_term != nullptr) {
-    psum[threadIdx.x >> 6][threadIdx.x & 63] = part;
-    __syncthreads();
-    if (threadIdx.x < 64 && n0 + int(threadIdx.x) < N) {
-      const int64_t c = int64_t(psum[0][threadIdx.x]) + psum[1][threadIdx.x] +
-                        psum[2][threadIdx.x] + psum[3][threadIdx.x];
-      atomicAdd(reinterpret_cast<unsigned long long*>(col_term + n0 +
-                                                      threadIdx.x),
-                static_cast<unsigned long long>(b_mul * c));
+    uint32_t o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      o[e] = uint32_t(flipped_byte_to_bf16(u[2 * e])) |
+             (uint32_t(flipped_byte_to_bf16(u[2 * e + 1])) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(&tile[kk][c]);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  } else {
+    const uint16_t* B16 = static_cast<const uint16_t*>(Bv);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int kk = (tid >> 3) + 32 * r, c = (tid & 7) * 8;  // 32 rows x 8
+      const int k = k0 + kk, n = n0 + c;
+      uint4 v;
+      if (k < K && n + 8 <= N &&
+          (reinterpret_cast<uintptr_t>(B16 + int64_t(k) * ldb + n) & 15) == 0) {
+        v = __ldcs(reinterpret_cast<const uint4*>(B16 + int64_t(k) * ldb + n));
+      } else {
+        uint16_t e16[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          e16[e] = (k < K && n + e < N) ? B16[int64_t(k) * ldb + n + e] : 0;
+        v = make_uint4(e16[0] | (uint32_t(e16[1]) << 16),
+                       e16[2] | (uint32_t(e16[3]) << 16),
+                       e16[4] | (uint32_t(e16[5]) << 16),
+                       e16[6] | (uint32_t(e16[7]) << 16));
+      }
+      *reinterpret_cast<uint4*>(&tile[kk][c]) = v;
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int nn = i >> 6, kk = i & 63;
-    const int n = n0 + nn, k = k0 + kk;
-    if (n < N && k < K) W[int64_t(n) * ldw + k] = tile[kk][nn];
+  // ---- store: 16-byte K runs of the rows of W
+  const int warp = tid >> 5, lane = tid & 31;
+  const int kr = warp * 8;  // this warp's K run within the tile
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int nn = lane + 32 * r;
+    uint16_t e16[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e16[i] = tile[kr + i][nn];
+    const int n = n0 + nn, k = k0 + kr;
+    if (n < N) {
+      uint16_t* dst = W + int64_t(n) * ldw + k;
+      if (k + 8 <= K) {
+        *reinterpret_cast<uint4*>(dst) =
+            make_uint4(e16[0] | (uint32_t(e16[1]) << 16),
+                       e16[2] | (uint32_t(e16[3]) << 16),
+                       e16[4] | (uint32_t(e16[5]) << 16),
+                       e16[6] | (uint32_t(e16[7]) << 16));
+      } else {
+        for (int i = 0; k + i < K; ++i) dst[i] = e16[i];
+      }
+    }
+    if constexpr (I8) {
+      // the run's stored values (exact small integers in bfloat16)
+      int part = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k + i < K) part += int(__uint_as_float(uint32_t(e16[i]) << 16));
+      psum[warp][nn] = part;
+    }
+  }
+  if constexpr (I8) {
+    if (col_term != nullptr) {
+      __syncthreads();
+      if (tid < kTrTile && n0 + tid < N) {
+        int64_t c = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) c += psum[w][tid];
+        atomicAdd(reinterpret_cast<unsigned long long*>(col_term + n0 + tid),
+                  static_cast<unsigned long long>(b_mul * c));
+      }
+    }
   }
 }
 
