@@ -48,6 +48,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_FP64_TFLOPS = 1.25
+NOMINAL_HBM_GBS = 7900.0
+# dense BF16 tensor-core rate per SM per clock (128 x 256 x 16 x 2 flops
+# per 128-cycle MMA), for the nominal denominators reported beside the
+# measured ones
+BF16_FLOP_PER_SM_CLK = 8192.0
 
 # DRAM bytes per launch of each dominant kernel from one ncu capture, keyed
 # by the SHA-256 of the kernel's source file at capture time (a changed
@@ -596,6 +601,26 @@ def run_reference(args, dist):
     return 0
 
 
+def add_nominal(roof, sms, clk):
+    """Context denominators beside the measured peak (frac stays against the
+    measured one): for the BF16 tensor pipe SMs x 8192 flop/clk x the
+    maximum SM clock and x the median SM clock of the timed region; for HBM
+    the nominal HBM3e bandwidth.  FP64 (DMMA pipe) gets none."""
+    if roof["unit"] == "GB/s":
+        roof["nominal_peak"] = NOMINAL_HBM_GBS
+        roof["frac_of_nominal"] = roof["achieved"] / NOMINAL_HBM_GBS
+        return
+    if "fp64" in roof.get("peak_note", roof.get("peak_source", "")):
+        return
+    mx, med = clk.get("sm_max_mhz"), clk.get("sm_mhz")
+    if mx:
+        roof["nominal_peak_max_clock"] = sms * BF16_FLOP_PER_SM_CLK * mx * 1e6 / 1e12
+    if med:
+        nom = sms * BF16_FLOP_PER_SM_CLK * med * 1e6 / 1e12
+        roof["nominal_peak_run_clock"] = nom
+        roof["frac_of_nominal_run_clock"] = roof["achieved"] / nom
+
+
 def _dtype_tag(w):
     if w["dtype_in"] == "i8":
         sa, sb = w.get("a_signed", True), w.get("b_signed", True)
@@ -647,6 +672,7 @@ def main(argv=None):
                            with_e2e=True, sustain_s=2.0)
     clocks.stop()
     clk = clocks.summary(*res["host_window"])
+    sms = torch.cuda.get_device_properties(dist.local_rank).multi_processor_count
 
     per_dtype = {}
     if not args.headline_only:
@@ -657,11 +683,14 @@ def main(argv=None):
             wm = workload_meta(name)
             k = 3 if wm["dtype_in"] == "f64" else max(3, min(args.steps, 20))
             r = measure_workload(torch, dist, name, k, 3, with_e2e=False)
+            # (the clock record covers the headline's timed region only)
+            add_nominal(r["roofline"], sms, {"sm_max_mhz": clk.get("sm_max_mhz")})
             per_dtype[name] = {"value": r["value"], "unit": r["unit"],
                                "ms_per_step": r["ms_per_step"], "steps": k,
                                "pct_of_bf16_peak": r["pct_of_bf16_peak"],
                                "l2": r["l2"],
                                "roofline": r["roofline"]}
+    add_nominal(res["roofline"], sms, clk)
 
     cpu = None
     if dist.rank == 0 and dist.world == 1:
