@@ -402,13 +402,17 @@ extern "C" mma_status_t mma_gemm_batched_ex(
                                 static_cast<const float*>(C),
                                 static_cast<float*>(D));
       // small and mid-size dense blocks: warp-level MMAs streaming from HBM
-      if (batched_mma_fits(M, N, K, lda, ldb, ldc, ldd, C != nullptr))
+      if (batched_mma_fits(M, N, K, lda, ldb, ldc, ldd, C != nullptr, false))
         return launch_batched_mma(ctx, bf16, out16, M, N, K, A, B, C, D, batch,
                                   G, abid, blgp);
       return launch_gemm_tc_batched(ctx, bf16, out16, M, N, K, A, lda, B, ldb,
                                     C, ldc, D, ldd, batch, G, abid, blgp);
     }
     case MMA_I8:
+      // small and mid-size dense blocks: integer warp-level MMAs, exact
+      if (batched_mma_fits(M, N, K, lda, ldb, ldc, ldd, C != nullptr, true))
+        return launch_batched_i8_mma(ctx, M, N, K, A, B, C, D, batch, G, abid,
+                                     blgp);
       return with_workspace(
           ctx, gemm_i8_tc_batched_workspace_bytes(M, N, K, batch),
           [&](void* ws) {

@@ -204,6 +204,123 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// INT8 -> INT32 (exact; the INT32 accumulators wrap like the INT8 GEMM's):
+// the same structure with m16n8k32 integer MMAs.  A lane's fragment bytes
+// for one 32-deep K step are the 8 contiguous physical k = 8t .. 8t+7 of a
+// row (one 8-byte load): the low word takes the fragment's k = 4t .. 4t+3,
+// the high word k = 16+4t .. 16+4t+3, identically in A and B.  K beyond the
+// block (K a multiple of 8) reads as zero.
+template <int MT, int NT>
+__global__ void __launch_bounds__(kThreads, 2)
+    batched_i8_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B,
+                      const int32_t* __restrict__ C, int32_t* __restrict__ D,
+                      int M, int N, int K, int64_t batch, int group, int abid,
+                      int blgp) {
+  constexpr int WM = 16 * MT, WN = 8 * NT;
+  constexpr int KS = 2;  // k32 steps per chunk: all their loads in flight
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int tiles_n = N / WN;
+  const int64_t per_entry = int64_t(M / WM) * tiles_n;
+  const int64_t units = batch * per_entry;
+  const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const int64_t b = u / per_entry;
+    const int r = int(u - b * per_entry);
+    const int tm = r / tiles_n, tn = r - tm * tiles_n;
+    const int64_t za = (b / group) * group + abid;
+    const int64_t zb = (b & ~int64_t(3)) + blgp_quarter(blgp, int(b & 3));
+    const int8_t* At = A + (za * M + tm * WM) * int64_t(K);
+    const int8_t* Bt = B + (zb * N + tn * WN) * int64_t(K);
+    const int64_t c0 = (b * M + tm * WM) * int64_t(N) + tn * WN;
+
+    int acc[MT][NT][4];
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+      for (int ni = 0; ni < NT; ++ni) {
+        const int64_t o0 = c0 + int64_t(mi * 16 + g) * N + ni * 8 + 2 * t;
+        const int64_t o1 = o0 + int64_t(8) * N;
+        if (C != nullptr) {
+          const int2 v0 = __ldcs(reinterpret_cast<const int2*>(C + o0));
+          const int2 v1 = __ldcs(reinterpret_cast<const int2*>(C + o1));
+          acc[mi][ni][0] = v0.x; acc[mi][ni][1] = v0.y;
+          acc[mi][ni][2] = v1.x; acc[mi][ni][3] = v1.y;
+        } else {
+          acc[mi][ni][0] = acc[mi][ni][1] = acc[mi][ni][2] = acc[mi][ni][3] = 0;
+        }
+      }
+
+    for (int k0 = 0; k0 < K; k0 += 32 * KS) {
+      uint2 af[KS][MT][2];
+      uint2 bf[KS][NT];
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        const int kk = k0 + s * 32 + 8 * t;
+        const bool in = kk < K;
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          af[s][mi][0] = in ? __ldg(reinterpret_cast<const uint2*>(
+                                  At + int64_t(mi * 16 + g) * K + kk))
+                            : make_uint2(0u, 0u);
+          af[s][mi][1] = in ? __ldg(reinterpret_cast<const uint2*>(
+                                  At + int64_t(mi * 16 + g + 8) * K + kk))
+                            : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int ni = 0; ni < NT; ++ni)
+          bf[s][ni] = in ? __ldg(reinterpret_cast<const uint2*>(
+                               Bt + int64_t(ni * 8 + g) * K + kk))
+                         : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        if (k0 + s * 32 < K) {
+#pragma unroll
+          for (int mi = 0; mi < MT; ++mi) {
+            const uint32_t a[4] = {af[s][mi][0].x, af[s][mi][1].x,
+                                   af[s][mi][0].y, af[s][mi][1].y};
+#pragma unroll
+            for (int ni = 0; ni < NT; ++ni) {
+              const uint32_t bb[2] = {bf[s][ni].x, bf[s][ni].y};
+              mma_s8_16832(acc[mi][ni], a, bb);
+            }
+          }
+        }
+      }
+    }
+
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+      for (int ni = 0; ni < NT; ++ni) {
+        const int64_t o0 = c0 + int64_t(mi * 16 + g) * N + ni * 8 + 2 * t;
+        const int64_t o1 = o0 + int64_t(8) * N;
+        __stcs(reinterpret_cast<int2*>(D + o0), make_int2(acc[mi][ni][0], acc[mi][ni][1]));
+        __stcs(reinterpret_cast<int2*>(D + o1), make_int2(acc[mi][ni][2], acc[mi][ni][3]));
+      }
+  }
+}
+
+template <int MT, int NT>
+mma_status_t run_i8(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
+                    const void* A, const void* B, const void* C, void* D,
+                    int64_t batch, int group, int abid, int blgp) {
+  const int64_t units = batch * (M / (16 * MT)) * (N / (8 * NT));
+  int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
+  const int64_t cap = int64_t(ctx.num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  ctx.mark_start();
+  batched_i8_kernel<MT, NT><<<int(blocks), kThreads, 0, ctx.stream>>>(
+      static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
+      static_cast<const int32_t*>(C), static_cast<int32_t*>(D), int(M),
+      int(N), int(K), batch, group, abid, blgp);
+  ctx.mark_stop();
+  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}
+
 template <int MT, int NT, bool BF16, bool OUT16>
 mma_status_t run(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
                  const void* A, const void* B, const void* C, void* D,
@@ -240,12 +357,17 @@ mma_status_t pick(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
 // kernel against the tensor-memory GEMM: 32^3 93 against 7, 64^3 73 against
 // 29, 96 x 96 x 64 65 against 58, 128^3 54 against 88 (larger blocks carry
 // enough work per tile for the tensor-memory GEMM; here each warp re-reads
-// the A and B rows its neighbours share).  MMA_GB300_BATCHED (mma or tc)
-// overrides the size rule, for tuning.
+// the A and B rows its neighbours share).  INT8 blocks go through BF16
+// copies on the tensor-memory side, so the integer kernel keeps them up to
+// kMaxBlockMacsI8: 16^3 59 against 1, 32^3 86 against 6, 64^3 73 against
+// 20, 128^3 56 against 49.  MMA_GB300_BATCHED (mma or tc) overrides the
+// size rule, for tuning.
 constexpr int64_t kMaxBlockMacs = int64_t(96) * 96 * 64;
+constexpr int64_t kMaxBlockMacsI8 = int64_t(128) * 128 * 128;
 
 bool batched_mma_fits(int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int64_t ldc, int64_t ldd, bool has_c) {
+                      int64_t ldb, int64_t ldc, int64_t ldd, bool has_c,
+                      bool i8) {
   static const int forced = [] {
     const char* e = getenv("MMA_GB300_BATCHED");
     if (!e) return 0;
@@ -258,7 +380,16 @@ bool batched_mma_fits(int64_t M, int64_t N, int64_t K, int64_t lda,
                         (!has_c || ldc == N) && M < (int64_t(1) << 24) &&
                         N < (int64_t(1) << 24) && K < (int64_t(1) << 24);
   if (!shape_ok || forced < 0) return false;
-  return forced > 0 || M * N * K <= kMaxBlockMacs;
+  return forced > 0 || M * N * K <= (i8 ? kMaxBlockMacsI8 : kMaxBlockMacs);
+}
+
+mma_status_t launch_batched_i8_mma(const Ctx& ctx, int64_t M, int64_t N,
+                                   int64_t K, const void* A, const void* B,
+                                   const void* C, void* D, int64_t batch,
+                                   int group, int abid, int blgp) {
+  if (M % 32 == 0 && N % 32 == 0)
+    return run_i8<2, 4>(ctx, M, N, K, A, B, C, D, batch, group, abid, blgp);
+  return run_i8<1, 2>(ctx, M, N, K, A, B, C, D, batch, group, abid, blgp);
 }
 
 mma_status_t launch_batched_mma(const Ctx& ctx, bool bf16, bool out16,

@@ -72,11 +72,17 @@ mma_status_t launch_gemm_i8_tc_batched(const Ctx& ctx, int64_t M, int64_t N,
 // Batched FP16/BF16 blocks streamed from HBM by warp-level MMAs (small and
 // mid-size blocks; see batched_mma_fits), FP32 or 16-bit C and D.
 bool batched_mma_fits(int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int64_t ldc, int64_t ldd, bool has_c);
+                      int64_t ldb, int64_t ldc, int64_t ldd, bool has_c,
+                      bool i8);
 mma_status_t launch_batched_mma(const Ctx& ctx, bool bf16, bool out16,
                                 int64_t M, int64_t N, int64_t K, const void* A,
                                 const void* B, const void* C, void* D,
                                 int64_t batch, int group, int abid, int blgp);
+// The same for INT8 -> INT32 (exact), with integer warp-level MMAs.
+mma_status_t launch_batched_i8_mma(const Ctx& ctx, int64_t M, int64_t N,
+                                   int64_t K, const void* A, const void* B,
+                                   const void* C, void* D, int64_t batch,
+                                   int group, int abid, int blgp);
 
 // Batched FP64 (DMMA), same tile conventions.
 mma_status_t launch_gemm_f64_batched(const Ctx& ctx, int64_t M, int64_t N,

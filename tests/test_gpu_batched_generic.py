@@ -229,3 +229,35 @@ def test_streaming_kernel_16bit_and_no_c(dtype_in, M, N, K):
                               group=4, abid=0, blgp=7)
     check(dtype_in, run(bf, use_c=False), want(bf, use_c=False), absab(bf),
           f"{dtype_in} {M}x{N}x{K} no C")
+
+
+# INT8 blocks up to 128^3 multiply-adds take the integer streaming kernel
+I8_STREAM_SHAPES = [(16, 16, 16), (32, 32, 32), (64, 64, 64), (16, 48, 80),
+                    (96, 64, 96), (32, 96, 48), (128, 128, 128)]
+
+
+@pytest.mark.parametrize("M,N,K", I8_STREAM_SHAPES)
+@pytest.mark.parametrize("G,abid,blgp", [(1, 0, 0), (4, 1, 3), (16, 5, 6)])
+def test_streaming_kernel_int8_exact(M, N, K, G, abid, blgp):
+    """Small and mid-size INT8 blocks on the integer warp-level kernel (K a
+    multiple of 16: the last 32-deep step of K = 16, 48, 80 is half empty
+    and reads as zero), bit-exact."""
+    bi = synth.batched_inputs(f"bs_i8_{M}_{N}_{K}", "i8", 64, M=M, N=N, K=K,
+                              group=G, abid=abid, blgp=blgp)
+    check("i8", run(bi), want(bi), None, f"i8 {M}x{N}x{K} G={G} blgp={blgp}")
+    check("i8", run(bi, use_c=False), want(bi, use_c=False), None,
+          f"i8 {M}x{N}x{K} no C")
+
+
+def test_streaming_kernel_int8_wraps_like_int32():
+    """Every product 127 * 127 with C at the top of INT32: D wraps modulo
+    2^32 exactly as an INT32 accumulator does (closed form)."""
+    import torch
+    batch, M, N, K = 8, 32, 32, 64
+    A = np.full((batch, M, K), 127, np.int8)
+    B = np.full((batch, N, K), 127, np.int8)
+    C = np.full((batch, M, N), 2 ** 31 - 100, np.int32)
+    D = binding.gemm_batched(to_dev(A), to_dev(B), to_dev(C), group=2, abid=1)
+    torch.cuda.synchronize()
+    exact = 2 ** 31 - 100 + K * 127 * 127
+    assert np.all(D.cpu().numpy() == np.int32(exact - 2 ** 32))
