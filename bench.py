@@ -59,17 +59,19 @@ BF16_FLOP_PER_SM_CLK = 8192.0
 # source makes the figure stale, and it is then reported as null).
 NCU_TRAFFIC: dict = {
     # ncu --set full, one launch after the warm-up launches (profiles/*.md)
-    "gemm_i8_4096": {"sha": "d4f2c4571a8cf9cb", "bytes": 188936192 + 44193536},
-    "gemm_u8_4096_clamp": {"sha": "d4f2c4571a8cf9cb", "bytes": 189157888 + 43582976},
-    "gemm_bf16_8192": {"sha": "d4f2c4571a8cf9cb", "bytes": 1577342000 + 259705088},
-    "gemm_bf16_skinny_16384x128x4096": {"sha": "d4f2c4571a8cf9cb",
-                                        "bytes": 143704832 + 3561472},
+    "gemm_i8_4096": {"sha": "139849220def4c09", "bytes": 184691456 + 43476480},
+    "gemm_u8_4096_clamp": {"sha": "139849220def4c09", "bytes": 184855040 + 43655168},
+    "gemm_bf16_8192": {"sha": "139849220def4c09", "bytes": 1576947000 + 259965184},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "139849220def4c09",
+                                        "bytes": 143715584 + 3787264},
     "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "795afc87d77db152",
                                                "bytes": 436228352 + 225458688},
-    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "d4f2c4571a8cf9cb",
-                                                "bytes": 876352512 + 496451072},
-    "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "ead9532501d7686b",
-                                              "bytes": 436271616 + 215038976},
+    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "139849220def4c09",
+                                                "bytes": 877809664 + 496396800},
+    "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
+                                              "bytes": 436278272 + 215408384},
+    "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
+                                            "bytes": 352372736 + 211523072},
 }
 
 
@@ -220,9 +222,10 @@ def workload_meta(name):
         nbytes = (w["M"] * w["K"] + w["N"] * w["K"]) * isz + 2 * w["M"] * w["N"] * osz
     else:
         ops = 2.0 * w["batch"] * w["M"] * w["N"] * w["K"]
-        tile_in = w["M"] * w["K"] * 2
+        isz = {"f16": 2, "bf16": 2, "i8": 1}[w["dtype_in"]]
+        tile_in = w["M"] * w["K"] * isz
         nbytes = (w["batch"] // w["group"]) * tile_in + w["batch"] * (
-            w["N"] * w["K"] * 2 + 2 * w["M"] * w["N"] * 4)
+            w["N"] * w["K"] * isz + 2 * w["M"] * w["N"] * 4)
     w["ops"] = ops
     w["algorithmic_bytes"] = nbytes
     w["unit"] = "TOP/s" if w["dtype_in"] == "i8" else "TFLOP/s"

@@ -169,29 +169,36 @@ def test_k_zero_and_empty():
 
 
 @pytest.mark.parametrize("name", ["batched_bf16_128x128x128_b8192_g4_abid1",
-                                  "batched_bf16_32x32x32_b65536_g4_abid1"])
+                                  "batched_bf16_32x32x32_b65536_g4_abid1",
+                                  "batched_i8_32x32x32_b65536_g4_abid1"])
 def test_full_size_generic_batched_workload(name):
-    """The batched workloads of 128^3 blocks (tensor-memory GEMM) and 32^3
-    blocks (warp-level streaming kernel), groups of 4 (source 1): sampled
-    entries (and the last) against the oracle on those entries' tiles;
-    every output finite."""
+    """The batched workloads of 128^3 BF16 blocks (tensor-memory GEMM), 32^3
+    BF16 blocks (warp-level streaming kernel) and 32^3 INT8 blocks (integer
+    streaming kernel), groups of 4 (source 1): sampled entries (and the
+    last) against the oracle on those entries' tiles; BF16 outputs finite,
+    INT8 bit-exact."""
     import torch
     w = synth.WORKLOADS[name]
-    bi = synth.batched_inputs(name, "bf16", w["batch"], M=w["M"], N=w["N"],
+    dt = w["dtype_in"]
+    bi = synth.batched_inputs(name, dt, w["batch"], M=w["M"], N=w["N"],
                               K=w["K"], group=w["group"], abid=w["abid"],
-                              dist=w["dist"])
-    D = binding.gemm_batched(to_dev(bi.A, "bf16"), to_dev(bi.B, "bf16"),
+                              dist=w.get("dist", "uniform"))
+    D = binding.gemm_batched(to_dev(bi.A, dt), to_dev(bi.B, dt),
                              to_dev(bi.C), group=bi.group, abid=bi.abid)
     torch.cuda.synchronize()
-    assert bool(torch.isfinite(D).all())
+    if dt != "i8":
+        assert bool(torch.isfinite(D).all())
     rng = np.random.default_rng(99)
     ents = np.unique(np.append(rng.choice(bi.batch, 63, replace=False), bi.batch - 1))
     src = (ents // bi.group) * bi.group + bi.abid
     A, B, C = (np.ascontiguousarray(x) for x in (bi.A[src], bi.B[ents], bi.C[ents]))
-    want = oracle.gemm_batched("bf16", A, B, C)
-    ab = oracle.gemm_batched("bf16", A & 0x7FFF, B & 0x7FFF, None).astype(np.float64)
+    want = oracle.gemm_batched(dt, A, B, C)
     got = D[torch.from_numpy(ents).cuda()].cpu().numpy()
-    check("bf16", got, want, ab, name)
+    if dt == "i8":
+        check("i8", got, want, None, name)
+        return
+    ab = oracle.gemm_batched(dt, A & 0x7FFF, B & 0x7FFF, None).astype(np.float64)
+    check(dt, got, want, ab, name)
 
 
 # Dense blocks with M, N, K multiples of 16 and at most 96 * 96 * 64
