@@ -693,6 +693,10 @@ def main(argv=None):
                                "pct_of_bf16_peak": r["pct_of_bf16_peak"],
                                "l2": r["l2"],
                                "roofline": r["roofline"]}
+            if dist.rank == 0 and dist.world == 1:
+                # the oracle beside each row, on a short bounded sample
+                per_dtype[name]["cpu_baseline"] = cpu_baseline(name, target_s=2.0)
+                _INPUT_CACHE.pop(name, None)
     add_nominal(res["roofline"], sms, clk)
 
     cpu = None
