@@ -255,7 +255,17 @@ def kernel_source(w):
     if w["kind"] == "batched":
         if (w["M"], w["N"], w["K"]) == (16, 16, 16):
             return "mixed_precision_dense_02_gb300/csrc/batched16.cu"
-        if w["M"] * w["N"] * w["K"] <= 96 * 96 * 64:
+        macs = w["M"] * w["N"] * w["K"]
+        if w["dtype_in"] == "i8":
+            if macs <= 128 ** 3 and w["M"] % 16 == 0 and w["N"] % 16 == 0 \
+                    and w["K"] % 16 == 0:
+                return "mixed_precision_dense_02_gb300/csrc/batched_mma.cu"
+            return "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu"
+        if w["dtype_in"] == "f64":
+            return "mixed_precision_dense_02_gb300/csrc/gemm_f64.cu"
+        if all(w[d] % 64 == 0 for d in "MNK") and macs <= 1 << 20:
+            return "mixed_precision_dense_02_gb300/csrc/batched_tile.cu"
+        if macs <= 96 * 96 * 64 and all(w[d] % 16 == 0 for d in "MNK"):
             return "mixed_precision_dense_02_gb300/csrc/batched_mma.cu"
         return "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu"
     if w["dtype_in"] == "i8" and not i8_on_tensor_pipe(w):

@@ -401,6 +401,10 @@ extern "C" mma_status_t mma_gemm_batched_ex(
         return launch_batched16(ctx, bf16, batch, G, abid, blgp, A, B,
                                 static_cast<const float*>(C),
                                 static_cast<float*>(D));
+      // mid-size dense blocks in multiples of 64: CTA-cooperative tiles
+      if (batched_tile_fits(M, N, K, lda, ldb, ldc, ldd, C != nullptr))
+        return launch_batched_tile(ctx, bf16, out16, M, N, K, A, B, C, D,
+                                   batch, G, abid, blgp);
       // small and mid-size dense blocks: warp-level MMAs streaming from HBM
       if (batched_mma_fits(M, N, K, lda, ldb, ldc, ldd, C != nullptr, false))
         return launch_batched_mma(ctx, bf16, out16, M, N, K, A, B, C, D, batch,

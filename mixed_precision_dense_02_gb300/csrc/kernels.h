@@ -78,6 +78,16 @@ mma_status_t launch_batched_mma(const Ctx& ctx, bool bf16, bool out16,
                                 int64_t M, int64_t N, int64_t K, const void* A,
                                 const void* B, const void* C, void* D,
                                 int64_t batch, int group, int abid, int blgp);
+// Batched FP16/BF16 blocks with M, N, K multiples of 64 (see
+// batched_tile_fits): CTAs of four warps, operands staged once per CTA tile
+// through a cp.async ring.
+bool batched_tile_fits(int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldc, int64_t ldd, bool has_c);
+mma_status_t launch_batched_tile(const Ctx& ctx, bool bf16, bool out16,
+                                 int64_t M, int64_t N, int64_t K,
+                                 const void* A, const void* B, const void* C,
+                                 void* D, int64_t batch, int group, int abid,
+                                 int blgp);
 // The same for INT8 -> INT32 (exact), with integer warp-level MMAs.
 mma_status_t launch_batched_i8_mma(const Ctx& ctx, int64_t M, int64_t N,
                                    int64_t K, const void* A, const void* B,

@@ -266,6 +266,11 @@ WORKLOADS = {
     "batched_i8_32x32x32_b65536_g4_abid1": dict(
         kind="batched", dtype_in="i8", batch=65536, M=32, N=32, K=32,
         group=4, abid=1),
+    # batched 64 x 64 x 64 blocks (the CTA-cooperative tile kernel), groups
+    # of 4 with source 1
+    "batched_bf16_64x64x64_b16384_g4_abid1": dict(
+        kind="batched", dtype_in="bf16", batch=16384, M=64, N=64, K=64,
+        group=4, abid=1, dist="uniform"),
     # batched 128 x 128 x 128 tiles (larger blocks than the 16^3 form) with
     # the A block of each group of 4 broadcast from entry 1 of the group
     "batched_bf16_128x128x128_b8192_g4_abid1": dict(

@@ -169,12 +169,14 @@ def test_k_zero_and_empty():
 
 
 @pytest.mark.parametrize("name", ["batched_bf16_128x128x128_b8192_g4_abid1",
+                                  "batched_bf16_64x64x64_b16384_g4_abid1",
                                   "batched_bf16_32x32x32_b65536_g4_abid1",
                                   "batched_i8_32x32x32_b65536_g4_abid1"])
 def test_full_size_generic_batched_workload(name):
-    """The batched workloads of 128^3 BF16 blocks (tensor-memory GEMM), 32^3
-    BF16 blocks (warp-level streaming kernel) and 32^3 INT8 blocks (integer
-    streaming kernel), groups of 4 (source 1): sampled entries (and the
+    """The batched workloads of 128^3 BF16 blocks (tensor-memory GEMM), 64^3
+    BF16 blocks (CTA-cooperative tile kernel), 32^3 BF16 blocks (warp-level
+    streaming kernel) and 32^3 INT8 blocks (integer streaming kernel),
+    groups of 4 (source 1): sampled entries (and the
     last) against the oracle on those entries' tiles; BF16 outputs finite,
     INT8 bit-exact."""
     import torch
@@ -268,3 +270,83 @@ def test_streaming_kernel_int8_wraps_like_int32():
     torch.cuda.synchronize()
     exact = 2 ** 31 - 100 + K * 127 * 127
     assert np.all(D.cpu().numpy() == np.int32(exact - 2 ** 32))
+
+
+# FP16/BF16 blocks with M, N, K multiples of 64 and at most 2^20
+# multiply-adds take the CTA-cooperative kernel (64 x 64 CTA tiles, operands
+# staged once per tile through a cp.async ring crossing tile boundaries)
+TILE_SHAPES = [(64, 64, 64), (128, 64, 128), (64, 128, 64), (128, 128, 64),
+               (64, 64, 256), (64, 192, 64)]
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", TILE_SHAPES)
+@pytest.mark.parametrize("G,abid,blgp", [(1, 0, 0), (4, 3, 3), (16, 9, 4)])
+def test_cooperative_tile_kernel(dtype_in, M, N, K, G, abid, blgp):
+    bi = synth.batched_inputs(f"bt_{M}_{N}_{K}", dtype_in, 48, M=M, N=N, K=K,
+                              group=G, abid=abid, blgp=blgp)
+    check(dtype_in, run(bi), want(bi), absab(bi),
+          f"{dtype_in} {M}x{N}x{K} G={G} blgp={blgp}")
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("K", [64, 128])   # C staged in shared memory / read directly
+def test_cooperative_tile_kernel_16bit_and_no_c(dtype_in, K):
+    M, N = 64, 128
+    bi = synth.batched_inputs(f"bt_h{K}", dtype_in, 32, M=M, N=N, K=K, group=2,
+                              abid=1, blgp=1, acc16=True)
+    got = run(bi, acc="same")
+    for b in range(bi.batch):
+        sa = (b // 2) * 2 + 1
+        sb = (b // 4) * 4 + oracle.blgp_source(1, b % 4)
+        w, ab = oracle.gemm_acc16(dtype_in, bi.A[sa], bi.B[sb], bi.C[b],
+                                  want_absab=True)
+        check16(dtype_in, got[b], w, ab, f"{dtype_in}->16 tile entry {b}")
+    bf = synth.batched_inputs(f"bt_n{K}", dtype_in, 40, M=M, N=N, K=K, group=4,
+                              abid=0, blgp=5)
+    check(dtype_in, run(bf, use_c=False), want(bf, use_c=False), absab(bf),
+          f"{dtype_in} tile kernel no C")
+
+
+_FORCED_TILE_SCRIPT = """
+import sys, numpy as np, torch
+sys.path[:0] = [sys.argv[1], sys.argv[1] + '/tests']
+from mixed_precision_dense_02_gb300 import binding, synth
+from helpers import to_dev
+binding.load()
+out = {}
+for (M, N, K, dt) in [(128, 128, 128, 'bf16'), (256, 256, 64, 'f16'),
+                      (128, 128, 256, 'bf16')]:
+    bi = synth.batched_inputs(f'btf_{M}_{N}_{K}', dt, 24, M=M, N=N, K=K,
+                              group=4, abid=2, blgp=6)
+    D = binding.gemm_batched(to_dev(bi.A, dt), to_dev(bi.B, dt), to_dev(bi.C),
+                             group=4, abid=2, blgp=6)
+    torch.cuda.synchronize()
+    out[f'{M}_{N}_{K}_{dt}'] = D.cpu().numpy()
+binding.device_status()
+np.savez(sys.argv[2], **out)
+"""
+
+
+def test_cooperative_tile_kernel_forced_on_larger_blocks(tmp_path):
+    """MMA_GB300_BATCHED=tile sends blocks above the routing threshold (128^3,
+    256 x 256 x 64, 128 x 128 x 256) to the CTA-cooperative kernel; run in a
+    child process (the override is read once per process) and compared
+    with the oracle here."""
+    import os
+    import pathlib
+    import subprocess
+    import sys
+    root = str(pathlib.Path(__file__).resolve().parents[1])
+    out = tmp_path / "forced_tile.npz"
+    env = dict(os.environ, MMA_GB300_BATCHED="tile")
+    r = subprocess.run([sys.executable, "-c", _FORCED_TILE_SCRIPT, root, str(out)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    got = np.load(out)
+    for (M, N, K, dt) in [(128, 128, 128, "bf16"), (256, 256, 64, "f16"),
+                          (128, 128, 256, "bf16")]:
+        bi = synth.batched_inputs(f"btf_{M}_{N}_{K}", dt, 24, M=M, N=N, K=K,
+                                  group=4, abid=2, blgp=6)
+        check(dt, got[f"{M}_{N}_{K}_{dt}"], want(bi), absab(bi),
+              f"forced tile {dt} {M}x{N}x{K}")
