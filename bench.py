@@ -68,6 +68,8 @@ NCU_TRAFFIC: dict = {
                                                "bytes": 436228352 + 225458688},
     "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "139849220def4c09",
                                                 "bytes": 877809664 + 496396800},
+    "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "5d7d33c8c58a2c04",
+                                              "bytes": 436264192 + 226831104},
     "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
                                               "bytes": 436278272 + 215408384},
     "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
