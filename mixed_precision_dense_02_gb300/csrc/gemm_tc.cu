@@ -800,6 +800,12 @@ __global__ void __launch_bounds__(kConvThreads)
   const int64_t cpr = (K + 15) / 16;  // chunks per row
   const int64_t total = int64_t(M + N) * cpr;
   constexpr int64_t kSpan = int64_t(kConvThreads) * kConvUnroll;
+  // the 8-bit inputs are read once (evict first); the widened operands
+  // are read back by the GEMM right after this pass (evict last), which
+  // then finds most of them in L2
+  uint64_t pol_first, pol_last;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_first));
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_last));
   for (int64_t base = int64_t(blockIdx.x) * kSpan; base < total;
        base += int64_t(gridDim.x) * kSpan) {
     int4 v[kConvUnroll];
@@ -812,7 +818,9 @@ __global__ void __launch_bounds__(kConvThreads)
         const int c = int(i - r * cpr) * 16;
         if (c + 16 <= K) {
           const int8_t* src = r < M ? A + r * lda + c : B + (r - M) * ldb + c;
-          v[u] = __ldcs(reinterpret_cast<const int4*>(src));
+          asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.s32 {%0, %1, %2, %3}, [%4], %5;"
+                       : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                       : "l"(src), "l"(pol_first));
         }
       }
     }
@@ -828,8 +836,10 @@ __global__ void __launch_bounds__(kConvThreads)
         flip4(v[u], kFlipSigned, w);
         uint4 o0, o1;
         u8x16_to_bf16(w, o0, o1);
-        reinterpret_cast<uint4*>(dst)[0] = o0;
-        reinterpret_cast<uint4*>(dst)[1] = o1;
+        asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+                     :: "l"(dst), "r"(o0.x), "r"(o0.y), "r"(o0.z), "r"(o0.w), "l"(pol_last) : "memory");
+        asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+                     :: "l"(dst + 8), "r"(o1.x), "r"(o1.y), "r"(o1.z), "r"(o1.w), "l"(pol_last) : "memory");
       } else {
         const int8_t* src = r < M ? A + r * lda + c : B + (r - M) * ldb + c;
         for (int j = 0; c + j < K; ++j)
