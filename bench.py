@@ -58,16 +58,18 @@ BF16_FLOP_PER_SM_CLK = 8192.0
 # by the SHA-256 of the kernel's source file at capture time (a changed
 # source makes the figure stale, and it is then reported as null).
 NCU_TRAFFIC: dict = {
-    # ncu --set full, one launch after the warm-up launches (profiles/*.md)
-    "gemm_i8_4096": {"sha": "139849220def4c09", "bytes": 184691456 + 43476480},
-    "gemm_u8_4096_clamp": {"sha": "139849220def4c09", "bytes": 184855040 + 43655168},
-    "gemm_bf16_8192": {"sha": "139849220def4c09", "bytes": 1576947000 + 259965184},
-    "gemm_bf16_skinny_16384x128x4096": {"sha": "139849220def4c09",
-                                        "bytes": 143715584 + 3787264},
+    # one ncu capture per workload (dram__bytes_read.sum and
+    # dram__bytes_write.sum of one launch after the warm-up launches;
+    # profiles/*.md)
+    "gemm_i8_4096": {"sha": "2841693fa147362f", "bytes": 188872704 + 43678976},
+    "gemm_u8_4096_clamp": {"sha": "2841693fa147362f", "bytes": 189120768 + 43365120},
+    "gemm_bf16_8192": {"sha": "2841693fa147362f", "bytes": 1631446000 + 258660096},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "2841693fa147362f",
+                                        "bytes": 143702528 + 3225856},
     "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "795afc87d77db152",
                                                "bytes": 436228352 + 225458688},
-    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "139849220def4c09",
-                                                "bytes": 877809664 + 496396800},
+    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "2841693fa147362f",
+                                                "bytes": 876100608 + 495900672},
     "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "5d7d33c8c58a2c04",
                                               "bytes": 436264192 + 226831104},
     "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
@@ -75,8 +77,8 @@ NCU_TRAFFIC: dict = {
     "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
                                             "bytes": 352372736 + 211523072},
     "gemm_f64_4096_rowB": {"sha": "a6bd67c690b12ddb", "bytes": 3657537000 + 130594048},
-    "gemm_bf16_acc16_8192": {"sha": "139849220def4c09", "bytes": 1406566000 + 129594112},
-    "gemm_f16_256": {"sha": "139849220def4c09", "bytes": 570624 + 0},
+    "gemm_bf16_acc16_8192": {"sha": "2841693fa147362f", "bytes": 1493787000 + 129100288},
+    "gemm_f16_256": {"sha": "2841693fa147362f", "bytes": 570624 + 0},
 }
 
 

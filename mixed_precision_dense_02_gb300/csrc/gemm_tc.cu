@@ -1150,19 +1150,35 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
                       BatchArgs bat = BatchArgs{1, 1, 0, 0}) {
   constexpr int kpc = kI8ChunkK / BK;
   // Shared memory: operand ring (a pair stages half of B per CTA) plus the
-  // epilogue's staging ring of 4 blocks per warp (2 for single-CTA wide
-  // tiles, whose 48 KB stages leave room for only 4 of them).
+  // epilogue's staging ring.  Wide pair tiles: the MMA issuer spends most
+  // of its time waiting for operand stages to land, so FP32 and 16-bit
+  // results take six stages and 2 staging blocks per warp (their epilogue
+  // drains one accumulator per tile, with a whole tile of MMA work to hide
+  // it); the exact integer modes drain a 1024-deep chunk at a time and emit
+  // C + sums within one chunk's MMA time, which needs 4 staging blocks per
+  // warp (2 C loads ahead), so they keep five stages.  Single-CTA wide
+  // tiles (48 KB stages) take four stages and 2 staging blocks.
   if constexpr (EPI != Epi::I32SAT) {
     // 224-wide pair tiles (FP32 and exact-INT32 results: 112 columns per
     // epilogue warp, seven 16-column blocks)
     if constexpr (EPI == Epi::F32 || EPI == Epi::I32EXACT ||
                   EPI == Epi::I32SATW) {
-      if (bn == 224 && cl == 2)
-        return run<224, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+      if (bn == 224 && cl == 2) {
+        if constexpr (EPI == Epi::F32)
+          return run<224, 6, BF16, EPI, 2, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+        else
+          return run<224, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+      }
     }
-    if (bn >= 224)
-      return cl == 2 ? run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
-                     : run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+    if (bn >= 224) {
+      if (cl == 2) {
+        if constexpr (!int_mode(EPI))
+          return run<256, 6, BF16, EPI, 2, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+        else
+          return run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+      }
+      return run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+    }
   }
   // Single CTAs on 128-wide tiles with at most four K steps per tile (small
   // or batched small-block problems): the C stream is as large as the
