@@ -501,6 +501,9 @@ def measure_workload(torch, dist, name, steps, warmup, with_e2e, sustain_s=0.0):
                      "unit": unit, "frac": achieved / peak, "traffic": traffic,
                      "peak_source": note, "kernel_launches_timed": len(launch_ms),
                      "kernel_ms_mean": mean_ms,
+                     "kernel_ms_median": (statistics.median(launch_ms)
+                                          if launch_ms else None),
+                     "kernel_ms_best": min(launch_ms) if launch_ms else None,
                      "algorithmic_bytes_per_launch": w["algorithmic_bytes"],
                      "ops_per_launch": w["ops"]},
         "pct_of_bf16_peak": None, "host_window": (t0, t1),

@@ -56,9 +56,9 @@ def check(dtype_in: str, got: np.ndarray, want: np.ndarray,
     if dtype_in == "i8":
         if not np.array_equal(got, want):
             bad = np.argwhere(got != want)
-            i, j = bad[0]
+            idx = tuple(int(v) for v in bad[0])
             raise AssertionError(f"{what}: {len(bad)} INT32 mismatches, first "
-                                 f"at {(i, j)}: {got[i, j]} vs {want[i, j]}")
+                                 f"at {idx}: {got[idx]} vs {want[idx]}")
         return
     rel, ab0 = TOL[dtype_in]
     g = got.astype(np.float64)

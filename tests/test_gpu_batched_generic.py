@@ -350,3 +350,31 @@ def test_cooperative_tile_kernel_forced_on_larger_blocks(tmp_path):
                                   group=4, abid=2, blgp=6)
         check(dt, got[f"{M}_{N}_{K}_{dt}"], want(bi), absab(bi),
               f"forced tile {dt} {M}x{N}x{K}")
+
+
+# C and D the same buffer (in place): every batched kernel reads an
+# output's addend before it writes that output
+INPLACE_CASES = [
+    ("bf16", 16, 16, 16, 64),     # 16^3 streaming kernel
+    ("bf16", 32, 32, 32, 64),     # warp-level streaming kernel
+    ("f16", 64, 64, 64, 32),      # CTA-cooperative tile kernel, C staged
+    ("bf16", 64, 128, 128, 32),   # CTA-cooperative tile kernel, C direct
+    ("bf16", 128, 128, 128, 16),  # tensor-memory GEMM
+    ("i8", 32, 32, 32, 64),       # integer streaming kernel
+    ("i8", 160, 96, 64, 8),       # INT8 on the tensor-memory GEMM
+    ("f64", 24, 40, 16, 8),       # FP64 DMMA tiles
+]
+
+
+@pytest.mark.parametrize("dtype_in,M,N,K,batch", INPLACE_CASES)
+def test_batched_in_place(dtype_in, M, N, K, batch):
+    import torch
+    bi = synth.batched_inputs(f"bip_{M}_{N}_{K}", dtype_in, batch, M=M, N=N,
+                              K=K, group=4, abid=3, blgp=2)
+    C = to_dev(bi.C)
+    D = binding.gemm_batched(to_dev(bi.A, dtype_in), to_dev(bi.B, dtype_in), C,
+                             C, group=4, abid=3, blgp=2)
+    torch.cuda.synchronize()
+    assert D.data_ptr() == C.data_ptr()
+    check(dtype_in, C.cpu().numpy(), want(bi), absab(bi) if dtype_in != "i8" else None,
+          f"{dtype_in} {M}x{N}x{K} in place")
