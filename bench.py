@@ -61,15 +61,15 @@ NCU_TRAFFIC: dict = {
     # one ncu capture per workload (dram__bytes_read.sum and
     # dram__bytes_write.sum of one launch after the warm-up launches;
     # profiles/*.md)
-    "gemm_i8_4096": {"sha": "2841693fa147362f", "bytes": 188872704 + 43678976},
-    "gemm_u8_4096_clamp": {"sha": "2841693fa147362f", "bytes": 189120768 + 43365120},
-    "gemm_bf16_8192": {"sha": "2841693fa147362f", "bytes": 1631446000 + 258660096},
-    "gemm_bf16_skinny_16384x128x4096": {"sha": "2841693fa147362f",
-                                        "bytes": 143702528 + 3225856},
+    "gemm_i8_4096": {"sha": "1fa40d449dccf124", "bytes": 179292416 + 42687488},
+    "gemm_u8_4096_clamp": {"sha": "1fa40d449dccf124", "bytes": 184625664 + 43099648},
+    "gemm_bf16_8192": {"sha": "1fa40d449dccf124", "bytes": 1628860000 + 258911744},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "1fa40d449dccf124",
+                                        "bytes": 143704320 + 3153408},
     "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "795afc87d77db152",
                                                "bytes": 436228352 + 225458688},
-    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "2841693fa147362f",
-                                                "bytes": 876100608 + 495900672},
+    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "1fa40d449dccf124",
+                                                "bytes": 877373184 + 496142336},
     "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "5d7d33c8c58a2c04",
                                               "bytes": 436264192 + 226831104},
     "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
@@ -77,8 +77,8 @@ NCU_TRAFFIC: dict = {
     "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
                                             "bytes": 352372736 + 211523072},
     "gemm_f64_4096_rowB": {"sha": "a6bd67c690b12ddb", "bytes": 3657537000 + 130594048},
-    "gemm_bf16_acc16_8192": {"sha": "2841693fa147362f", "bytes": 1493787000 + 129100288},
-    "gemm_f16_256": {"sha": "2841693fa147362f", "bytes": 570624 + 0},
+    "gemm_bf16_acc16_8192": {"sha": "1fa40d449dccf124", "bytes": 1485834000 + 129398528},
+    "gemm_f16_256": {"sha": "1fa40d449dccf124", "bytes": 570624 + 0},
 }
 
 

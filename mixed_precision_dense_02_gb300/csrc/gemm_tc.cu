@@ -442,6 +442,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // PF0 blocks is requested at once (a CTA with a single tile then has
     // all of its C in flight while its main loop runs).
     constexpr int PF0 = NSTG < NBLK ? NSTG : NBLK;
+    // Exact INT8 (sums modulo 2^32, so C may join them in any order): the
+    // C blocks are added to the INT32 register sums while the unit's
+    // chunks run, two blocks per chunk through staging slots 0 and 1 (one
+    // step: both requested, then both consumed after the next chunk's
+    // drain), and the emission only stores D.  Its C latency hides behind
+    // MMA work, and two staging blocks per warp suffice.
+    // (Instances with two staging blocks per warp; with one or two chunks
+    // per tile the host picks the four-block ring, whose C loads run ahead
+    // in the emission instead.)
+    constexpr bool kEarlyC = EPI == Epi::I32EXACT && NSTG == 2;
+    static_assert(!kEarlyC || NSTG >= 2, "early C uses staging slots 0 and 1");
+    constexpr int NMP = (NBLK + 1) / 2;  // early-C steps per unit
+    uint32_t cpar = 0;                   // phase parity of slots 0 and 1
     uint32_t g = 0;  // blocks emitted so far by this warp
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -559,9 +572,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&wbar[b]);  // wholly outside C and D: nothing to load
       }
     };
-    if (has_c && lane == 0 && first_unit < units)
+    if (!kEarlyC && has_c && lane == 0 && first_unit < units)
       for (int jj = 0; jj < PF0; ++jj) request_c(uint32_t(jj), first_unit, jj);
     __syncwarp();
+    // Early C, step m of the unit at (row0, colh, z): (lane 0) request
+    // blocks 2m and 2m + 1 into slots 0 and 1, once every store that read
+    // them has finished; a block outside C (or beyond the unit) only
+    // arrives, so both slots advance one phase per step.
+    [[maybe_unused]] auto early_c_issue = [&](int m, int row0, int colh, int z) {
+      if (lane == 0) {
+        bulk_wait_group_read<0>();
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl) {
+          const int jj = 2 * m + sl;
+          if (jj < NBLK && row0 < M && colh + jj * COLS < N) {
+            mbar_arrive_expect_tx(&wbar[sl], kStgBytes);
+            tma_load_3d(&tmC, &wbar[sl], stg + sl * kStgBytes, colh + jj * COLS,
+                        row0, z);
+          } else {
+            mbar_arrive(&wbar[sl]);
+          }
+        }
+      }
+      __syncwarp();
+    };
     for (int u = first_unit; u < units && ok; u += unit_step) {
       int row0, colh, zc;
       unit_origin(u, row0, colh, zc);
@@ -584,6 +618,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < HALF; ++j) iacc[j] = 0u;
         }
+        // early C: steps issued and consumed in this unit
+        [[maybe_unused]] int mp_issued = 0, mp_done = 0;
+        // Wait for the oldest issued step's two blocks and add them to the
+        // sums (the step number selects registers through an unrolled
+        // match, so iacc stays in registers).
+        [[maybe_unused]] auto early_c_finish = [&]() -> bool {
+          bool okc = mbar_wait(&wbar[0], cpar, abort_flag, status) &&
+                     mbar_wait(&wbar[1], cpar, abort_flag, status);
+          if (!__all_sync(0xffffffffu, okc)) return false;
+#pragma unroll
+          for (int m = 0; m < NMP; ++m) {
+            if (m != mp_done) continue;
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) {
+              const int jj = 2 * m + sl;
+              if (jj >= NBLK) continue;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint4 w = *chunk(stg + sl * kStgBytes, c);
+                iacc[jj * 16 + 4 * c + 0] += w.x;
+                iacc[jj * 16 + 4 * c + 1] += w.y;
+                iacc[jj * 16 + 4 * c + 2] += w.z;
+                iacc[jj * 16 + 4 * c + 3] += w.w;
+              }
+            }
+          }
+          __syncwarp();  // every lane has read both slots
+          cpar ^= 1u;
+          ++mp_done;
+          return true;
+        };
+        if constexpr (kEarlyC) {
+          if (has_c) early_c_issue(mp_issued++, row0, colh, zc);
+        }
         for (int ch = 0; ch < chunks; ++ch) {
           ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
           if (!__all_sync(0xffffffffu, ok)) {
@@ -605,6 +673,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           release_acc(acc);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
+          if constexpr (kEarlyC) {
+            if (has_c && mp_done < mp_issued) {
+              if (!early_c_finish()) {
+                ok = false;
+                break;
+              }
+              if (mp_issued < NMP) early_c_issue(mp_issued++, row0, colh, zc);
+            }
+          }
           if constexpr (EPI == Epi::I32SAT) {
             // every kSatFlush chunks, and after the last one
             if ((ch + 1) % kSatFlush == 0 || ch + 1 == chunks) {
@@ -614,6 +691,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        if constexpr (kEarlyC) {
+          // fewer chunks than steps: the remaining C blocks now
+          while (has_c && ok && mp_done < NMP) {
+            if (mp_done == mp_issued) early_c_issue(mp_issued++, row0, colh, zc);
+            ok = early_c_finish();
+          }
+          if (!ok) break;
+        }
       } else {
         ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -625,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < NBLK; ++j, ++g) {
         uint8_t* buf = stg + (g % NSTG) * kStgBytes;
         if (lane == 0) {
-          if (has_c) {
+          if (has_c && !kEarlyC) {
             // the C of block g + PF, possibly in this warp's next unit
             int jj = j + PF, uu = u;
             if (jj >= NBLK) {
@@ -655,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // every TMEM read of this accumulator is done: release it
           if (j == NBLK - 1) release_acc(acc);
         }
-        if (has_c) {
+        if (has_c && !kEarlyC) {
           ok = mbar_wait(&wbar[g % NSTG], (g / NSTG) & 1u, abort_flag, status);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
@@ -665,7 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint4* p = chunk(buf, c);
-          const uint4 w = has_c ? *p : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w =
+              has_c && !kEarlyC ? *p : make_uint4(0u, 0u, 0u, 0u);
           uint4 o;
           if constexpr (EPI == Epi::H16) {
             const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
@@ -1151,11 +1237,13 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
   constexpr int kpc = kI8ChunkK / BK;
   // Shared memory: operand ring (a pair stages half of B per CTA) plus the
   // epilogue's staging ring.  Wide pair tiles: the MMA issuer spends most
-  // of its time waiting for operand stages to land, so FP32 and 16-bit
-  // results take six stages and 2 staging blocks per warp (their epilogue
-  // drains one accumulator per tile, with a whole tile of MMA work to hide
-  // it); the exact integer modes drain a 1024-deep chunk at a time and emit
-  // C + sums within one chunk's MMA time, which needs 4 staging blocks per
+  // of its time waiting for operand stages to land, so FP32, 16-bit and
+  // exact-INT32 results take six stages and 2 staging blocks per warp
+  // (FP32 and 16-bit drain one accumulator per tile, with a whole tile of
+  // MMA work to hide it; exact INT32 adds C to its register sums while the
+  // chunks run, from three 1024-deep chunks per tile up).  The saturating
+  // mode, and exact INT32 with one or two chunks, add C as each block is
+  // emitted, within one chunk's MMA time, which needs 4 staging blocks per
   // warp (2 C loads ahead), so they keep five stages.  Single-CTA wide
   // tiles (48 KB stages) take four stages and 2 staging blocks.
   if constexpr (EPI != Epi::I32SAT) {
@@ -1164,18 +1252,28 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
     if constexpr (EPI == Epi::F32 || EPI == Epi::I32EXACT ||
                   EPI == Epi::I32SATW) {
       if (bn == 224 && cl == 2) {
-        if constexpr (EPI == Epi::F32)
+        if constexpr (EPI == Epi::F32) {
           return run<224, 6, BF16, EPI, 2, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
-        else
+        } else if constexpr (EPI == Epi::I32EXACT) {
+          if (K > 2 * kI8ChunkK)
+            return run<224, 6, BF16, EPI, 2, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
           return run<224, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+        } else {
+          return run<224, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+        }
       }
     }
     if (bn >= 224) {
       if (cl == 2) {
-        if constexpr (!int_mode(EPI))
+        if constexpr (EPI == Epi::F32 || EPI == Epi::H16) {
           return run<256, 6, BF16, EPI, 2, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
-        else
+        } else if constexpr (EPI == Epi::I32EXACT) {
+          if (K > 2 * kI8ChunkK)
+            return run<256, 6, BF16, EPI, 2, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
           return run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+        } else {
+          return run<256, 5, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+        }
       }
       return run<256, 4, BF16, EPI, 1, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
     }
