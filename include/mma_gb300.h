@@ -187,10 +187,21 @@ mma_status_t mma_gemm_i8_ex(int64_t M, int64_t N, int64_t K, const void *A,
  * B, C and D are never broadcast here (see mma_gemm_batched_ex for B).
  * Pairs: the four of mma_gemm plus 16-bit accumulate; any M, N, K >= 0;
  * leading dimensions and alignment as for mma_gemm (each tile is one
- * mma_gemm problem).  16 x 16 x 16 FP16/BF16 -> FP32 tiles with all leading
- * dimensions 16 take an HBM-streaming kernel; other shapes run on the
- * tensor-core GEMM kernels (INT8: through BF16 copies of every tile in the
- * library's scratch buffer, grown like mma_gemm's).
+ * mma_gemm problem).  The kernel follows the block shape (dense tiles,
+ * leading dimensions equal to the tile's row length):
+ *   - 16 x 16 x 16 FP16/BF16 -> FP32: an HBM-streaming kernel;
+ *   - FP16/BF16 with M, N, K multiples of 64 and M*N*K <= 2^20: a
+ *     CTA-cooperative kernel (64 x 64 tiles, operands staged once in shared
+ *     memory);
+ *   - FP16/BF16 with M, N, K multiples of 16 and M*N*K <= 96*96*64, and
+ *     INT8 with M, N, K multiples of 16 and M*N*K <= 128^3: warp-level
+ *     streaming kernels;
+ *   - everything else: the tensor-memory GEMM over per-entry tensor maps
+ *     (INT8: through BF16 copies of every tile in the library's scratch
+ *     buffer, grown like mma_gemm's); FP64: DMMA tiles.
+ * The choice changes speed only: FP16/BF16 results agree within the
+ * accumulation tolerance (the routes sum in different orders), and INT8
+ * results are bit-identical across routes.
  * Constraints: a_broadcast_group in {1, 2, 4, 8, 16}; 0 <= a_broadcast_id
  * < a_broadcast_group; batch % a_broadcast_group == 0 (else
  * MMA_ERR_INVALID_ARG); batch < 2^31 (else MMA_ERR_UNSUPPORTED).

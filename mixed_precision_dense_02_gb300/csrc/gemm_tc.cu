@@ -9,22 +9,26 @@
 // K loop over staged panels, bounds-predicated store) is the one of
 // "RDNA3 dense WMMA builtins", section "Using WMMA builtins as a compute
 // policy", rebuilt for sm_103a:
-//   * persistent CTAs (one per SM), tiles visited in M-grouped order so the
+//   * persistent CTAs (one per SM, or CTA pairs sharing one 256-row MMA
+//     tile through cta_group::2), tiles visited in M-grouped order so the
 //     A and B panels in flight stay resident in L2;
-//   * warp 0 drives TMA: 128x64 A and BNx64 B boxes, 128-byte swizzled,
-//     into a STAGES-deep shared-memory ring guarded by mbarriers;
-//   * warp 1 issues tcgen05.mma (M=128, N=BN, K=16) from one thread into a
-//     double-buffered FP32 accumulator in tensor memory;
+//   * warp 0 drives TMA: 128x64 A and BNx64 B boxes (a pair's CTAs each
+//     load half of B), 128-byte swizzled, into a STAGES-deep shared-memory
+//     ring guarded by mbarriers;
+//   * warp 1 issues tcgen05.mma (M=128 or 256, N=BN, K=16) from one thread
+//     into a double-buffered FP32 accumulator in tensor memory;
 //   * warps 2..9 (two per tensor-memory lane quarter, one per column half)
-//     drain the accumulator with tcgen05.ld, add C and store D with 16-byte
-//     vector accesses, overlapping the next tile's MMAs.
+//     drain the accumulator with tcgen05.ld and emit 32-row x 16-column
+//     blocks through a small per-warp staging ring: C arrives by TMA load,
+//     D leaves by TMA store, overlapping the next tile's MMAs.
 // The same kernel carries the exact INT8 -> INT32 product on the BF16
 // tensor pipe (sm_103a has no integer kind of tcgen05.mma): int8 operands
 // are widened to BF16 (exact), K is split into chunks short enough that
 // every FP32 partial sum is an exactly representable integer, and the
-// epilogue sums the chunks in INT32 (see Epi::I32EXACT).
-// Ragged M/N/K edges: TMA zero-fills out-of-bounds box elements (so they
-// add nothing to the sum) and the epilogue predicates its stores.
+// epilogue sums the chunks in INT32 registers (see Epi::I32EXACT; C joins
+// those sums while the chunks run).
+// Ragged M/N/K edges: TMA zero-fills out-of-bounds load boxes (so they add
+// nothing to the sum) and clips stores to the tensor's extent.
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
