@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -55,30 +56,31 @@ NOMINAL_HBM_GBS = 7900.0
 BF16_FLOP_PER_SM_CLK = 8192.0
 
 # DRAM bytes per launch of each dominant kernel from one ncu capture, keyed
-# by the SHA-256 of the kernel's source file at capture time (a changed
-# source makes the figure stale, and it is then reported as null).
+# by the SHA-256 of the kernel source's code (comments and whitespace
+# removed, see source_sha) at capture time: changed code makes the figure
+# stale, and it is then reported as null.
 NCU_TRAFFIC: dict = {
     # one ncu capture per workload (dram__bytes_read.sum and
     # dram__bytes_write.sum of one launch after the warm-up launches;
     # profiles/*.md)
-    "gemm_i8_4096": {"sha": "1fa40d449dccf124", "bytes": 179292416 + 42687488},
-    "gemm_u8_4096_clamp": {"sha": "1fa40d449dccf124", "bytes": 184625664 + 43099648},
-    "gemm_bf16_8192": {"sha": "1fa40d449dccf124", "bytes": 1628860000 + 258911744},
-    "gemm_bf16_skinny_16384x128x4096": {"sha": "1fa40d449dccf124",
+    "gemm_i8_4096": {"sha": "a140329b581276a6", "bytes": 179292416 + 42687488},
+    "gemm_u8_4096_clamp": {"sha": "a140329b581276a6", "bytes": 184625664 + 43099648},
+    "gemm_bf16_8192": {"sha": "a140329b581276a6", "bytes": 1628860000 + 258911744},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "a140329b581276a6",
                                         "bytes": 143704320 + 3153408},
-    "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "795afc87d77db152",
+    "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "e9a765212730005e",
                                                "bytes": 436228352 + 225458688},
-    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "1fa40d449dccf124",
+    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "a140329b581276a6",
                                                 "bytes": 877373184 + 496142336},
-    "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "5d7d33c8c58a2c04",
+    "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "b66bc38f681758d7",
                                               "bytes": 436264192 + 226831104},
-    "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
+    "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "ee0bc3694a9ab89f",
                                               "bytes": 436278272 + 215408384},
-    "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "fde2f73a7ff31de0",
+    "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "ee0bc3694a9ab89f",
                                             "bytes": 352372736 + 211523072},
-    "gemm_f64_4096_rowB": {"sha": "a6bd67c690b12ddb", "bytes": 3657537000 + 130594048},
-    "gemm_bf16_acc16_8192": {"sha": "1fa40d449dccf124", "bytes": 1485834000 + 129398528},
-    "gemm_f16_256": {"sha": "1fa40d449dccf124", "bytes": 570624 + 0},
+    "gemm_f64_4096_rowB": {"sha": "b947734a2fa7d71b", "bytes": 3657537000 + 130594048},
+    "gemm_bf16_acc16_8192": {"sha": "a140329b581276a6", "bytes": 1485834000 + 129398528},
+    "gemm_f16_256": {"sha": "a140329b581276a6", "bytes": 570624 + 0},
 }
 
 
@@ -101,12 +103,20 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def source_sha(rel):
+    """SHA-256 (16 hex digits) of a kernel source with its comments and
+    whitespace removed: what the compiler sees, so that editing a comment
+    does not disown a traffic figure taken from the same code."""
     try:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
     except OSError:
         return None
+    code = "".join(_COMMENT.sub(" ", text).split())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 class Dist:

@@ -94,3 +94,26 @@ def test_workload_meta_algorithmic_figures():
     w = bench.workload_meta("gemm_i8_4096")
     assert w["ops"] == 2 * 4096 ** 3 and w["unit"] == "TOP/s"
     assert w["algorithmic_bytes"] == 2 * 4096 ** 2 + 2 * 4 * 4096 ** 2
+
+
+def test_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    """The traffic figures are keyed by the code of a kernel source: a
+    comment or whitespace edit keeps the key, a code edit changes it."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f = tmp_path / "k.cu"
+    f.write_text("// kernel\n__global__ void k(int* p) { p[0] = 1; }\n")
+    h0 = bench.source_sha("k.cu")
+    f.write_text("/* another\n   comment */ __global__  void k(int* p)\n"
+                 "{  // store\n  p[0] = 1;\n}\n")
+    assert bench.source_sha("k.cu") == h0
+    f.write_text("__global__ void k(int* p) { p[0] = 2; }\n")
+    assert bench.source_sha("k.cu") != h0
+    assert bench.source_sha("missing.cu") is None
+
+
+def test_traffic_keys_name_existing_workloads():
+    from mixed_precision_dense_02_gb300 import synth
+    assert set(bench.NCU_TRAFFIC) <= set(synth.WORKLOADS)
+    for rec in bench.NCU_TRAFFIC.values():
+        assert len(rec["sha"]) == 16
+        assert rec["bytes"] > 0
