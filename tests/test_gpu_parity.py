@@ -186,13 +186,26 @@ def test_i8_exact_large_partial_sums_then_unit_steps():
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (129, 300, 1025), (513, 257, 3000),
-                                   (1024, 1024, 8192)])
+                                   (1024, 1024, 8192), (2100, 2300, 3000)])
 def test_i8_tensor_pipe_shapes_exact(M, N, K):
     """Shapes on the tcgen05 exact-INT8 path: ragged tiles, K tails and
-    several K chunks."""
+    several K chunks.  From three chunks up C joins the INT32 sums during
+    the chunk phase: 513 x 257 x 3000 on single CTAs, 2100 x 2300 x 3000 on
+    CTA pairs (ragged in M, N and K)."""
     g = synth.gemm_inputs(f"i8tc_{M}_{N}_{K}", "i8", M, N, K)
     want, _ = oracle_ref(g)
     check("i8", run_gemm(g, pad=1), want, None, f"i8 {M}x{N}x{K}")
+
+
+def test_i8_early_c_without_c_on_pairs():
+    """The chunk-phase C path with C absent (D = A*B) on CTA pairs."""
+    import torch
+    M, N, K = 2100, 2300, 3072  # unpadded rows: K a multiple of 16
+    g = synth.gemm_inputs("i8tc_noc", "i8", M, N, K)
+    D = binding.gemm(to_dev(g.A), to_dev(g.B))
+    torch.cuda.synchronize()
+    want = oracle.gemm("i8", g.A, g.B, np.zeros((M, N), np.int32))
+    check("i8", D.cpu().numpy(), want, None, "i8 pairs, no C")
 
 
 # ----------------------------------------- FP16/BF16 with 16-bit accumulate
