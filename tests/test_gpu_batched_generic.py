@@ -378,3 +378,18 @@ def test_batched_in_place(dtype_in, M, N, K, batch):
     assert D.data_ptr() == C.data_ptr()
     check(dtype_in, C.cpu().numpy(), want(bi), absab(bi) if dtype_in != "i8" else None,
           f"{dtype_in} {M}x{N}x{K} in place")
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_batched_i8_tensor_memory_long_k(in_place):
+    """Batched INT8 on the tensor-memory GEMM with three 1024-deep chunks
+    per tile, where C joins the INT32 sums during the chunk phase through
+    the entry's own tensor-map coordinate; broadcast and B pattern on."""
+    import torch
+    bi = synth.batched_inputs("bi8_long_k", "i8", 8, M=144, N=96, K=3072,
+                              group=4, abid=3, blgp=2)
+    C = to_dev(bi.C)
+    D = binding.gemm_batched(to_dev(bi.A, "i8"), to_dev(bi.B, "i8"), C,
+                             C if in_place else None, group=4, abid=3, blgp=2)
+    torch.cuda.synchronize()
+    check("i8", D.cpu().numpy(), want(bi), None, f"batched i8 long K in_place={in_place}")
