@@ -117,3 +117,54 @@ def test_traffic_keys_name_existing_workloads():
     for rec in bench.NCU_TRAFFIC.values():
         assert len(rec["sha"]) == 16
         assert rec["bytes"] > 0
+
+
+def _cxx_constant(rel, name):
+    """Value of `constexpr ... name = <integer expression>;` in a library
+    source: literals, int64_t(...) casts, *, << only."""
+    import ast
+    import re
+    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+        m = re.search(r"constexpr\s+\w+\s+" + name + r"\s*=\s*([^;]+);", f.read())
+    assert m, f"{name} not found in {rel}"
+    expr = re.sub(r"int64_t\(([^()]*)\)", r"(\1)", m.group(1))
+
+    def ev(node):
+        if isinstance(node, ast.Expression):
+            return ev(node.body)
+        if isinstance(node, ast.Constant) and isinstance(node.value, (int, float)):
+            return node.value
+        if isinstance(node, ast.BinOp) and isinstance(node.op, (ast.Mult, ast.LShift)):
+            a, b = ev(node.left), ev(node.right)
+            return a * b if isinstance(node.op, ast.Mult) else a << b
+        raise AssertionError(f"unexpected expression {expr!r}")
+
+    return ev(ast.parse(expr.strip(), mode="eval"))
+
+
+def test_bench_kernel_attribution_follows_the_library_routing():
+    """bench.py attributes each workload's traffic figure to the source
+    file of the kernel the library picks; its thresholds must be the
+    library's own."""
+    csrc = "mixed_precision_dense_02_gb300/csrc/"
+    tile_max = _cxx_constant(csrc + "batched_tile.cu", "kTileMaxMacs")
+    mma_max = _cxx_constant(csrc + "batched_mma.cu", "kMaxBlockMacs")
+    mma_max_i8 = _cxx_constant(csrc + "batched_mma.cu", "kMaxBlockMacsI8")
+    i8_min = _cxx_constant(csrc + "api.cu", "kI8TensorCoreMinWork")
+
+    def src(dt, M, N, K, kind="batched"):
+        return bench.kernel_source({"kind": kind, "dtype_in": dt, "M": M,
+                                    "N": N, "K": K}).rsplit("/", 1)[-1]
+
+    assert tile_max == 1 << 20 and src("bf16", 128, 64, 128) == "batched_tile.cu"
+    assert src("bf16", 128, 128, 128) == "gemm_tc.cu"            # 2^21 > tile_max
+    assert mma_max == 96 * 96 * 64 and src("bf16", 96, 96, 64) == "batched_mma.cu"
+    assert src("bf16", 96, 96, 80) == "gemm_tc.cu"               # above mma_max
+    assert mma_max_i8 == 128 ** 3 and src("i8", 128, 128, 128) == "batched_mma.cu"
+    assert src("i8", 144, 128, 128) == "gemm_tc.cu"
+    assert src("bf16", 16, 16, 16) == "batched16.cu"
+    assert i8_min == 2.0 ** 24
+    small = {"kind": "gemm", "dtype_in": "i8", "M": 256, "N": 256, "K": 255}
+    big = dict(small, K=256)
+    assert bench.kernel_source(small).endswith("gemm_i8.cu")
+    assert bench.kernel_source(big).endswith("gemm_tc.cu")
