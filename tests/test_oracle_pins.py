@@ -593,3 +593,127 @@ def test_batched_generic_shapes_are_independent_products(oracle_mod, M, N, K):
     D = oracle_mod.gemm_batched("bf16", bi.A, bi.B, bi.C)
     for b in range(batch):
         assert np.array_equal(D[b], oracle_mod.gemm("bf16", bi.A[b], bi.B[b], bi.C[b]))
+
+
+# ------------------- c5 batched INT8 / FP64 branches and row-major B tiles
+
+def _brute_batched_int(A, B, C, b_layout, src_a, src_b):
+    """Exact integer batched product in Python-sized integers (numpy int64
+    with |sum| far below 2^63): entry b reads A[src_a[b]] and B[src_b[b]]."""
+    D = []
+    for b in range(A.shape[0]):
+        a = A[src_a[b]].astype(np.int64)
+        bt = B[src_b[b]].astype(np.int64)
+        bm = bt.T if b_layout == "col" else bt  # K x N
+        D.append(a @ bm + (0 if C is None else C[b].astype(np.int64)))
+    return np.stack(D)
+
+
+def _maps(batch, G, abid, blgp, table):
+    src_a = [(b // G) * G + abid for b in range(batch)]
+    src_b = [(b // 4) * 4 + table[b % 4] for b in range(batch)] if blgp else list(range(batch))
+    return src_a, src_b
+
+
+@pytest.mark.parametrize("b_layout", ["col", "row"])
+@pytest.mark.parametrize("G,abid,blgp", [(1, 0, 0), (4, 1, 0), (2, 1, 3), (8, 5, 6), (4, 3, 1)])
+def test_batched_i8_branch_bruteforce(oracle_mod, b_layout, G, abid, blgp):
+    """The batched oracle's INT8 branch against exact integer arithmetic on
+    every entry, with the A broadcast (cbsz/abid, "Common MFMA parameters",
+    Shared parameters) and the B lane-group pattern (Dense MFMA parameters,
+    blgp) gathered by the maps the page defines.  N != K and M != N, so a
+    tile stride taken from the wrong extent, or counted in the wrong
+    element size, reads another tile and fails."""
+    batch, M, N, K = 16, 5, 7, 11
+    rng = np.random.default_rng(100 + G * 10 + abid + blgp)
+    A = rng.integers(-128, 128, (batch, M, K), dtype=np.int64).astype(np.int8)
+    shape_b = (batch, N, K) if b_layout == "col" else (batch, K, N)
+    B = rng.integers(-128, 128, shape_b, dtype=np.int64).astype(np.int8)
+    C = rng.integers(-(1 << 20), 1 << 20, (batch, M, N), dtype=np.int64).astype(np.int32)
+    table = _golden_blgp()[blgp]
+    src_a, src_b = _maps(batch, G, abid, blgp, table)
+    D = oracle_mod.gemm_batched("i8", A, B, C, group=G, abid=abid,
+                                b_layout=b_layout, blgp=blgp)
+    assert D.dtype == np.int32
+    want = _brute_batched_int(A, B, C, b_layout, src_a, src_b)
+    assert np.array_equal(D.astype(np.int64), want)
+    # C = None reads as zero
+    D0 = oracle_mod.gemm_batched("i8", A, B, None, group=G, abid=abid,
+                                 b_layout=b_layout, blgp=blgp)
+    assert np.array_equal(D0.astype(np.int64), want - C.astype(np.int64))
+
+
+@pytest.mark.parametrize("b_layout", ["col", "row"])
+@pytest.mark.parametrize("G,abid,blgp", [(1, 0, 0), (4, 1, 0), (2, 0, 2), (16, 9, 7)])
+def test_batched_f64_branch_exact_on_integers(oracle_mod, b_layout, G, abid, blgp):
+    """The FP64 branch on integer-valued doubles, whose sums are exact:
+    the result must equal the integer brute force bit for bit, entry by
+    entry, under every source map."""
+    batch, M, N, K = 16, 6, 9, 13
+    rng = np.random.default_rng(200 + G + abid + blgp)
+    A = rng.integers(-1000, 1001, (batch, M, K)).astype(np.float64)
+    shape_b = (batch, N, K) if b_layout == "col" else (batch, K, N)
+    B = rng.integers(-1000, 1001, shape_b).astype(np.float64)
+    C = rng.integers(-10 ** 6, 10 ** 6, (batch, M, N)).astype(np.float64)
+    table = _golden_blgp()[blgp]
+    src_a, src_b = _maps(batch, G, abid, blgp, table)
+    D = oracle_mod.gemm_batched("f64", A, B, C, group=G, abid=abid,
+                                b_layout=b_layout, blgp=blgp)
+    assert D.dtype == np.float64
+    want = _brute_batched_int(A.astype(np.int64), B.astype(np.int64),
+                              C.astype(np.int64), b_layout, src_a, src_b)
+    assert np.array_equal(D, want.astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype_in", ["i8", "f64"])
+def test_batched_tagged_tiles_int8_and_f64(oracle_mod, dtype_in):
+    """The page's worked example (cbsz = 2, abid = 1: block 1's A to blocks
+    0, 2, 3 and block 5's to 4, 6, 7) read off tagged tiles in the INT8 and
+    FP64 branches: A tile t = (t + 1) I, B = I, C = 0, so D_b = (src + 1) I.
+    Non-square 16 x 16 x 16 tiles are not needed here; the rows and K are
+    equal, so the tag also checks that nothing off the diagonal leaks in."""
+    rows = _golden_broadcast()
+    batch, n = 16, 16
+    dt = np.int8 if dtype_in == "i8" else np.float64
+    eye = np.eye(n, dtype=bool)
+    A = np.zeros((batch, n, n), dt)
+    for t in range(batch):
+        A[t][eye] = t + 1
+    B = np.broadcast_to(eye.astype(dt), (batch, n, n)).copy()
+    C = np.zeros((batch, n, n), np.int32 if dtype_in == "i8" else np.float64)
+    checked = 0
+    for r in rows:
+        if r[0] != "src":
+            continue
+        G, abid, block, source = map(int, r[1:])
+        D = oracle_mod.gemm_batched(dtype_in, A, B, C, group=G, abid=abid)
+        assert D[block, 0, 0] == source + 1 and D[block, n - 1, n - 1] == source + 1
+        assert D[block, 0, 1] == 0 and D[block, 5, 4] == 0
+        checked += 1
+    assert checked >= 8
+
+
+@pytest.mark.parametrize("dtype_in", ["bf16", "i8", "f64"])
+def test_batched_row_major_b_equals_column_major(oracle_mod, dtype_in):
+    """Row-major B tiles (batch, K, N) hold the same matrices as the
+    column-major (batch, N, K) tiles transposed, so both layouts give the
+    same D bit for bit (the oracle sums k in the same order); with K != N
+    a tile stride computed from the wrong extent reads shifted data."""
+    batch, M, N, K = 8, 7, 12, 20
+    bi = synth.batched_inputs(f"rowb_pin_{dtype_in}", dtype_in, batch, M=M, N=N,
+                              K=K, group=2, abid=1)
+    Bt = np.ascontiguousarray(np.swapaxes(bi.B, 1, 2))  # (batch, K, N)
+    for blgp in (0, 5):
+        Dc = oracle_mod.gemm_batched(dtype_in, bi.A, bi.B, bi.C, group=2, abid=1,
+                                     blgp=blgp)
+        Dr = oracle_mod.gemm_batched(dtype_in, bi.A, Bt, bi.C, group=2, abid=1,
+                                     b_layout="row", blgp=blgp)
+        assert np.array_equal(Dc, Dr)
+        # and each entry equals the single-problem oracle with row-major B
+        # (pattern 5 sends quarter 1's B tile to the whole group of four)
+        for b in (0, 3, batch - 1):
+            src = (b // 2) * 2 + 1
+            bsrc = (b // 4) * 4 + 1 if blgp == 5 else b
+            single = oracle_mod.gemm(dtype_in, bi.A[src], Bt[bsrc], bi.C[b],
+                                     b_layout="row")
+            assert np.array_equal(Dr[b], single)
