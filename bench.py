@@ -61,8 +61,7 @@ BF16_FLOP_PER_SM_CLK = 8192.0
 # stale, and it is then reported as null.
 NCU_TRAFFIC: dict = {
     # one ncu capture per workload (dram__bytes_read.sum and
-    # dram__bytes_write.sum of one launch after the warm-up launches;
-    # profiles/*.md)
+    # dram__bytes_write.sum of one launch after the warm-up launches)
     "gemm_i8_4096": {"sha": "a140329b581276a6", "bytes": 179292416 + 42687488},
     "gemm_u8_4096_clamp": {"sha": "a140329b581276a6", "bytes": 184625664 + 43099648},
     "gemm_bf16_8192": {"sha": "a140329b581276a6", "bytes": 1628860000 + 258911744},

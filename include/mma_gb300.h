@@ -310,8 +310,10 @@ mma_status_t mma_profile_end(float *ms, int max_count, int *count);
  * MMA_NOALLOC_SCRATCH_BYTES (for example M = N = K = 4096); larger problems
  * return MMA_ERR_UNSUPPORTED and launch nothing.
  * Set-up: the first call on each device, made with that device current,
- * looks up the array's device address (cudaGetSymbolAddress) and caches it;
- * make that first call before any stream capture begins.
+ * looks up the array's device address (cudaGetSymbolAddress) and caches it
+ * for the device's current context (after cudaDeviceReset the next call
+ * looks it up again); make that first call before any stream capture
+ * begins.  Status codes and profiling (mma_profile_begin) as for mma_gemm.
  * Sharing: all calls on a device use the same array and leave their data in
  * it (nothing there needs to start at zero); calls whose work overlaps on
  * the GPU race on it, so order calls issued on different streams.

@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/mma_gb300.h): argument
 // validation, per-device set-up and dispatch to the kernels.  Nothing here
 // computes any part of D = A * B + C; every arithmetic step runs on the GPU.
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,13 +16,12 @@ __device__ unsigned g_mma_status;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
   bool ready = false;
   bool usable = false;
   int num_sms = 0;
   unsigned* status = nullptr;
+  uint64_t gen = 0;  // context the fields above were set up in
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -36,6 +36,7 @@ struct Profile {
   int count = 0;
   cudaEvent_t ev[2 * kProfMax] = {};
   bool created = false;
+  uint64_t gen = 0;  // context the events belong to
 };
 Profile g_prof;
 std::mutex g_prof_mu;
@@ -49,22 +50,43 @@ struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
   cudaEvent_t done = nullptr;
+  uint64_t gen = 0;  // context the buffer and event belong to
 };
 Workspace g_ws[kMaxDevices];
 std::mutex g_ws_mu;
 
-// Attach the next profiling event pair (if any) to a launch context.
-void attach_profile(Ctx& ctx) {
-  std::lock_guard<std::mutex> lk(g_prof_mu);
-  if (!g_prof.active || g_prof.device != ctx.device || g_prof.count >= kProfMax)
-    return;
-  ctx.prof_start = g_prof.ev[2 * g_prof.count];
-  ctx.prof_stop = g_prof.ev[2 * g_prof.count + 1];
-  ++g_prof.count;
+// Identifier of the calling thread's current CUDA context plus one (0 when
+// no context is current yet).  Without the driver's context-id call every
+// context reads as 1, and state is then set up once per device.
+uint64_t current_context_gen() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+  });
+  if (!get_cur || !get_id) return 1;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 1;
+  return uint64_t(id) + 1;
 }
 
-// Per-device set-up, once, with that device current: SM count, the
-// architecture check and the device address of the status word.
+// Per-device set-up, once per context, with that device current: SM count,
+// the architecture check and the device address of the status word.  A
+// replaced context (cudaDeviceReset) is set up again.
 const DeviceInfo* device_info(int* dev_out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -72,9 +94,11 @@ const DeviceInfo* device_info(int* dev_out) {
     return nullptr;
   }
   *dev_out = dev;
+  uint64_t gen = current_context_gen();
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready || (gen != 0 && gen != d.gen)) {
+    d = DeviceInfo{};
     d.ready = true;
     int major = 0, minor = 0, sms = 0;
     void* p = nullptr;
@@ -92,8 +116,16 @@ const DeviceInfo* device_info(int* dev_out) {
     } else {
       cudaGetLastError();
     }
+    // the symbol lookup made the device's primary context current
+    if (gen == 0) gen = current_context_gen();
+    d.gen = gen != 0 ? gen : 1;
   }
   return d.usable ? &d : nullptr;
+}
+
+Ctx make_ctx(void* stream, int dev, const DeviceInfo* info) {
+  return Ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms,
+             info->status, info->gen};
 }
 
 bool aligned16(const void* p) {
@@ -133,9 +165,18 @@ bool current_ctx(void* stream, Ctx* out) {
   int dev = -1;
   const DeviceInfo* info = device_info(&dev);
   if (!info) return false;
-  *out = Ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms,
-             info->status};
+  *out = make_ctx(stream, dev, info);
   return true;
+}
+
+void attach_profile(Ctx& ctx) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof.active || g_prof.device != ctx.device || g_prof.gen != ctx.gen ||
+      g_prof.count >= kProfMax)
+    return;
+  ctx.prof_start = g_prof.ev[2 * g_prof.count];
+  ctx.prof_stop = g_prof.ev[2 * g_prof.count + 1];
+  ++g_prof.count;
 }
 
 mma_status_t launch_copy_c(const Ctx& ctx, int64_t M, int64_t N,
@@ -166,6 +207,12 @@ template <class F>
 mma_status_t with_workspace(const Ctx& ctx, size_t need, F&& enqueue) {
   std::lock_guard<std::mutex> lk(g_ws_mu);
   Workspace& w = g_ws[ctx.device];
+  if (w.gen != ctx.gen) {
+    // set up in a context that has since been replaced: its buffer and
+    // event went with it
+    w = Workspace{};
+    w.gen = ctx.gen;
+  }
   if (!w.done &&
       cudaEventCreateWithFlags(&w.done, cudaEventDisableTiming) != cudaSuccess) {
     cudaGetLastError();
@@ -271,7 +318,7 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
   int dev = -1;
   const DeviceInfo* info = device_info(&dev);
   if (!info) return MMA_ERR_NO_DEVICE;
-  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  Ctx ctx = make_ctx(stream, dev, info);
   attach_profile(ctx);
 
   if (K == 0) return launch_copy_c(ctx, M, N, int(ea), C, ldc, D, ldd);
@@ -333,7 +380,7 @@ extern "C" mma_status_t mma_gemm_i8_ex(int64_t M, int64_t N, int64_t K,
   int dev = -1;
   const DeviceInfo* info = device_info(&dev);
   if (!info) return MMA_ERR_NO_DEVICE;
-  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  Ctx ctx = make_ctx(stream, dev, info);
   attach_profile(ctx);
   if (K == 0) {
     // D = C: a 32-bit C is in range, so saturation changes nothing
@@ -384,7 +431,7 @@ extern "C" mma_status_t mma_gemm_batched_ex(
   int dev = -1;
   const DeviceInfo* info = device_info(&dev);
   if (!info) return MMA_ERR_NO_DEVICE;
-  Ctx ctx{static_cast<cudaStream_t>(stream), dev, info->num_sms, info->status};
+  Ctx ctx = make_ctx(stream, dev, info);
   attach_profile(ctx);
   // K == 0: D = C tile by tile; the tiles are contiguous, so batch * M rows
   if (K == 0) return launch_copy_c(ctx, batch * M, N, int(ea), C, ldc, D, ldd);
@@ -471,9 +518,14 @@ extern "C" mma_status_t mma_device_status(void* stream) {
 
 extern "C" mma_status_t mma_profile_begin(void) {
   int dev = -1;
-  if (!device_info(&dev)) return MMA_ERR_NO_DEVICE;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info) return MMA_ERR_NO_DEVICE;
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (g_prof.created && g_prof.device != dev) return MMA_ERR_INVALID_ARG;
+  if (g_prof.created && g_prof.gen != info->gen) {
+    // the events belonged to a context that has since been replaced
+    g_prof.created = false;
+  }
   if (!g_prof.created) {
     for (int i = 0; i < 2 * kProfMax; ++i) {
       if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
@@ -484,6 +536,7 @@ extern "C" mma_status_t mma_profile_begin(void) {
     }
     g_prof.created = true;
     g_prof.device = dev;
+    g_prof.gen = info->gen;
   }
   g_prof.active = true;
   g_prof.count = 0;

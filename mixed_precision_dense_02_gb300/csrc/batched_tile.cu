@@ -322,22 +322,23 @@ mma_status_t run_tile(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
                       const void* A, const void* B, const void* C, void* D,
                       int64_t batch, int group, int abid, int blgp) {
   auto kern = batched_tile_kernel<BF16, OUT16, STAGE_C>;
-  static bool attr_set[64] = {};
-  static int per_sm[64] = {};
-  const int dev = ctx.device & 63;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<OUT16, STAGE_C>()) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm[dev], kern, kTileThreads, smem_bytes<OUT16, STAGE_C>()) != cudaSuccess ||
-        per_sm[dev] < 1) {
-      cudaGetLastError();
-      return MMA_ERR_LAUNCH;
-    }
-    attr_set[dev] = true;
-  }
+  // shared-memory limit and resident CTAs per SM, once per context
+  static PerContext<int> occupancy;
+  int per_sm = 0;
+  if (!occupancy.get(ctx, &per_sm, [&](int* v) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<OUT16, STAGE_C>()) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                v, kern, kTileThreads, smem_bytes<OUT16, STAGE_C>()) != cudaSuccess ||
+            *v < 1) {
+          cudaGetLastError();
+          return false;
+        }
+        return true;
+      }))
+    return MMA_ERR_LAUNCH;
   const int64_t units = batch * (M / TM) * (N / TN);
-  int64_t blocks = int64_t(ctx.num_sms) * per_sm[dev];
+  int64_t blocks = int64_t(ctx.num_sms) * per_sm;
   if (blocks > units) blocks = units;
   ctx.mark_start();
   kern<<<int(blocks), kTileThreads, smem_bytes<OUT16, STAGE_C>(), ctx.stream>>>(

@@ -1122,13 +1122,16 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
     tc = td;  // never read: the kernel loads C only when it is given
   }
   auto kern = gemm_tc_kernel<BN, STAGES, BF16, EPI, CL, NSTG>;
-  static bool smem_set[64] = {};  // per device, once per instantiation
-  if (!smem_set[ctx.device & 63]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::ALLOC) != cudaSuccess)
-      return MMA_ERR_LAUNCH;
-    smem_set[ctx.device & 63] = true;
-  }
+  // the dynamic shared-memory limit, once per context and instantiation
+  static PerContext<bool> smem_attr;
+  bool attr_ok = false;
+  if (!smem_attr.get(ctx, &attr_ok, [&](bool* v) {
+        *v = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  L::ALLOC) == cudaSuccess;
+        if (!*v) cudaGetLastError();
+        return *v;
+      }))
+    return MMA_ERR_LAUNCH;
   const int64_t units =
       ((M + BM * CL - 1) / (BM * CL)) * ((N + BN - 1) / BN) * bat.batch;
   if (units > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
@@ -1149,17 +1152,22 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   // per unit of work)
   int64_t clusters = ctx.num_sms / CL;
   if (CL > 1) {
-    static int resident[64] = {};
-    int& r = resident[ctx.device & 63];
-    if (r == 0) {
-      cfg.gridDim = dim3(unsigned(CL * (ctx.num_sms / CL)), 1, 1);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        return MMA_ERR_LAUNCH;
-      }
-      r = n;
-    }
+    // clusters resident at once, once per context and instantiation
+    static PerContext<int> resident;
+    int r = 0;
+    if (!resident.get(ctx, &r, [&](int* v) {
+          cudaLaunchConfig_t probe = cfg;
+          probe.gridDim = dim3(unsigned(CL * (ctx.num_sms / CL)), 1, 1);
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, kern, &probe) != cudaSuccess ||
+              n < 1) {
+            cudaGetLastError();
+            return false;
+          }
+          *v = n;
+          return true;
+        }))
+      return MMA_ERR_LAUNCH;
     clusters = r;
   }
   if (clusters > units) clusters = units;

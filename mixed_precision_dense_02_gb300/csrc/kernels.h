@@ -5,15 +5,24 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/mma_gb300.h"
 
 namespace mmagb {
+
+constexpr int kMaxDevices = 64;
 
 struct Ctx {
   cudaStream_t stream;
   int device;
   int num_sms;
   unsigned* status;  // device status word (bounded-wait timeouts)
+  // Identifier of the device's current CUDA context (unique within the
+  // process, never 0): state cached for one context (kernel attributes,
+  // symbol addresses, buffers) is set up again when it changes, e.g. after
+  // cudaDeviceReset.
+  uint64_t gen = 0;
   // When profiling is active: events recorded on `stream` immediately
   // before and after the call's dominant (contraction) kernel; else null.
   cudaEvent_t prof_start = nullptr;
@@ -132,6 +141,43 @@ mma_status_t launch_batched16(const Ctx& ctx, bool bf16, int64_t batch,
 // Launch context for the current device (false if it is not a usable
 // sm_103 device).
 bool current_ctx(void* stream, Ctx* out);
+
+// Attach the next profiling event pair (if profiling is active) to a launch
+// context.
+void attach_profile(Ctx& ctx);
+
+// A value set up once per device context (a kernel attribute, an occupancy
+// figure, a symbol address): `compute(&value)` runs on the first use in a
+// context, under a lock, so concurrent first calls from several host
+// threads neither race nor repeat it, and runs again when the device's
+// context has been replaced.  Returns false, and caches nothing, when
+// compute fails.
+template <class T>
+class PerContext {
+ public:
+  template <class F>
+  bool get(const Ctx& ctx, T* out, F&& compute) {
+    if (ctx.device < 0 || ctx.device >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(mu_);
+    Slot& s = slot_[ctx.device];
+    if (s.gen != ctx.gen) {
+      T v{};
+      if (!compute(&v)) return false;
+      s.value = v;
+      s.gen = ctx.gen;
+    }
+    *out = s.value;
+    return true;
+  }
+
+ private:
+  struct Slot {
+    uint64_t gen = 0;
+    T value{};
+  };
+  std::mutex mu_;
+  Slot slot_[kMaxDevices];
+};
 
 // K == 0: D = C (or 0), elementwise, element size 2, 4 or 8 bytes.
 mma_status_t launch_copy_c(const Ctx& ctx, int64_t M, int64_t N,

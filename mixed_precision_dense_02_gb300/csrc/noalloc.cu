@@ -14,16 +14,16 @@
 // GPU that loads the library until the process exits.
 //
 // Set-up: the first call on each device (with that device current) looks
-// the array's device address up with cudaGetSymbolAddress and caches it;
-// make that first call before any stream capture begins.  Every call on a
+// the array's device address up with cudaGetSymbolAddress and caches it
+// for the device's context (a context that replaces it, after
+// cudaDeviceReset, looks it up again); make that first call before any
+// stream capture begins.  Every call on a
 // device shares the one array and leaves its contents behind; nothing in it
 // has to start at zero, because each call rewrites every scratch element it
 // later reads.  Two calls whose work overlaps on the GPU (different
 // streams, no ordering between them) race on the array: order them.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "kernels.h"
 
@@ -35,32 +35,21 @@ static __device__ __align__(256) unsigned char
 namespace mmagb {
 namespace {
 
-constexpr int kMaxDevices = 64;
+PerContext<void*> g_scratch;
 
-struct ScratchSlot {
-  bool ready = false;
+// Device address of the scratch array in the context of `ctx` (whose device
+// is current), or null if the lookup fails.
+void* scratch_address(const Ctx& ctx) {
   void* ptr = nullptr;
-};
-ScratchSlot g_slot[kMaxDevices];
-std::mutex g_slot_mu;
-
-// Device address of the scratch array on `dev` (which must be current).
-void* scratch_address(int dev) {
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_slot_mu);
-  ScratchSlot& s = g_slot[dev];
-  if (!s.ready) {
-    void* p = nullptr;
-    const cudaError_t e =
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    s.ptr = p;
-    s.ready = true;
-  }
-  return s.ptr;
+  if (!g_scratch.get(ctx, &ptr, [](void** v) {
+        if (cudaGetSymbolAddress(v, g_noalloc_scratch) != cudaSuccess) {
+          cudaGetLastError();
+          return false;
+        }
+        return *v != nullptr;
+      }))
+    return nullptr;
+  return ptr;
 }
 
 bool aligned16(const void* p) {
@@ -101,8 +90,9 @@ extern "C" mma_status_t mma_gemm_i8_noalloc(int64_t M, int64_t N, int64_t K,
 
   Ctx ctx{};
   if (!current_ctx(stream, &ctx)) return MMA_ERR_NO_DEVICE;
+  attach_profile(ctx);
   if (K == 0) return launch_copy_c(ctx, M, N, 4, C, ldc, D, ldd);
-  void* scratch = scratch_address(ctx.device);
+  void* scratch = scratch_address(ctx);
   if (scratch == nullptr) return MMA_ERR_LAUNCH;
   return launch_gemm_i8_tc(ctx, M, N, K, static_cast<const int8_t*>(A), lda,
                            static_cast<const int8_t*>(B), ldb,

@@ -117,3 +117,109 @@ def oracle_ref(g, rows=None, cols=None):
         return oracle.gemm("i8", A, B, C, b_layout=g.b_layout), None
     return oracle.gemm(g.dtype_in, A, B, C, b_layout=g.b_layout,
                        want_absab=True)
+
+
+# ------------------------------------------------------------ guard bands
+#
+# compute-sanitizer is not available to these tests, so out-of-bounds
+# stores are caught with canaries instead: every output is embedded in a
+# larger device buffer whose bytes outside the output all hold CANARY, and
+# after the call each of those bytes must still hold it (the padding
+# columns between N and the leading dimension, a guard row above and below
+# the matrix, a guard entry before and after a batch).  A store from a
+# ragged TMA box, a predicated warp-level store or a tile half that
+# overhangs its problem changes one of them.
+
+CANARY = 0xA5
+
+
+def _torch_dtype(np_dtype, dtype_in=None):
+    import torch
+    m = {np.dtype(np.float32): torch.float32, np.dtype(np.float64): torch.float64,
+         np.dtype(np.int32): torch.int32, np.dtype(np.int8): torch.int8,
+         np.dtype(np.uint8): torch.uint8}
+    if np.dtype(np_dtype) == np.dtype(np.uint16):
+        return torch.bfloat16 if dtype_in == "bf16" else torch.float16
+    return m[np.dtype(np_dtype)]
+
+
+def _check_canary(buf, inside, what):
+    """buf: device tensor; inside: boolean numpy mask over buf's bytes
+    (True where the call may write)."""
+    import torch
+    torch.cuda.synchronize()
+    raw = buf.contiguous().view(torch.uint8).cpu().numpy().reshape(inside.shape)
+    bad = (raw != CANARY) & ~inside
+    if np.any(bad):
+        idx = np.argwhere(bad)
+        raise AssertionError(f"{what}: {len(idx)} guard bytes overwritten, first at "
+                             f"byte index {tuple(int(v) for v in idx[0])} "
+                             f"(value 0x{int(raw[tuple(idx[0])]):02X})")
+
+
+class GuardedMatrix:
+    """An M x N device matrix inside a canary-filled buffer: `lead` guard
+    rows above, `tail` below, and the leading dimension rounded up to 16
+    bytes plus `pad` more 16-byte chunks of padding columns.  `view` is the
+    matrix (pass it as C or D); `init` (numpy, M x N) fills it."""
+
+    def __init__(self, M, N, np_dtype, *, dtype_in=None, init=None, pad=1,
+                 lead=1, tail=1):
+        import torch
+        self.M, self.N = M, N
+        esize = np.dtype(np_dtype).itemsize
+        per = 16 // esize
+        self.ld = ((N + per - 1) // per) * per + pad * per
+        self.lead, self.tail, self.esize = lead, tail, esize
+        rows = M + lead + tail
+        flat = torch.full((rows * self.ld * esize,), CANARY, dtype=torch.uint8,
+                          device=torch_dev())
+        self.buf = flat.view(_torch_dtype(np_dtype, dtype_in)).view(rows, self.ld)
+        self.view = self.buf[lead:lead + M, :N]
+        if init is not None:
+            self.view.copy_(to_dev(np.ascontiguousarray(init), dtype_in))
+
+    def verify(self, what="guard"):
+        rows = self.M + self.lead + self.tail
+        inside = np.zeros((rows, self.ld * self.esize), bool)
+        inside[self.lead:self.lead + self.M, :self.N * self.esize] = True
+        _check_canary(self.buf, inside, what)
+
+
+class GuardedBatch:
+    """`batch` contiguous M x N tiles (tile stride M * ld, ld >= N) inside a
+    canary-filled buffer with `lead` guard tiles before and `tail` after.
+    With ld == N, `view` is the contiguous (batch, M, N) tensor the batched
+    binding takes; `ptr` and `ld` serve raw C-ABI calls with ld > N."""
+
+    def __init__(self, batch, M, N, np_dtype, *, dtype_in=None, init=None,
+                 pad_cols=0, lead=1, tail=1):
+        import torch
+        self.batch, self.M, self.N = batch, M, N
+        esize = np.dtype(np_dtype).itemsize
+        self.esize = esize
+        self.ld = N + pad_cols
+        self.lead, self.tail = lead, tail
+        tiles = batch + lead + tail
+        flat = torch.full((tiles * M * self.ld * esize,), CANARY, dtype=torch.uint8,
+                          device=torch_dev())
+        self.buf = flat.view(_torch_dtype(np_dtype, dtype_in)).view(tiles, M, self.ld)
+        self.tiles = self.buf[lead:lead + batch]          # (batch, M, ld)
+        self.view = self.tiles if pad_cols == 0 else None
+        self.ptr = self.tiles.data_ptr()
+        if init is not None:
+            self.tiles[:, :, :N].copy_(to_dev(np.ascontiguousarray(init), dtype_in))
+
+    def result(self):
+        """The (batch, M, N) outputs as a host array (16-bit floats as bits)."""
+        import torch
+        t = self.tiles[:, :, :self.N]
+        if t.dtype in (torch.float16, torch.bfloat16):
+            return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        return t.contiguous().cpu().numpy()
+
+    def verify(self, what="guard"):
+        tiles = self.batch + self.lead + self.tail
+        inside = np.zeros((tiles, self.M, self.ld * self.esize), bool)
+        inside[self.lead:self.lead + self.batch, :, :self.N * self.esize] = True
+        _check_canary(self.buf, inside, what)

@@ -17,7 +17,7 @@ import pytest
 import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import check, check16, to_dev
+from helpers import GuardedBatch, check, check16, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -33,15 +33,20 @@ def _lib():
     binding.device_status()
 
 
+OUT_NP = {"f16": np.float32, "bf16": np.float32, "i8": np.int32, "f64": np.float64}
+
+
 def run(bi, *, use_c=True, acc=None):
-    import torch
-    D = binding.gemm_batched(to_dev(bi.A, bi.dtype_in), to_dev(bi.B, bi.dtype_in),
-                             to_dev(bi.C, bi.dtype_in) if use_c else None,
-                             group=bi.group, abid=bi.abid, blgp=bi.blgp, acc=acc)
-    torch.cuda.synchronize()
-    if D.dtype in (torch.float16, torch.bfloat16):   # 16-bit results as bits
-        return D.view(torch.int16).cpu().numpy().view(np.uint16)
-    return D.cpu().numpy()
+    """The batched call with D inside a guard band (a canary tile before
+    and after the batch); 16-bit results come back as bit patterns."""
+    out16 = acc == "same" or (use_c and bi.C.dtype == np.uint16)
+    Gd = GuardedBatch(bi.batch, bi.M, bi.N, np.uint16 if out16 else OUT_NP[bi.dtype_in],
+                      dtype_in=bi.dtype_in)
+    binding.gemm_batched(to_dev(bi.A, bi.dtype_in), to_dev(bi.B, bi.dtype_in),
+                         to_dev(bi.C, bi.dtype_in) if use_c else None, Gd.view,
+                         group=bi.group, abid=bi.abid, blgp=bi.blgp, acc=acc)
+    Gd.verify(f"batched {bi.dtype_in} {bi.M}x{bi.N}x{bi.K} x{bi.batch} D guard")
+    return Gd.result()
 
 
 def absab(bi):
@@ -371,12 +376,13 @@ def test_batched_in_place(dtype_in, M, N, K, batch):
     import torch
     bi = synth.batched_inputs(f"bip_{M}_{N}_{K}", dtype_in, batch, M=M, N=N,
                               K=K, group=4, abid=3, blgp=2)
-    C = to_dev(bi.C)
+    Gc = GuardedBatch(batch, M, N, OUT_NP[dtype_in], init=bi.C)
+    C = Gc.view
     D = binding.gemm_batched(to_dev(bi.A, dtype_in), to_dev(bi.B, dtype_in), C,
                              C, group=4, abid=3, blgp=2)
-    torch.cuda.synchronize()
+    Gc.verify(f"{dtype_in} {M}x{N}x{K} in place guard")
     assert D.data_ptr() == C.data_ptr()
-    check(dtype_in, C.cpu().numpy(), want(bi), absab(bi) if dtype_in != "i8" else None,
+    check(dtype_in, Gc.result(), want(bi), absab(bi) if dtype_in != "i8" else None,
           f"{dtype_in} {M}x{N}x{K} in place")
 
 
@@ -393,3 +399,43 @@ def test_batched_i8_tensor_memory_long_k(in_place):
                              C if in_place else None, group=4, abid=3, blgp=2)
     torch.cuda.synchronize()
     check("i8", D.cpu().numpy(), want(bi), None, f"batched i8 long K in_place={in_place}")
+
+
+# Batched outputs with padding columns (ldc = ldd > N, tile stride M * ld)
+# through the raw C ABI, inside guard bands: nothing may be written to the
+# padding columns of any tile, nor before the first or after the last tile.
+PADDED_LD_CASES = [
+    ("bf16", 16, 16, 16, 64, 4),
+    ("bf16", 32, 32, 32, 64, 4),
+    ("f16", 64, 64, 64, 32, 8),
+    ("bf16", 64, 128, 128, 16, 4),
+    ("bf16", 128, 128, 128, 16, 4),
+    ("bf16", 100, 72, 40, 12, 4),
+    ("i8", 32, 32, 32, 64, 4),
+    ("i8", 160, 96, 64, 8, 4),
+    ("f64", 24, 40, 16, 8, 2),
+]
+
+
+@pytest.mark.parametrize("dtype_in,M,N,K,batch,pad", PADDED_LD_CASES)
+def test_batched_padded_ld_guard(dtype_in, M, N, K, batch, pad):
+    import torch
+    bi = synth.batched_inputs(f"bpld_{dtype_in}_{M}_{N}_{K}", dtype_in, batch, M=M,
+                              N=N, K=K, group=2, abid=1, blgp=7)
+    codes = {"f16": (binding.MMA_F16, binding.MMA_F32),
+             "bf16": (binding.MMA_BF16, binding.MMA_F32),
+             "i8": (binding.MMA_I8, binding.MMA_I32),
+             "f64": (binding.MMA_F64, binding.MMA_F64)}[dtype_in]
+    out_dt = OUT_NP[dtype_in]
+    Gc = GuardedBatch(batch, M, N, out_dt, init=bi.C, pad_cols=pad)
+    Gd = GuardedBatch(batch, M, N, out_dt, pad_cols=pad)
+    A, B = to_dev(bi.A, dtype_in), to_dev(bi.B, dtype_in)
+    st = binding.mma_gemm_batched_ex(codes[0], codes[1], M, N, K, A.data_ptr(), K,
+                                     B.data_ptr(), K, Gc.ptr, Gc.ld, Gd.ptr, Gd.ld,
+                                     batch, 2, 1, 7,
+                                     torch.cuda.current_stream().cuda_stream)
+    assert st == 0, binding.STATUS.get(st, st)
+    Gd.verify(f"batched {dtype_in} {M}x{N}x{K} padded ldd guard")
+    Gc.verify(f"batched {dtype_in} {M}x{N}x{K} padded ldc (input) guard")
+    check(dtype_in, Gd.result(), want(bi), absab(bi) if dtype_in != "i8" else None,
+          f"batched {dtype_in} {M}x{N}x{K} padded ld")

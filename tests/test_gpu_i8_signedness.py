@@ -21,7 +21,7 @@ import pytest
 import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import check, dev_padded, to_dev
+from helpers import GuardedMatrix, check, dev_padded, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -50,9 +50,9 @@ def run_i8x(A, B, C, *, clamp, b_layout="col", pad=0):
     Bd = dev_padded(B, extra=pad)
     Cd = None if C is None else dev_padded(C, extra=pad)
     M, N = A.shape[0], (B.shape[0] if b_layout == "col" else B.shape[1])
-    Dd = dev_padded(np.full((M, N), 0x3C3C3C3C, np.int32), extra=pad + 1)
-    out = binding.gemm_i8_ex(Ad, Bd, Cd, Dd, clamp=clamp, b_layout=b_layout)
-    torch.cuda.synchronize()
+    Gd = GuardedMatrix(M, N, np.int32, pad=pad + 1)
+    out = binding.gemm_i8_ex(Ad, Bd, Cd, Gd.view, clamp=clamp, b_layout=b_layout)
+    Gd.verify(f"8-bit {M}x{N}x{A.shape[1]} clamp={clamp} {b_layout}-B D guard")
     return out.cpu().numpy()
 
 
@@ -170,32 +170,24 @@ def test_long_k_folds_and_saturates_once(sa, sb):
 
 
 def test_full_size_u8_clamp_workload():
-    """The 4096^3 unsigned saturating workload: sampled blocks against the
-    oracle, and at every output the properties that hold at any size for
-    nonnegative products: C <= D, and D - C <= K * 255^2 unless D saturated."""
+    """The 4096^3 unsigned saturating workload, D inside guard bands: every
+    one of the 16.8 M outputs against the oracle, bit for bit (the oracle
+    needs a few seconds), and the properties that hold at any size for
+    nonnegative products: C <= D, and D - C <= K * 255^2 unless D
+    saturated."""
     import torch
     name = "gemm_u8_4096_clamp"
     g = synth.workload_gemm_inputs(name)
     A, B, C = to_dev(g.A), to_dev(g.B), to_dev(g.C)
-    D = binding.gemm_i8_ex(A, B, C, clamp=True)
-    torch.cuda.synchronize()
+    Gd = GuardedMatrix(g.M, g.N, np.int32)
+    D = binding.gemm_i8_ex(A, B, C, Gd.view, clamp=True)
+    Gd.verify(f"{name} D guard")
     d64, c64 = D.long(), C.long()
     assert bool((d64 >= c64).all())
     assert bool(((d64 == I32_MAX) | (d64 - c64 <= g.K * 255 * 255)).all())
     assert int((d64 == I32_MAX).sum()) > 0
-    rng = np.random.default_rng(4321)
-    rows = np.unique(np.append(rng.choice(g.M, 95, replace=False), g.M - 1))
-    cols = np.unique(np.append(rng.choice(g.N, 95, replace=False), g.N - 1))
-    # add some saturated outputs to the sample
-    sat = torch.nonzero(D == I32_MAX)[:24].cpu().numpy()
-    rows = np.unique(np.concatenate([rows, sat[:, 0]]))
-    cols = np.unique(np.concatenate([cols, sat[:, 1]]))
-    want, ov = oracle.gemm_i8_ex(np.ascontiguousarray(g.A[rows]),
-                                 np.ascontiguousarray(g.B[cols]),
-                                 np.ascontiguousarray(g.C[np.ix_(rows, cols)]),
-                                 clamp=True)
-    got = D[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
-    check("i8", got, want, None, name)
+    want, ov = oracle.gemm_i8_ex(g.A, g.B, g.C, clamp=True)
+    check("i8", D.cpu().numpy(), want, None, name)
     assert ov > 0
 
 

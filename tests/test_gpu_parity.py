@@ -14,7 +14,8 @@ import pytest
 import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import check, check16, dev_padded, oracle_ref, to_dev
+from helpers import (GuardedBatch, GuardedMatrix, check, check16, dev_padded,
+                     oracle_ref, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,17 +34,20 @@ def _lib():
 
 
 def run_gemm(g, *, pad=0, use_c=True, inplace=False):
-    """Run the GPU GEMM for GemmInputs g with padded leading dimensions."""
-    import torch
+    """Run the GPU GEMM for GemmInputs g with padded leading dimensions; D
+    (or C = D in place) sits in a canary-filled buffer whose guard rows and
+    padding columns must come back untouched."""
     A = dev_padded(g.A, g.dtype_in, extra=pad)
     B = dev_padded(g.B, g.dtype_in, extra=pad)
-    C = dev_padded(g.C, extra=pad) if use_c else None
+    out_dt = OUT_NP[g.dtype_in]
     if inplace:
-        D = C
+        G = GuardedMatrix(g.M, g.N, out_dt, init=g.C, pad=pad + 1)
+        C = G.view
     else:
-        D = dev_padded(np.zeros_like(g.C), extra=pad + 1)
-    out = binding.gemm_ex(A, B, C, D, b_layout=g.b_layout)
-    torch.cuda.synchronize()
+        G = GuardedMatrix(g.M, g.N, out_dt, pad=pad + 1)
+        C = dev_padded(g.C, extra=pad) if use_c else None
+    out = binding.gemm_ex(A, B, C, G.view, b_layout=g.b_layout)
+    G.verify(f"{g.dtype_in} {g.M}x{g.N}x{g.K} {g.b_layout}-B D guard")
     return out.cpu().numpy()
 
 
@@ -185,6 +189,72 @@ def test_i8_exact_large_partial_sums_then_unit_steps():
     check("i8", run_gemm(g), want, None, "large partial sums then unit steps")
 
 
+def _mixed_step_operands(M, N, K, seed):
+    """8-bit operands whose 16-deep K steps mix 2^14-sized products with
+    +-1 products while each 1024-deep chunk's running sum climbs towards
+    the exact-FP32 limit 2^24.  Rows of A and columns of B come in four
+    families (index mod 4); a family fixes where the unit entries sit in
+    every chunk and the value of all other entries:
+      0: all steps 2^14 products, then the last 16 steps of the chunk each
+         hold one +-1 product (chunk sum 2^24 - 16 * 2^14 +- 16);
+      1: one +-1 product in every step (chunk sum 64 * 15 * 2^14 +- 64);
+      2: a single +-1 product at step 37 (chunk sum 2^24 - 2^14 +- 1, the
+         closest to 2^24 a unit product allows: every int8 product other
+         than (-128)^2 is at least 128 below 2^14, so a chunk of 1024
+         products reaches no integer strictly between 2^24 - 128 and 2^24);
+      3: as 1, with B's other entries +127, so the sums fall towards
+         -64 * 15 * 16256.
+    Rows and columns of different families meet at +-128 products as
+    well.  The unit signs are random per entry."""
+    rng = np.random.default_rng(seed)
+    step = np.arange(64)
+    units = [
+        np.concatenate([np.zeros(48 * 16, bool),
+                        np.eye(16, dtype=bool)[(step[48:] * 5) % 16].ravel()]),
+        np.eye(16, dtype=bool)[(step * 3) % 16].ravel(),
+        np.zeros(1024, bool),
+        np.eye(16, dtype=bool)[(step * 7 + 1) % 16].ravel(),
+    ]
+    units[2][37 * 16 + 9] = True
+    big_a = [-128, -128, -128, -128]
+    big_b = [-128, -128, -128, 127]
+
+    def operand(rows, big):
+        X = np.empty((rows, K), np.int8)
+        for f in range(4):
+            mask = np.resize(units[f], K)
+            sign = rng.choice(np.array([-1, 1], np.int8), size=(len(range(f, rows, 4)), K))
+            X[f::4] = np.where(mask[None, :], sign, np.int8(big[f]))
+        return X
+
+    return operand(M, big_a), operand(N, big_b)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 4096), (2100, 2300, 4096)])
+@pytest.mark.parametrize("use_c", [False, True])
+def test_i8_exact_mixed_steps_near_the_fp32_limit(M, N, K, use_c):
+    """Exact INT8 on the tensor pipe where every 16-deep K step of a
+    1024-deep chunk mixes 2^14 products with +-1 products and the chunk's
+    partial sums approach +-2^24, on single CTAs (256 x 384) and on CTA
+    pairs (2100 x 2300, ragged), with and without C; bit-exact against the
+    oracle over the whole output."""
+    A, B = _mixed_step_operands(M, N, K, seed=M + N + int(use_c))
+    C = (synth.int_uniform(0, 29, M * N, -(1 << 20), 1 << 20).astype(np.int32).reshape(M, N)
+         if use_c else np.zeros((M, N), np.int32))
+    g = synth.GemmInputs("i8", M, N, K, A, B, C)
+    want = oracle.gemm("i8", A, B, C)
+    # the families reach the intended chunk sums (first chunk, C excluded)
+    c0 = A[:4, :1024].astype(np.int64) @ B[:4, :1024].T.astype(np.int64)
+    assert abs(int(c0[0, 0]) - ((1 << 24) - 16 * 16384)) <= 16
+    assert abs(int(c0[1, 1]) - 64 * 15 * 16384) <= 64
+    assert abs(int(c0[2, 2]) - ((1 << 24) - 16384)) == 1
+    assert abs(int(c0[3, 3]) + 64 * 15 * 16256) <= 64
+    if use_c:
+        check("i8", run_gemm(g, pad=1), want, None, f"i8 mixed steps {M}x{N}x{K} with C")
+    else:
+        check("i8", run_gemm(g, use_c=False), want, None, f"i8 mixed steps {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (129, 300, 1025), (513, 257, 3000),
                                    (1024, 1024, 8192), (2100, 2300, 3000)])
 def test_i8_tensor_pipe_shapes_exact(M, N, K):
@@ -221,10 +291,15 @@ def run_gemm16(g, *, pad=0, use_c=True, inplace=False):
     import torch
     A = dev_padded(g.A, g.dtype_in, extra=pad)
     B = dev_padded(g.B, g.dtype_in, extra=pad)
-    C = dev_padded(g.C, g.dtype_in, extra=pad) if use_c else None
-    D = C if inplace else dev_padded(np.zeros_like(g.C), g.dtype_in, extra=pad + 1)
-    out = binding.gemm_ex(A, B, C, D, b_layout=g.b_layout, acc="same")
-    torch.cuda.synchronize()
+    if inplace:
+        G = GuardedMatrix(g.M, g.N, np.uint16, dtype_in=g.dtype_in, init=g.C,
+                          pad=pad + 1)
+        C = G.view
+    else:
+        G = GuardedMatrix(g.M, g.N, np.uint16, dtype_in=g.dtype_in, pad=pad + 1)
+        C = dev_padded(g.C, g.dtype_in, extra=pad) if use_c else None
+    out = binding.gemm_ex(A, B, C, G.view, b_layout=g.b_layout, acc="same")
+    G.verify(f"{g.dtype_in}->16-bit {g.M}x{g.N}x{g.K} D guard")
     return out.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
@@ -280,9 +355,10 @@ def test_acc16_full_size_sampled():
     import torch
     M = N = K = 8192
     g = acc16_inputs("acc16_8192", "bf16", M, N, K)
+    Gd = GuardedMatrix(M, N, np.uint16, dtype_in="bf16")
     D = binding.gemm_ex(to_dev(g.A, "bf16"), to_dev(g.B, "bf16"), to_dev(g.C, "bf16"),
-                        acc="same")
-    torch.cuda.synchronize()
+                        Gd.view, acc="same")
+    Gd.verify("bf16->bf16 8192^3 D guard")
     rng = np.random.default_rng(99)
     rows = np.unique(np.append(rng.choice(M, 64, replace=False), M - 1))
     cols = np.unique(np.append(rng.choice(N, 64, replace=False), N - 1))
@@ -295,11 +371,11 @@ def test_acc16_full_size_sampled():
 # ------------------------------------------------------------ batched
 
 def run_batched(bi):
-    import torch
-    D = binding.gemm_batched(to_dev(bi.A, bi.dtype_in), to_dev(bi.B, bi.dtype_in),
-                             to_dev(bi.C), group=bi.group, abid=bi.abid)
-    torch.cuda.synchronize()
-    return D.cpu().numpy()
+    G = GuardedBatch(bi.batch, bi.M, bi.N, OUT_NP[bi.dtype_in])
+    binding.gemm_batched(to_dev(bi.A, bi.dtype_in), to_dev(bi.B, bi.dtype_in),
+                         to_dev(bi.C), G.view, group=bi.group, abid=bi.abid)
+    G.verify(f"batched {bi.dtype_in} x{bi.batch} D guard")
+    return G.result()
 
 
 def batched_absab(bi):
@@ -343,19 +419,27 @@ def _sample_blocks(g, rng, nrow, ncol):
     return np.unique(rows), np.unique(cols)
 
 
+FULL_COMPARE = {"gemm_i8_4096", "gemm_bf16_skinny_16384x128x4096"}
+
+
 @pytest.mark.parametrize("name", ["gemm_f16_256", "gemm_i8_4096", "gemm_bf16_8192",
                                   "gemm_f64_4096_rowB",
                                   "gemm_bf16_skinny_16384x128x4096"])
 def test_full_size_workload(name):
+    """The workloads at full size, D inside guard bands.  The INT8 headline
+    (16.8 M outputs, bit-exact) and the skinny BF16 product are compared in
+    full (the oracle needs a few seconds for each); the 8192^3 BF16 and the
+    4096^3 FP64 products on sampled row x column blocks."""
     import torch
     w = synth.WORKLOADS[name]
     g = synth.gemm_inputs(name, w["dtype_in"], w["M"], w["N"], w["K"],
                           dist=w.get("dist", "normal"),
                           b_layout=w.get("b_layout", "col"))
+    Gd = GuardedMatrix(g.M, g.N, OUT_NP[g.dtype_in])
     D = binding.gemm_ex(to_dev(g.A, g.dtype_in), to_dev(g.B, g.dtype_in),
-                        to_dev(g.C), b_layout=g.b_layout)
-    torch.cuda.synchronize()
-    if g.M * g.N * g.K <= 256 ** 3:
+                        to_dev(g.C), Gd.view, b_layout=g.b_layout)
+    Gd.verify(f"{name} D guard")
+    if g.M * g.N * g.K <= 256 ** 3 or name in FULL_COMPARE:
         want, ab = oracle_ref(g)
         check(g.dtype_in, D.cpu().numpy(), want, ab, name)
         return
@@ -385,9 +469,10 @@ def test_ragged_shapes_on_cta_pairs(dtype_in):
     import torch
     M, N, K = 2000, 2600, 1000
     g = synth.gemm_inputs(f"pair_ragged_{dtype_in}", dtype_in, M, N, K, dist="uniform")
+    Gd = GuardedMatrix(M, N, OUT_NP[dtype_in], pad=2)
     D = binding.gemm(dev_padded(g.A, dtype_in), dev_padded(g.B, dtype_in),
-                     dev_padded(g.C))
-    torch.cuda.synchronize()
+                     dev_padded(g.C), Gd.view)
+    Gd.verify(f"{dtype_in} ragged pairs D guard")
     rng = np.random.default_rng(11)
     rows = np.unique(np.append(rng.choice(M, 90, replace=False), [M - 1, M - 208]))
     A = np.ascontiguousarray(g.A[rows])

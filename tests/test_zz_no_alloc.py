@@ -1,27 +1,37 @@
-"""The allocation-free INT8 entry point, checked against the regular one.
+"""The allocation-free INT8 entry point, checked against the regular one
+and against the CPU oracle.
 
 mma_gemm_i8_noalloc is for callers that cannot let a library allocate device
 memory: programs whose own pool allocator has already reserved the memory
 they may use, and services that forbid cudaMalloc/cudaFree after start-up
 because those calls can stall the whole device.  Its scratch is a fixed
 array in the library's device image instead of a buffer grown with
-cudaMalloc.  Here it is called through the C ABI twice in a row, on two
-different problems (the first at the exact scratch limit, the second ragged
-and smaller, so stale scratch contents from the first would show), and each
-INT32 result must equal bit for bit what mma_gemm returns for the same
-inputs.  A problem one step past the limit must be refused.
+cudaMalloc.  Here it is called through the C ABI several times in a row:
 
-This file is named to be collected last, so that a run stopping at the first
-failure has already run every other test; it also passes on its own.
+* on two different problems (the first at the exact scratch limit, the
+  second ragged and smaller), each INT32 result equal bit for bit to what
+  mma_gemm returns for the same inputs and to the oracle over the whole
+  output;
+* after a call that fills the whole scratch with nonzero values, on a
+  problem whose K is not a multiple of 8, so the scratch rows carry stale
+  padding columns between K and their 16-byte-rounded width: nothing may
+  read them;
+* one step past the limit, which must be refused without launching.
+
+Every output sits in a canary-filled buffer whose guard rows and padding
+columns must come back untouched.  This file is named to be collected
+last, so that a run stopping at the first failure has already run every
+other test; it also passes on its own.
 """
 from __future__ import annotations
 
 import numpy as np
 import pytest
 
+import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import dev_padded
+from helpers import GuardedMatrix, check, dev_padded
 
 pytestmark = pytest.mark.gpu
 
@@ -59,17 +69,41 @@ def test_noalloc_matches_mma_gemm_on_two_calls_in_a_row(torch_cuda):
         A = dev_padded(g.A)
         B = dev_padded(g.B)
         C = dev_padded(g.C)
-        D = dev_padded(np.full((M, N), -7, np.int32), extra=1)
-        assert _noalloc(torch, A, B, C, D) == 0
+        Gd = GuardedMatrix(M, N, np.int32)
+        assert _noalloc(torch, A, B, C, Gd.view) == 0
         ref = binding.gemm(A, B, C)
         torch.cuda.synchronize()
-        assert ref.data_ptr() != D.data_ptr()
         binding.device_status()
-        assert torch.equal(D, ref), f"{M}x{N}x{K}: differs from mma_gemm"
-        # and the INT32 values are the exact ones (spot check against Python ints)
-        i, j = M - 1, N - 1
-        exact = int(np.dot(g.A[i].astype(np.int64), g.B[j].astype(np.int64))) + int(g.C[i, j])
-        assert int(D[i, j]) == exact
+        Gd.verify(f"noalloc {M}x{N}x{K} D guard")
+        assert torch.equal(Gd.view, ref), f"{M}x{N}x{K}: differs from mma_gemm"
+        check("i8", Gd.view.cpu().numpy(), oracle.gemm("i8", g.A, g.B, g.C), None,
+              f"noalloc {M}x{N}x{K} against the oracle")
+
+
+def test_noalloc_ignores_stale_scratch_beyond_k(torch_cuda):
+    torch = torch_cuda
+    dev = torch.device("cuda:0")
+    # fill the whole scratch with BF16 -1 (every row at its full width)
+    M = N = K = 4096
+    A = torch.full((M, K), -1, dtype=torch.int8, device=dev)
+    B = torch.full((N, K), -1, dtype=torch.int8, device=dev)
+    C = torch.zeros((M, N), dtype=torch.int32, device=dev)
+    D = torch.empty((M, N), dtype=torch.int32, device=dev)
+    assert _noalloc(torch, A, B, C, D) == 0
+    torch.cuda.synchronize()
+    assert bool((D == K).all())
+    # K = 1003: scratch rows are 1008 wide, columns 1003..1007 stale
+    M, N, K = 300, 520, 1003
+    g = synth.gemm_inputs("noalloc_k1003", "i8", M, N, K)
+    A2, B2, C2 = dev_padded(g.A), dev_padded(g.B), dev_padded(g.C)
+    assert A2.stride(0) == 1008 and B2.stride(0) == 1008
+    Gd = GuardedMatrix(M, N, np.int32)
+    assert _noalloc(torch, A2, B2, C2, Gd.view) == 0
+    torch.cuda.synchronize()
+    binding.device_status()
+    Gd.verify("noalloc K=1003 D guard")
+    check("i8", Gd.view.cpu().numpy(), oracle.gemm("i8", g.A, g.B, g.C), None,
+          "noalloc K=1003 after a full-scratch call")
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(torch_cuda):
