@@ -544,13 +544,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     // Store staging block `buf` to D at (col, row0) of entry z, or close an
-    // empty bulk group when the block lies wholly outside D.
+    // empty bulk group when the block lies wholly outside D.  A TMA store
+    // clipped at a row end that is not 16-byte aligned still writes that
+    // 16-byte chunk whole, which would overwrite the caller's columns past
+    // N; so D's tensor map ends at N_TMA (N rounded down to 16 bytes) and
+    // the columns [N_TMA, N) are stored by the lanes, one element each
+    // (lane = row of the block).
+    constexpr int EB = EPI == Epi::H16 ? 2 : 4;  // bytes per D element
+    const int n_tma = N & ~(16 / EB - 1);
     auto emit_block = [&](uint8_t* buf, int col, int row0, int z) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        if (col < N && row0 < M) tma_store_3d(&tmD, buf, col, row0, z);
+        if (col < n_tma && row0 < M) tma_store_3d(&tmD, buf, col, row0, z);
         bulk_commit_group();
+      }
+      if (col + COLS > n_tma && col < N && row0 + lane < M) {
+        const int c0 = col > n_tma ? col : n_tma;
+        const int c1 = col + COLS < N ? col + COLS : N;
+        uint8_t* drow = static_cast<uint8_t*>(Dv) +
+                        (int64_t(z) * M + row0 + lane) * ldd * EB;
+        for (int c = c0; c < c1; ++c) {
+          const int byte = (c - col) * EB;  // within the 64-byte block row
+          const uint8_t* src = buf + lane * 64 +
+                               (((byte >> 4) ^ ((lane >> 1) & 3)) << 4) +
+                               (byte & 15);
+          if constexpr (EB == 4)
+            *reinterpret_cast<uint32_t*>(drow + int64_t(c) * 4) =
+                *reinterpret_cast<const uint32_t*>(src);
+          else
+            *reinterpret_cast<uint16_t*>(drow + int64_t(c) * 2) =
+                *reinterpret_cast<const uint16_t*>(src);
+        }
       }
       __syncwarp();
     };
@@ -1031,6 +1056,8 @@ __global__ void __launch_bounds__(kRowThreads)
 
 // ----------------------------------------------------------------- host
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1053,7 +1080,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // overhanging a tile's last row or K reads zeros, never the next tile).
 bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t K,
                      int64_t rows, int64_t ld_elems, int box_rows, bool bf16,
-                     int64_t count = 1) {
+                     int64_t count) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(rows), cuuint64_t(count)};
@@ -1076,7 +1103,7 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t K,
 // x 1 box, 64-byte swizzle, matching the epilogue's staging blocks.
 bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
                  int64_t ld_elems, CUtensorMapDataType dt, int elem_bytes,
-                 int64_t count = 1) {
+                 int64_t count) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {cuuint64_t(N), cuuint64_t(M), cuuint64_t(count)};
@@ -1092,6 +1119,8 @@ bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 // pdl: launch as a programmatic dependent of the kernel just before it on
 // the stream (a pass that produced A or B).
@@ -1111,9 +1140,13 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   const int cd_bytes = EPI == Epi::H16 ? 2 : 4;
   CUtensorMap ta, tb, tc, td;
   const int64_t nt = bat.batch;  // tiles of each operand
+  // D's map ends at the last 16-byte boundary of its rows (the kernel's
+  // lanes store any columns beyond it); a map is still needed when that
+  // leaves none, though the kernel then never stores through it.
+  const int64_t n_tma = N & ~int64_t(16 / cd_bytes - 1);
   if (!make_kmajor_map(&ta, A, K, M, lda, BM, BF16, nt) ||
       !make_kmajor_map(&tb, B, K, N, ldb, BN / CL, BF16, nt) ||
-      !make_cd_map(&td, D, N, M, ldd, cd_type, cd_bytes, nt))
+      !make_cd_map(&td, D, n_tma > 0 ? n_tma : N, M, ldd, cd_type, cd_bytes, nt))
     return MMA_ERR_LAUNCH;
   if (C != nullptr) {
     if (!make_cd_map(&tc, C, N, M, ldc, cd_type, cd_bytes, nt))

@@ -2,6 +2,7 @@
 // Arguments arrive here already validated (sizes, pointers, alignment).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,6 +37,18 @@ struct Ctx {
   }
 };
 
+// TMA tensor maps (gemm_tc.cu).  K-major operand: `count` tiles of `rows`
+// rows of K contiguous 16-bit elements (leading dimension ld_elems, tile t
+// rows * ld_elems elements after tile t - 1), box 64 x box_rows x 1,
+// 128-byte swizzle, zero fill out of bounds.  Row-major C/D: `count` M x N
+// tiles, box 64 bytes x 32 rows x 1, 64-byte swizzle.
+bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t K,
+                     int64_t rows, int64_t ld_elems, int box_rows, bool bf16,
+                     int64_t count = 1);
+bool make_cd_map(CUtensorMap* map, const void* base, int64_t N, int64_t M,
+                 int64_t ld_elems, CUtensorMapDataType dt, int elem_bytes,
+                 int64_t count = 1);
+
 // tcgen05 GEMM, FP16/BF16 inputs, column-major B; C and D are FP32, or
 // with out16 of the input's 16-bit type (FP32 accumulation, one rounding).
 mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, bool out16,
@@ -43,6 +56,21 @@ mma_status_t launch_gemm_tc_f16(const Ctx& ctx, bool bf16, bool out16,
                                 int64_t lda, const void* B, int64_t ldb,
                                 const void* C, int64_t ldc, void* D,
                                 int64_t ldd);
+
+// Stream-K tcgen05 GEMM (gemm_sk.cu) for FP16/BF16 -> FP32 products with
+// fewer 128 x 128 output tiles than SMs: the tiles' K steps are split
+// evenly over all SMs, partial tiles meet in `partials`
+// (gemm_sk_workspace_bytes) behind per-warp release flags (`flags`,
+// gemm_sk_flag_count entries, each last written with an earlier sequence
+// number, 0 at allocation); `seq` is this call's nonzero sequence number.
+bool gemm_sk_fits(int num_sms, int64_t M, int64_t N, int64_t K);
+size_t gemm_sk_workspace_bytes(int num_sms);
+size_t gemm_sk_flag_count(int num_sms);
+mma_status_t launch_gemm_sk(const Ctx& ctx, bool bf16, int64_t M, int64_t N,
+                            int64_t K, const void* A, int64_t lda,
+                            const void* B, int64_t ldb, const float* C,
+                            int64_t ldc, float* D, int64_t ldd,
+                            float* partials, unsigned* flags, unsigned seq);
 
 // Exact 8-bit integer GEMM on the tcgen05 BF16 pipe.  `workspace` holds
 // gemm_i8_tc_workspace_bytes(M, N, K) bytes of device scratch for the BF16
