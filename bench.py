@@ -248,6 +248,53 @@ def workload_meta(name):
     return w
 
 
+# Issue-rate probes of this run (measure_probes): name -> record.
+_PROBES: dict = {}
+# (name, kind code of mma_peak_probe, unit, largest iteration count)
+PROBE_KINDS = (("tc_f16", 1, "TFLOP/s", 1 << 21),
+               ("dmma_f64", 2, "TFLOP/s", 1 << 40),
+               ("imma_s8", 3, "TOP/s", 1 << 40),
+               ("dfma_f64", 4, "TFLOP/s", 1 << 40))
+
+
+def measure_probes(torch, target_ms=20.0, reps=3):
+    """Per-pipe issue-rate probes (mma_peak_probe: every SM issues
+    independent back-to-back instructions of one kind): operations per
+    launch / CUDA-event launch time, best and median of `reps` launches of
+    about `target_ms`.  Fills _PROBES and returns it."""
+    from mixed_precision_dense_02_gb300 import binding
+    stream = torch.cuda.current_stream()
+
+    def launch(kind, n):
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        st, ops = binding.mma_peak_probe(kind, n, stream.cuda_stream)
+        ev1.record(stream)
+        ev1.synchronize()
+        if st != 0:
+            raise RuntimeError(f"mma_peak_probe({kind}) returned {binding.STATUS.get(st, st)}")
+        return ev0.elapsed_time(ev1), ops
+
+    for name, kind, unit, cap in PROBE_KINDS:
+        n = 16
+        ms, _ = launch(kind, n)
+        while ms < 2.0 and n < cap:
+            n = min(cap, n * 8)
+            ms, _ = launch(kind, n)
+        n = int(min(cap, max(1, n * target_ms / max(ms, 1e-3))))
+        times, ops = [], 0.0
+        for _ in range(reps):
+            ms, ops = launch(kind, n)
+            times.append(ms)
+        best = min(times)
+        _PROBES[name] = {"rate": ops / (best * 1e-3) / 1e12, "unit": unit,
+                         "rate_median": ops / (statistics.median(times) * 1e-3) / 1e12,
+                         "iterations": n, "ms_best": best, "ops_per_launch": ops}
+    binding.device_status()
+    return _PROBES
+
+
 def roofline_bound(name, w):
     """(bound, unit, peak, peak_note) of the workload's dominant kernel."""
     peaks, src = load_peaks()
@@ -259,6 +306,10 @@ def roofline_bound(name, w):
     if w["kind"] == "batched" or "skinny" in name:
         return "hbm", "GB/s", peaks["hbm_gbs"], f"hbm_gbs of {src}"
     if w["dtype_in"] == "f64":
+        if "dmma_f64" in _PROBES:
+            p = _PROBES["dmma_f64"]["rate"]
+            return ("tensor", "TFLOP/s", p, "measured DMMA issue-rate probe in this "
+                    f"run (mma_peak_probe, m8n8k4 FP64 on every SM): {p:.3f} TFLOP/s")
         p = peaks["bf16_tflops"] * NOMINAL_FP64_TFLOPS / NOMINAL_BF16_TFLOPS
         return "tensor", "TFLOP/s", p, f"bf16_tflops of {src} x nominal fp64/bf16 (1.25/2250)"
     return "tensor", "TFLOP/s", peaks["bf16_tflops"], f"bf16_tflops (burst) of {src}"
@@ -641,14 +692,20 @@ def run_reference(args, dist):
 def add_nominal(roof, sms, clk):
     """Context denominators beside the measured peak (frac stays against the
     measured one): for the BF16 tensor pipe SMs x 8192 flop/clk x the
-    maximum SM clock and x the median SM clock of the timed region; for HBM
-    the nominal HBM3e bandwidth.  FP64 (DMMA pipe) gets none."""
+    maximum SM clock and x the median SM clock of the row's own timed
+    region, and the tcgen05 issue-rate probe of this run; for HBM the
+    nominal HBM3e bandwidth.  FP64 (DMMA pipe, against its own probe) gets
+    none."""
+    roof["sm_mhz_run"] = clk.get("sm_mhz")
     if roof["unit"] == "GB/s":
         roof["nominal_peak"] = NOMINAL_HBM_GBS
         roof["frac_of_nominal"] = roof["achieved"] / NOMINAL_HBM_GBS
         return
-    if "fp64" in roof.get("peak_note", roof.get("peak_source", "")):
+    if "DMMA" in roof.get("peak_source", "") or "fp64" in roof.get("peak_source", ""):
         return
+    if "tc_f16" in _PROBES:
+        roof["probe_peak"] = _PROBES["tc_f16"]["rate"]
+        roof["frac_of_probe"] = roof["achieved"] / _PROBES["tc_f16"]["rate"]
     mx, med = clk.get("sm_max_mhz"), clk.get("sm_mhz")
     if mx:
         roof["nominal_peak_max_clock"] = sms * BF16_FLOP_PER_SM_CLK * mx * 1e6 / 1e12
@@ -685,6 +742,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--peaks", action="store_true",
+                    help="run only the per-pipe issue-rate probes and print them")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -705,9 +764,21 @@ def main(argv=None):
     clocks = ClockSampler(dist.local_rank)
     clocks.start()
     time.sleep(0.5)
+    # per-pipe issue-rate probes (a second or so): the FP64 row's peak and
+    # context for the tensor rows
+    t0p = time.time()
+    probes = measure_probes(torch)
+    probe_clk = clocks.summary(t0p, time.time())
+    if args.peaks:
+        clocks.stop()
+        if dist.rank == 0:
+            print(json.dumps({"probes": probes, "clocks": probe_clk,
+                              "n_sms": torch.cuda.get_device_properties(
+                                  dist.local_rank).multi_processor_count}), flush=True)
+        dist.close()
+        return 0
     res = measure_workload(torch, dist, args.workload, args.steps, args.warmup,
                            with_e2e=True, sustain_s=2.0)
-    clocks.stop()
     clk = clocks.summary(*res["host_window"])
     sms = torch.cuda.get_device_properties(dist.local_rank).multi_processor_count
 
@@ -719,9 +790,11 @@ def main(argv=None):
                 continue
             wm = workload_meta(name)
             k = 3 if wm["dtype_in"] == "f64" else max(3, min(args.steps, 20))
-            r = measure_workload(torch, dist, name, k, 3, with_e2e=False)
-            # (the clock record covers the headline's timed region only)
-            add_nominal(r["roofline"], sms, {"sm_max_mhz": clk.get("sm_max_mhz")})
+            r = measure_workload(torch, dist, name, k, 3, with_e2e=False,
+                                 sustain_s=1.0)
+            # the row's own clock record (its timed region, extended to a
+            # second of the same loop)
+            add_nominal(r["roofline"], sms, clocks.summary(*r["host_window"]))
             per_dtype[name] = {"value": r["value"], "unit": r["unit"],
                                "ms_per_step": r["ms_per_step"], "steps": k,
                                "pct_of_bf16_peak": r["pct_of_bf16_peak"],
@@ -731,6 +804,7 @@ def main(argv=None):
                 # the oracle beside each row, on a short bounded sample
                 per_dtype[name]["cpu_baseline"] = cpu_baseline(name, target_s=2.0)
                 _INPUT_CACHE.pop(name, None)
+    clocks.stop()
     add_nominal(res["roofline"], sms, clk)
 
     cpu = None
@@ -747,8 +821,16 @@ def main(argv=None):
             "config": _config(args.workload, w, res["l2"]),
             "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
             "clocks": clk, "gpu_launches": res["gpu_launches"],
+            "probes": dict(probes, clocks=probe_clk),
             "per_dtype": per_dtype,
         }
+        # a compact copy of every row last, so that a reader keeping only the
+        # end of the line still sees all of them: value, unit, roofline
+        # fraction (of the measured peak), mean kernel time in us
+        line["per_dtype_summary"] = {
+            name: [round(r["value"], 2), r["unit"], round(r["roofline"]["frac"], 3),
+                   round(r["roofline"]["kernel_ms_mean"] * 1e3, 2)]
+            for name, r in per_dtype.items()}
         print(json.dumps(line), flush=True)
     dist.close()
     return 0

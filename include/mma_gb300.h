@@ -49,7 +49,11 @@
  * (M + N) * roundup(K, 8) * 2 bytes, plus (M + N) * 8 bytes of correction
  * terms; batched INT8 products widen every tile, batch * (M + N) *
  * roundup(K, 8) * 2 bytes; FP16/BF16 products with row-major B transpose
- * B, N * roundup(K, 8) * 2 bytes.  That buffer is allocated once
+ * B, N * roundup(K, 8) * 2 bytes; FP16/BF16 -> FP32 products with
+ * column-major B and fewer 128 x 128 output tiles than SMs (and at least
+ * eight 64-deep K steps per tile) split K over every SM and meet in it,
+ * SMs * 64 KiB, plus a hand-off flag buffer of SMs * 32 bytes allocated
+ * (and zeroed) once per device.  That buffer is allocated once
  * per device by the first such call, grown (cudaMalloc, after the previous
  * user finishes) only when a larger problem arrives, and kept until the
  * process exits; calls on different streams are ordered on it by an event.
@@ -268,6 +272,61 @@ mma_status_t mma_device_status(void *stream);
  * range, MMA_ERR_NO_DEVICE without a device, else MMA_OK.
  */
 mma_status_t mma_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+/*
+ * mma_selftest_gemm_abort -- exercise the tcgen05 GEMM kernel's own abort
+ * path without faulting or hanging the GPU.  The pages have no counterpart;
+ * it backs the bounded-wait contract of the GEMM kernels with a test.
+ *
+ * Enqueues on `stream` the BF16 -> FP32 GEMM kernel for a 256 x 256 x 256
+ * product on single CTAs (cluster = 1) or on a CTA pair sharing one MMA
+ * (cluster = 2), with its operand producer told to issue no loads and every
+ * pipeline wait limited to limit_ns (10^6 .. 10^10 ns).  The MMA issuer's
+ * first stage wait therefore runs out with nothing in flight; the kernel
+ * raises its abort flag, records MMA_ERR_TIMEOUT in the device status word,
+ * drains, frees its tensor memory and exits, so the context stays usable.
+ * A and B (256 x 256 BF16) and D (256 x 256 FP32) are caller device
+ * buffers, 16-byte aligned; nothing reads or writes them.  Returns
+ * MMA_ERR_INVALID_ARG (bad cluster, limit or NULL buffer),
+ * MMA_ERR_MISALIGNED, MMA_ERR_NO_DEVICE or the launch status; a following
+ * mma_device_status(stream) returns MMA_ERR_TIMEOUT once.
+ */
+mma_status_t mma_selftest_gemm_abort(int cluster, int64_t limit_ns,
+                                     const void *A, const void *B, void *D,
+                                     void *stream);
+
+/*
+ * mma_peak_probe -- enqueue one issue-rate probe of a compute pipe on every
+ * SM of the current device and report the operations it performs.
+ *
+ * Passage: "CDNA2 dense MFMA builtins", section "Instruction throughput":
+ * peak throughput = operations per instruction / cycles per instruction x
+ * clock.  The probe measures that rate instead of deriving it: every SM
+ * issues `iterations` rounds of independent back-to-back instructions of
+ * one kind on register or shared-memory operands (no DRAM traffic), so
+ * *ops_per_launch (written before the launch) divided by the launch's
+ * duration (CUDA events around the call, on `stream`) is the pipe's rate
+ * at the clock the launch ran at.  Kinds:
+ *   MMA_PEAK_TC_F16  tcgen05.mma kind::f16, BF16 in, FP32 accumulate
+ *                    (M = 128, N = 256, K = 16; the FP16/BF16 and exact
+ *                    INT8 GEMMs' pipe); iterations <= 2^21
+ *   MMA_PEAK_DMMA    mma.sync m8n8k4 FP64 (the FP64 GEMM's instruction)
+ *   MMA_PEAK_IMMA    mma.sync m16n8k32 int8 -> int32 (small INT8 products)
+ *   MMA_PEAK_DFMA    scalar FP64 fused multiply-add
+ * One operation is one multiply or one add (a multiply-add counts 2).
+ * Returns MMA_ERR_INVALID_ARG for an unknown kind, iterations < 1 or above
+ * the kind's limit (2^40 for the warp-level kinds), or a NULL
+ * ops_per_launch; MMA_ERR_NO_DEVICE without a device; else the launch
+ * status.  Recorded by mma_profile_begin like the GEMM calls.
+ */
+typedef enum {
+  MMA_PEAK_TC_F16 = 1,
+  MMA_PEAK_DMMA = 2,
+  MMA_PEAK_IMMA = 3,
+  MMA_PEAK_DFMA = 4
+} mma_peak_kind_t;
+mma_status_t mma_peak_probe(int kind, int64_t iterations,
+                            double *ops_per_launch, void *stream);
 
 /*
  * mma_profile_begin / mma_profile_end -- per-launch timing of the dominant

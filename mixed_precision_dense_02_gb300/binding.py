@@ -40,6 +40,8 @@ SIGNATURES = {
                                    _i64, _p, _i64, _p]),
     "mma_device_status": (_int, [_p]),
     "mma_selftest_wait_timeout": (_int, [_i64, _p]),
+    "mma_selftest_gemm_abort": (_int, [_int, _i64, _p, _p, _p, _p]),
+    "mma_peak_probe": (_int, [_int, _i64, ctypes.POINTER(ctypes.c_double), _p]),
     "mma_profile_begin": (_int, []),
     "mma_profile_end": (_int, [ctypes.POINTER(ctypes.c_float), _int,
                                ctypes.POINTER(_int)]),
@@ -138,6 +140,23 @@ def mma_selftest_wait_timeout(limit_ns, stream) -> int:
     """Run one bounded wait that is made to run out (failure-detection
     self-test); mma_device_status then reports MMA_ERR_TIMEOUT once."""
     return load().mma_selftest_wait_timeout(limit_ns, stream)
+
+
+MMA_PEAK_TC_F16, MMA_PEAK_DMMA, MMA_PEAK_IMMA, MMA_PEAK_DFMA = 1, 2, 3, 4
+
+
+def mma_peak_probe(kind, iterations, stream) -> tuple:
+    """Enqueue one issue-rate probe; returns (status, operations per launch)."""
+    ops = ctypes.c_double(0.0)
+    st = load().mma_peak_probe(kind, iterations, ctypes.byref(ops), stream)
+    return st, ops.value
+
+
+def mma_selftest_gemm_abort(cluster, limit_ns, A, B, D, stream) -> int:
+    """Run the tcgen05 GEMM kernel with no operand loads and waits limited to
+    limit_ns, so its own abort path runs; mma_device_status then reports
+    MMA_ERR_TIMEOUT once."""
+    return load().mma_selftest_gemm_abort(cluster, limit_ns, A, B, D, stream)
 
 
 def mma_status_string(status: int) -> str:

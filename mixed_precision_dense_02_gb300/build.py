@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmma_gb300.so")
 SOURCES = ["api.cu", "gemm_tc.cu", "gemm_i8.cu", "gemm_f64.cu", "batched16.cu",
            "noalloc.cu", "selftest.cu", "batched_mma.cu",
-           "batched_tile.cu"]
+           "batched_tile.cu", "gemm_sk.cu", "peaks.cu"]
 HEADERS = ["ptx.cuh", "kernels.h"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = GENCODE + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler",

@@ -55,6 +55,17 @@ struct Workspace {
 Workspace g_ws[kMaxDevices];
 std::mutex g_ws_mu;
 
+// Stream-K hand-off flags: one small buffer per device (zeroed when
+// allocated) and the sequence number of the last stream-K call; calls use
+// the flags in the order the scratch buffer's event imposes on them.
+struct StreamKFlags {
+  unsigned* ptr = nullptr;
+  size_t count = 0;
+  unsigned seq = 0;
+  uint64_t gen = 0;
+};
+StreamKFlags g_skf[kMaxDevices];
+
 // Identifier of the calling thread's current CUDA context plus one (0 when
 // no context is current yet).  Without the driver's context-id call every
 // context reads as 1, and state is then set up once per device.
@@ -246,6 +257,47 @@ mma_status_t with_workspace(const Ctx& ctx, size_t need, F&& enqueue) {
 
 namespace {
 
+// Enqueue a stream-K GEMM: partial sums in the scratch buffer, hand-off
+// flags with a fresh sequence number.  Runs under the scratch buffer's lock
+// (inside with_workspace), which also orders the flags' users.
+mma_status_t enqueue_stream_k(const Ctx& ctx, bool bf16, int64_t M, int64_t N,
+                              int64_t K, const void* A, int64_t lda,
+                              const void* B, int64_t ldb, const void* C,
+                              int64_t ldc, void* D, int64_t ldd, void* ws) {
+  StreamKFlags& f = g_skf[ctx.device];
+  if (f.gen != ctx.gen) f = StreamKFlags{};  // set up in a replaced context
+  const size_t need = gemm_sk_flag_count(ctx.num_sms);
+  if (f.ptr == nullptr || f.count < need) {
+    if (f.ptr) cudaFree(f.ptr);
+    f = StreamKFlags{};
+    void* p = nullptr;
+    if (cudaMalloc(&p, need * sizeof(unsigned)) != cudaSuccess) {
+      cudaGetLastError();
+      return MMA_ERR_NO_MEMORY;
+    }
+    if (cudaMemset(p, 0, need * sizeof(unsigned)) != cudaSuccess) {
+      cudaFree(p);
+      cudaGetLastError();
+      return MMA_ERR_LAUNCH;
+    }
+    f.ptr = static_cast<unsigned*>(p);
+    f.count = need;
+    f.gen = ctx.gen;
+  }
+  // nonzero and different from every value still in the flags; after 2^32
+  // calls the flags are cleared again before the numbers repeat
+  if (++f.seq == 0) {
+    if (cudaMemsetAsync(f.ptr, 0, f.count * sizeof(unsigned), ctx.stream) !=
+        cudaSuccess)
+      return MMA_ERR_LAUNCH;
+    f.seq = 1;
+  }
+  return launch_gemm_sk(ctx, bf16, M, N, K, A, lda, B, ldb,
+                        static_cast<const float*>(C), ldc,
+                        static_cast<float*>(D), ldd, static_cast<float*>(ws),
+                        f.ptr, f.seq);
+}
+
 // Element sizes of a supported (dtype_in, dtype_acc) pair, or false.
 bool pair_sizes(int in, int acc, int64_t* in_b, int64_t* acc_b) {
   if ((in == MMA_F16 || in == MMA_BF16) && acc == MMA_F32) {
@@ -327,6 +379,14 @@ extern "C" mma_status_t mma_gemm_ex(int dtype_in, int dtype_acc, int64_t M,
     case MMA_BF16: {
       const bool bf16 = dtype_in == MMA_BF16;
       const bool out16 = dtype_acc != MMA_F32;
+      // fewer output tiles than SMs: K split across every SM (stream-K)
+      if (!b_row && !out16 && gemm_sk_fits(ctx.num_sms, M, N, K))
+        return with_workspace(ctx, gemm_sk_workspace_bytes(ctx.num_sms),
+                              [&](void* ws) {
+                                return enqueue_stream_k(ctx, bf16, M, N, K, A,
+                                                        lda, B, ldb, C, ldc, D,
+                                                        ldd, ws);
+                              });
       if (!b_row)
         return launch_gemm_tc_f16(ctx, bf16, out16, M, N, K, A, lda, B, ldb, C,
                                   ldc, D, ldd);

@@ -1,0 +1,450 @@
+// tcgen05 GEMM for problems with fewer output tiles than SMs (a tall,
+// narrow D such as 16384 x 128 with deep K): D = A * B + C, FP16/BF16
+// inputs, FP32 accumulation, A row-major, B column-major, C/D FP32
+// row-major.
+//
+// The K loop of each tile is the caller loop of "CDNA2 dense MFMA
+// builtins", section "Naming convention" (each step adds one K panel's
+// contribution to the M x N tile).  Here that loop is cut across CTAs so
+// that every SM streams operands: the tiles' K steps form one sequence of
+// tiles * ceil(K / 64) steps, and CTA c of G takes the contiguous range
+// [c * total / G, (c + 1) * total / G) of it ("stream-K").  A range is cut
+// at tile boundaries into pieces; a tile is finished by the CTA holding its
+// first piece (the one that starts at K step 0):
+//   * a piece that does not start at step 0 is always the first piece of
+//     its CTA; its FP32 partial sums go to a scratch slot of that CTA,
+//     followed by a release flag (the call's sequence number), and the CTA
+//     never waits before writing it;
+//   * the tile's first piece is its CTA's last piece; that CTA holds its C
+//     in registers (requested while the piece's MMAs run), waits for the
+//     other pieces' flags (acquire), adds ((acc_first + C) + partial_2) +
+//     partial_3 ..., in that fixed order, one FP32 rounding per addition,
+//     and stores D.
+// The waits only point from a CTA to higher-numbered CTAs, which write
+// their partials before waiting on anything, so no cycle of waits exists;
+// the sum order depends only on M, N, K and G, so results are identical
+// from run to run.  Every wait is bounded (MMA_ERR_TIMEOUT on expiry).
+//
+// Roles (320 threads): warp 0 TMA producer (128 x 64 A and B boxes,
+// 128-byte swizzle, STAGES-deep ring), warp 1 tcgen05.mma issuer (M = 128,
+// N = 128, K = 16) into a double-buffered FP32 accumulator in tensor
+// memory, warps 2..9 epilogue (two per tensor-memory lane quarter, 64
+// columns each): each thread owns one row of its warp's columns.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mmagb {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 64;
+constexpr int kUK = 16;
+constexpr int kEpi = 8;                     // epilogue warps
+constexpr int kThreadsSK = 64 + 32 * kEpi;  // 320
+constexpr int kHalf = kBN / 2;              // columns per epilogue warp
+constexpr int kBlk = kHalf / 16;            // 16-column blocks per warp
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kStageBytes = kABytes + kBN * kBK * 2;
+constexpr int kBarOffset = kStages * kStageBytes;
+constexpr int kSmemBytes = kBarOffset + (2 * kStages + 5) * 8 + 16 + 1024;
+// FP32 partial sums of one CTA's piece: 128 x 128
+constexpr int kSlotFloats = kBM * kBN;
+
+// First K step (of the whole sequence) of CTA c's range.
+__host__ __device__ __forceinline__ int64_t range_begin(int64_t c,
+                                                        int64_t total,
+                                                        int64_t grid) {
+  return c * total / grid;
+}
+
+// The CTA whose range holds step x.
+__device__ __forceinline__ int64_t owner_of(int64_t x, int64_t total,
+                                            int64_t grid) {
+  int64_t c = x * grid / total;
+  while (c + 1 < grid && range_begin(c + 1, total, grid) <= x) ++c;
+  while (c > 0 && range_begin(c, total, grid) > x) --c;
+  return c;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *flag == seq (bounded like mbar_wait: on expiry raise the
+// CTA's abort flag and record MMA_ERR_TIMEOUT).
+__device__ __forceinline__ bool wait_flag(const unsigned* flag, unsigned seq,
+                                          volatile int* abort_flag,
+                                          unsigned* status) {
+  if (ld_acquire_u32(flag) == seq) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_u32(flag) == seq) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Piece of CTA c's range starting at step s: tile t, K steps [k0, k1).
+struct Piece {
+  int t, k0, k1;
+};
+
+__device__ __forceinline__ Piece piece_at(int64_t s, int64_t end, int nk) {
+  Piece p;
+  p.t = int(s / nk);
+  p.k0 = int(s - int64_t(p.t) * nk);
+  const int64_t room = end - s;
+  p.k1 = room < int64_t(nk - p.k0) ? p.k0 + int(room) : nk;
+  return p;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreadsSK, 1)
+    gemm_sk_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB,
+                   const float* C, int64_t ldc, float* D, int64_t ldd, int M,
+                   int N, int K, float* __restrict__ partials,
+                   unsigned* __restrict__ flags, unsigned seq,
+                   unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int num_m = (M + kBM - 1) / kBM;
+  const int nk = (K + kBK - 1) / kBK;
+  const int64_t tiles = int64_t(num_m) * ((N + kBN - 1) / kBN);
+  const int64_t total = tiles * nk;
+  const int64_t grid = gridDim.x;
+  const int64_t cta = blockIdx.x;
+  const int64_t beg = range_begin(cta, total, grid);
+  const int64_t end = range_begin(cta + 1, total, grid);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpi);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * kBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int64_t s = beg; s < end && ok;) {
+        const Piece p = piece_at(s, end, nk);
+        const int mb = p.t % num_m, nb = p.t / num_m;
+        for (int kb = p.k0; kb < p.k1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_3d(&tmA, &full[stage], sa, kb * kBK, mb * kBM, 0);
+          tma_load_3d(&tmB, &full[stage], sa + kABytes, kb * kBK, nb * kBN, 0);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        s += p.k1 - p.k0;
+      }
+      // on abort, let every load still in flight land before exiting
+      if (!ok) {
+        for (int st = 0; st < kStages; ++st) {
+          const uint32_t fills =
+              issued / kStages + (uint32_t(st) < issued % kStages);
+          if (!fills) continue;
+          const uint32_t a = smem_u32(&full[st]);
+          const unsigned long long t0 = global_timer_ns();
+          while (!mbar_try_wait(a, (fills - 1) & 1u))
+            if (global_timer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_f16_f32(BF16, kBM, kBN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t s = beg; s < end && ok;) {
+        const Piece p = piece_at(s, end, nk);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * kBN);
+        for (int kb = p.k0; kb < p.k1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint64_t da = sw128_kmajor_desc(sa);
+          const uint64_t db = sw128_kmajor_desc(sa + kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUK; ++k)
+            umma_f16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc,
+                     (kb != p.k0 || k != 0) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        s += p.k1 - p.k0;
+      }
+      umma_commit(done);
+      const uint32_t a = smem_u32(done);
+      const unsigned long long t0 = global_timer_ns();
+      while (!mbar_try_wait(a, 0))
+        if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int ew = warp - 2;   // 0 .. 7
+    const int q = warp & 3;    // tensor-memory lane quarter
+    const int h = ew >> 2;     // column half
+    const int lane = threadIdx.x & 31;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int64_t s = beg; s < end && ok;) {
+      const Piece p = piece_at(s, end, nk);
+      const int mb = p.t % num_m, nb = p.t / num_m;
+      const int row = mb * kBM + q * 32 + lane;
+      const int col0 = nb * kBN + h * kHalf;
+      const bool head = p.k0 == 0;
+      const bool whole = head && p.k1 == nk;
+      // The tile's other pieces (only for a first piece that is not the
+      // whole tile): CTAs cta + 1 .. last, each holding it as its first.
+      int64_t last = cta;
+      if (head && !whole) last = owner_of(int64_t(p.t) * nk + nk - 1, total, grid);
+      // A first piece adds C: this thread's 64 values of it are requested
+      // now, while the piece's MMAs run, and held in registers.
+      float v[kHalf];
+      if (head) {
+        const bool live = C != nullptr && row < M;
+        const float* crow = live ? C + int64_t(row) * ldc : nullptr;
+#pragma unroll
+        for (int c = 0; c < kHalf / 4; ++c) {
+          const int cc = col0 + 4 * c;
+          float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (live && cc + 4 <= N) {
+            w = *reinterpret_cast<const float4*>(crow + cc);
+          } else if (live) {
+            if (cc < N) w.x = crow[cc];
+            if (cc + 1 < N) w.y = crow[cc + 1];
+            if (cc + 2 < N) w.z = crow[cc + 2];
+          }
+          v[4 * c] = w.x;
+          v[4 * c + 1] = w.y;
+          v[4 * c + 2] = w.z;
+          v[4 * c + 3] = w.w;
+        }
+      }
+      ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + uint32_t(acc * kBN + h * kHalf) + (uint32_t(q * 32) << 16);
+      if (!head) {
+        // partial sums to this CTA's slot, laid out so that each warp-wide
+        // 16-byte store covers 512 contiguous bytes
+        float4* slot = reinterpret_cast<float4*>(partials) +
+                       (cta * kEpi + ew) * (kBlk * 4 * 32);
+#pragma unroll
+        for (int j = 0; j < kBlk; ++j) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            slot[(j * 4 + c) * 32 + lane] =
+                make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                            __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_u32(&flags[cta * kEpi + ew], seq);
+      } else {
+        // D = ((acc + C) + partial of cta + 1) + partial of cta + 2 ...: a
+        // fixed order, one FP32 rounding per addition
+#pragma unroll
+        for (int j = 0; j < kBlk; ++j) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[16 * j + e] += __uint_as_float(r[e]);
+        }
+        for (int64_t o = cta + 1; o <= last && ok; ++o) {
+          ok = wait_flag(&flags[o * kEpi + ew], seq, abort_flag, status);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          // every 16-byte piece of the partial in flight at once
+          const float4* slot = reinterpret_cast<const float4*>(partials) +
+                               (o * kEpi + ew) * (kBlk * 4 * 32);
+          float4 w[kHalf / 4];
+#pragma unroll
+          for (int c = 0; c < kHalf / 4; ++c) w[c] = __ldcg(&slot[c * 32 + lane]);
+#pragma unroll
+          for (int c = 0; c < kHalf / 4; ++c) {
+            v[4 * c] += w[c].x;
+            v[4 * c + 1] += w[c].y;
+            v[4 * c + 2] += w[c].z;
+            v[4 * c + 3] += w[c].w;
+          }
+        }
+        if (!ok) break;
+        if (row < M) {
+          float* drow = D + int64_t(row) * ldd;
+#pragma unroll
+          for (int c = 0; c < kHalf / 4; ++c) {
+            const int cc = col0 + 4 * c;
+            if (cc + 4 <= N) {
+              *reinterpret_cast<float4*>(drow + cc) =
+                  make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            } else {
+              for (int e = 0; e < 4 && cc + e < N; ++e) drow[cc + e] = v[4 * c + e];
+            }
+          }
+        }
+      }
+      // this warp's reads of the accumulator are done
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+      s += p.k1 - p.k0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * kBN);
+  }
+}
+
+}  // namespace
+
+// Stream-K applies to FP32-result products whose 128 x 128 tiles are fewer
+// than the SMs, with at least two K steps per CTA on average and at least
+// eight per tile (MMA_GB300_STREAMK=0 turns it off, =1 on wherever the
+// sizes allow it, for tuning).
+bool gemm_sk_fits(int num_sms, int64_t M, int64_t N, int64_t K) {
+  static const int forced = [] {
+    const char* e = getenv("MMA_GB300_STREAMK");
+    if (!e) return -1;
+    return e[0] == '0' ? 0 : 1;
+  }();
+  if (forced == 0 || M <= 0 || N <= 0 || K <= 0) return false;
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int64_t nk = (K + kBK - 1) / kBK;
+  if (tiles * nk >= (int64_t(1) << 31)) return false;
+  if (forced == 1) return tiles * nk >= 2 && tiles < (int64_t(1) << 31);
+  return 2 * tiles < num_sms && nk >= 8 && tiles * nk >= 2 * int64_t(num_sms);
+}
+
+size_t gemm_sk_workspace_bytes(int num_sms) {
+  return size_t(num_sms) * kSlotFloats * sizeof(float);
+}
+
+size_t gemm_sk_flag_count(int num_sms) { return size_t(num_sms) * kEpi; }
+
+mma_status_t launch_gemm_sk(const Ctx& ctx, bool bf16, int64_t M, int64_t N,
+                            int64_t K, const void* A, int64_t lda,
+                            const void* B, int64_t ldb, const float* C,
+                            int64_t ldc, float* D, int64_t ldd,
+                            float* partials, unsigned* flags, unsigned seq) {
+  CUtensorMap ta, tb;
+  if (!make_kmajor_map(&ta, A, K, M, lda, kBM, bf16) ||
+      !make_kmajor_map(&tb, B, K, N, ldb, kBN, bf16))
+    return MMA_ERR_LAUNCH;
+  auto kern = bf16 ? gemm_sk_kernel<true> : gemm_sk_kernel<false>;
+  static PerContext<bool> smem_attr[2];
+  bool attr_ok = false;
+  if (!smem_attr[bf16 ? 1 : 0].get(ctx, &attr_ok, [&](bool* v) {
+        *v = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSmemBytes) == cudaSuccess;
+        if (!*v) cudaGetLastError();
+        return *v;
+      }))
+    return MMA_ERR_LAUNCH;
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int64_t total = tiles * ((K + kBK - 1) / kBK);
+  int64_t grid = ctx.num_sms;
+  if (grid > total) grid = total;
+  ctx.mark_start();
+  kern<<<unsigned(grid), kThreadsSK, kSmemBytes, ctx.stream>>>(
+      ta, tb, C, ldc, D, ldd, int(M), int(N), int(K), partials, flags, seq,
+      ctx.status);
+  ctx.mark_stop();
+  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}
+
+}  // namespace mmagb

@@ -137,6 +137,17 @@ __device__ __forceinline__ int blgp_source(int p, int q) {
   return p - 4;
 }
 
+// Failure-detection self-test hook, set only by the library's self-test
+// entry point (every GEMM call passes {kWaitLimitNs, 0}): the limit of the
+// kernel's bounded waits, and whether the producer issues no operand loads
+// at all, so that the MMA issuer's first stage wait runs out with nothing
+// in flight and the abort path (flag, drain, tensor-memory release, exit)
+// runs for real.
+struct TestHook {
+  unsigned long long wait_limit_ns;
+  int skip_loads;
+};
+
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n,
                                             int& mb, int& nb) {
   const int per_group = kGroupM * num_n;
@@ -205,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    void* __restrict__ Dv, int64_t ldd, int M, int N, int K,
                    int kb_per_chunk, BatchArgs bat,
                    const int64_t* __restrict__ row_term,
-                   const int64_t* __restrict__ col_term, unsigned* status) {
+                   const int64_t* __restrict__ col_term, unsigned* status,
+                   const TestHook hook) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   constexpr int HALF = BN / 2;  // columns per epilogue warp
   static_assert(EPI != Epi::I32SAT || BN == 128, "I32SAT uses 128-wide tiles");
@@ -308,12 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode(u, mu, nb, za, zb, zc);
         const int mb = mu * CL + rank;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status, hook.wait_limit_ns)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + stage * L::STAGE_BYTES;
-          if constexpr (CL == 1) {
+          if (hook.skip_loads) {
+            // self-test: no load, so the stage never fills
+          } else if constexpr (CL == 1) {
             mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
             tma_load_3d(&tmA, &full[stage], sa, kb * BK, mb * BM, za);
             tma_load_3d(&tmB, &full[stage], sa + L::A_BYTES, kb * BK, nb * BN,
@@ -327,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d_pair(&tmB, fb, sa + L::A_BYTES, kb * BK,
                              nb * BN + rank * (BN / CL), zb);
           }
-          ++issued;
+          if (!hook.skip_loads) ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -360,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = first_unit; u < units && ok; u += unit_step) {
         for (int ch = 0; ch < chunks && ok; ++ch) {
-          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) {
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, status, hook.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -369,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb0 = ch * kpc;
           const int kb1 = min(num_kb, kb0 + kpc);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, status)) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, status, hook.wait_limit_ns)) {
               ok = false;
               break;
             }
@@ -653,8 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // sums (the step number selects registers through an unrolled
         // match, so iacc stays in registers).
         [[maybe_unused]] auto early_c_finish = [&]() -> bool {
-          bool okc = mbar_wait(&wbar[0], cpar, abort_flag, status) &&
-                     mbar_wait(&wbar[1], cpar, abort_flag, status);
+          bool okc = mbar_wait(&wbar[0], cpar, abort_flag, status, hook.wait_limit_ns) &&
+                     mbar_wait(&wbar[1], cpar, abort_flag, status, hook.wait_limit_ns);
           if (!__all_sync(0xffffffffu, okc)) return false;
 #pragma unroll
           for (int m = 0; m < NMP; ++m) {
@@ -682,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (has_c) early_c_issue(mp_issued++, row0, colh, zc);
         }
         for (int ch = 0; ch < chunks; ++ch) {
-          ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
+          ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status, hook.wait_limit_ns);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -729,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
       } else {
-        ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
+        ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status, hook.wait_limit_ns);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         taddr = tmem_base + uint32_t(acc * BN + h * HALF) +
@@ -770,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == NBLK - 1) release_acc(acc);
         }
         if (has_c && !kEarlyC) {
-          ok = mbar_wait(&wbar[g % NSTG], (g / NSTG) & 1u, abort_flag, status);
+          ok = mbar_wait(&wbar[g % NSTG], (g / NSTG) & 1u, abort_flag, status, hook.wait_limit_ns);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -996,6 +1010,11 @@ __global__ void __launch_bounds__(kRowThreads)
   const int64_t warp0 =
       (int64_t(blockIdx.x) * kRowThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kRowThreads) >> 5;
+  // as in i8_to_bf16_kernel: the 8-bit inputs are read once (evict first),
+  // the widened operands are read back by the GEMM next (evict last)
+  uint64_t pol_first, pol_last;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_first));
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_last));
   for (int64_t base = warp0 * rows_per_warp; base < rows;
        base += nwarps * rows_per_warp) {
     const int64_t r = base + lane / G;
@@ -1013,7 +1032,9 @@ __global__ void __launch_bounds__(kRowThreads)
           const int64_t c = c0 + int64_t(u) * G;
           v[u] = make_int4(0, 0, 0, 0);
           if (c < cpr && c * 16 + 16 <= K)
-            v[u] = __ldcs(reinterpret_cast<const int4*>(src + c * 16));
+            asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.s32 {%0, %1, %2, %3}, [%4], %5;"
+                         : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                         : "l"(src + c * 16), "l"(pol_first));
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -1024,8 +1045,10 @@ __global__ void __launch_bounds__(kRowThreads)
             flip4(v[u], flip, w);
             uint4 o0, o1;
             u8x16_to_bf16(w, o0, o1);
-            reinterpret_cast<uint4*>(dst + c * 16)[0] = o0;
-            reinterpret_cast<uint4*>(dst + c * 16)[1] = o1;
+            asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+                         :: "l"(dst + c * 16), "r"(o0.x), "r"(o0.y), "r"(o0.z), "r"(o0.w), "l"(pol_last) : "memory");
+            asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+                         :: "l"(dst + c * 16 + 8), "r"(o1.x), "r"(o1.y), "r"(o1.z), "r"(o1.w), "l"(pol_last) : "memory");
             // the 16 bytes' unsigned sum, four at a time
             const unsigned ones = 0x01010101u;
             s += __dp4a(w[0], ones, __dp4a(w[1], ones,
@@ -1129,7 +1152,8 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd,
                  int kb_per_chunk, BatchArgs bat, const int64_t* row_term,
-                 const int64_t* col_term) {
+                 const int64_t* col_term,
+                 TestHook hook = TestHook{kWaitLimitNs, 0}) {
   using L = Layout<BN, STAGES, CL, NSTG>;
   static_assert(L::ALLOC <= 232448, "shared memory per CTA");
   const CUtensorMapDataType cd_type =
@@ -1210,7 +1234,7 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, td, C, ldc, D, ldd, int(M), int(N),
                          int(K), kb_per_chunk, bat, row_term, col_term,
-                         ctx.status);
+                         ctx.status, hook);
   ctx.mark_stop();
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -1655,6 +1679,21 @@ mma_status_t launch_gemm_i8_tc_batched(const Ctx& ctx, int64_t M, int64_t N,
                                        tile_n(ctx, M, N, batch, cl, true), cl,
                                        M, N, K, W, ldw, Bw, ldw, C, ldc, D, ldd,
                                        nullptr, nullptr, bat);
+}
+
+mma_status_t launch_gemm_tc_abort_selftest(const Ctx& ctx, int cluster,
+                                           int64_t limit_ns, const void* A,
+                                           const void* B, void* D) {
+  constexpr int64_t n = 256;
+  const TestHook hook{static_cast<unsigned long long>(limit_ns), 1};
+  const BatchArgs one{1, 1, 0, 0};
+  if (cluster == 2)
+    return run<128, 6, true, Epi::F32, 2, 4>(ctx, false, n, n, n, A, n, B, n,
+                                             nullptr, 0, D, n, kI8ChunkK / BK,
+                                             one, nullptr, nullptr, hook);
+  return run<128, 5, true, Epi::F32, 1, 4>(ctx, false, n, n, n, A, n, B, n,
+                                           nullptr, 0, D, n, kI8ChunkK / BK,
+                                           one, nullptr, nullptr, hook);
 }
 
 }  // namespace mmagb

@@ -166,6 +166,15 @@ mma_status_t launch_batched16(const Ctx& ctx, bool bf16, int64_t batch,
                               int group, int abid, int blgp, const void* A,
                               const void* B, const float* C, float* D);
 
+// Failure-detection self-test of the tcgen05 GEMM itself: a 256 x 256 x
+// 256 BF16 product on single CTAs (cluster 1) or a CTA pair (cluster 2)
+// whose producer issues no loads and whose bounded waits give up after
+// limit_ns, so the real abort path runs (A, B, D: caller buffers of that
+// size, never read or written).
+mma_status_t launch_gemm_tc_abort_selftest(const Ctx& ctx, int cluster,
+                                           int64_t limit_ns, const void* A,
+                                           const void* B, void* D);
+
 // Launch context for the current device (false if it is not a usable
 // sm_103 device).
 bool current_ctx(void* stream, Ctx* out);

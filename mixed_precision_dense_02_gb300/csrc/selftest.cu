@@ -1,5 +1,6 @@
-// mma_selftest_wait_timeout: the failure-detection path of the pipeline
-// kernels, exercised on purpose without faulting or hanging the GPU.
+// mma_selftest_wait_timeout, mma_selftest_gemm_abort: the failure-detection
+// path of the pipeline kernels, exercised on purpose without faulting or
+// hanging the GPU.
 //
 // Every wait of the tcgen05 pipeline (TMA stage, accumulator hand-off, C
 // block) is mbar_wait from ptx.cuh: bounded by a time limit, after which it
@@ -7,7 +8,12 @@
 // device status word and returns false, so the kernel drains and exits and
 // the context stays usable.  This kernel runs that same wait on an mbarrier
 // that no thread ever arrives on, with a short caller-chosen limit, so the
-// wait runs out exactly as a stuck pipeline's would.
+// wait runs out exactly as a stuck pipeline's would.  The second runs the
+// tcgen05 GEMM kernel itself, single CTAs or a CTA pair, with its producer
+// told to issue no loads and its waits limited to limit_ns: the MMA
+// issuer's first stage wait runs out with no copy or MMA in flight, and
+// the kernel's own abort path (abort flag, drain, tensor-memory release,
+// cluster exit) runs for real.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,4 +54,18 @@ extern "C" mma_status_t mma_selftest_wait_timeout(int64_t limit_ns,
   wait_timeout_kernel<<<1, 32, 0, ctx.stream>>>(
       ctx.status, static_cast<unsigned long long>(limit_ns));
   return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+}
+
+extern "C" mma_status_t mma_selftest_gemm_abort(int cluster, int64_t limit_ns,
+                                                const void* A, const void* B,
+                                                void* D, void* stream) {
+  if (cluster != 1 && cluster != 2) return MMA_ERR_INVALID_ARG;
+  if (limit_ns < 1000000 || limit_ns > 10000000000ll) return MMA_ERR_INVALID_ARG;
+  if (!A || !B || !D) return MMA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(D)) & 15u)
+    return MMA_ERR_MISALIGNED;
+  Ctx ctx{};
+  if (!current_ctx(stream, &ctx)) return MMA_ERR_NO_DEVICE;
+  return launch_gemm_tc_abort_selftest(ctx, cluster, limit_ns, A, B, D);
 }

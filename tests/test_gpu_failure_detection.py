@@ -89,3 +89,39 @@ def test_scratch_buffer_shared_by_two_streams(torch_cuda):
         for rep in range(3):
             got = outs[2 * rep + k].cpu().numpy()
             assert np.array_equal(got, want), (k, rep)
+
+
+@pytest.mark.parametrize("cluster", [1, 2])
+def test_gemm_kernel_abort_path(torch_cuda, cluster):
+    """The tcgen05 GEMM kernel itself, on single CTAs and on a CTA pair, with
+    its producer issuing no loads and its waits limited to 50 ms: the call
+    returns, the kernel ends by itself, the timeout is reported exactly once,
+    its output buffer is untouched, and the tensor memory it held was freed:
+    the same kernel shapes then run twice more and match the oracle."""
+    torch = torch_cuda
+    stream = torch.cuda.current_stream().cuda_stream
+    assert binding.mma_device_status(stream) == MMA_OK
+    dev = torch.device("cuda:0")
+    A = torch.zeros((256, 256), dtype=torch.bfloat16, device=dev)
+    B = torch.zeros_like(A)
+    D = torch.full((256, 256), 7.0, dtype=torch.float32, device=dev)
+    for _ in range(2):
+        t0 = time.time()
+        assert binding.mma_selftest_gemm_abort(cluster, 50_000_000, A.data_ptr(),
+                                               B.data_ptr(), D.data_ptr(), stream) == MMA_OK
+        torch.cuda.synchronize()
+        assert time.time() - t0 < 10.0
+        assert binding.mma_device_status(stream) == MMA_ERR_TIMEOUT
+        assert binding.mma_device_status(stream) == MMA_OK
+    assert bool((D == 7.0).all())
+    # afterwards: products on single CTAs (256^3) and on CTA pairs
+    # (2048 x 2560 x 512, a full wave of pair tiles) are exact again
+    for (M, N, K) in [(256, 256, 256), (2048, 2560, 512)]:
+        g = synth.gemm_inputs(f"abort_after_{M}", "bf16", M, N, K, dist="uniform")
+        out = binding.gemm(to_dev(g.A, "bf16"), to_dev(g.B, "bf16"), to_dev(g.C))
+        torch.cuda.synchronize()
+        rows = np.arange(0, M, 7)
+        want, ab = oracle.gemm("bf16", np.ascontiguousarray(g.A[rows]), g.B,
+                               np.ascontiguousarray(g.C[rows]), want_absab=True)
+        check("bf16", out.cpu().numpy()[rows], want, ab, f"after abort {M}x{N}x{K}")
+    assert binding.mma_device_status(stream) == MMA_OK

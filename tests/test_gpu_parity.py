@@ -483,3 +483,4 @@ def test_ragged_shapes_on_cta_pairs(dtype_in):
     else:
         want, ab = oracle.gemm(dtype_in, A, g.B, C, want_absab=True)
         check(dtype_in, got, want, ab, f"{dtype_in} ragged pairs")
+
