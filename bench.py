@@ -47,6 +47,7 @@ L2_BYTES = 129 * 1024 * 1024
 MAX_SET_BYTES = 8 << 30  # device memory cap for the rotating input sets
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
+GB300_SMS = 152
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_FP64_TFLOPS = 1.25
 NOMINAL_HBM_GBS = 7900.0
@@ -334,10 +335,26 @@ def kernel_source(w):
         return "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu"
     if w["dtype_in"] == "i8" and not i8_on_tensor_pipe(w):
         return "mixed_precision_dense_02_gb300/csrc/gemm_i8.cu"
+    if stream_k_applies(w):
+        return "mixed_precision_dense_02_gb300/csrc/gemm_sk.cu"
     return {"f16": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
             "bf16": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
             "i8": "mixed_precision_dense_02_gb300/csrc/gemm_tc.cu",
             "f64": "mixed_precision_dense_02_gb300/csrc/gemm_f64.cu"}[w["dtype_in"]]
+
+
+def stream_k_applies(w, sms=GB300_SMS):
+    """FP16/BF16 -> FP32 products with column-major B, fewer than half as
+    many 128 x 128 output tiles as SMs, at least 8 K steps of 64 and two per
+    SM: the library splits the tiles' K steps over every SM (gemm_sk.cu,
+    the rule of gemm_sk_fits)."""
+    if w["kind"] != "gemm" or w["dtype_in"] not in ("f16", "bf16"):
+        return False
+    if w.get("acc16") or w.get("b_layout", "col") != "col":
+        return False
+    tiles = -(-w["M"] // 128) * -(-w["N"] // 128)
+    nk = -(-w["K"] // 64)
+    return 2 * tiles < sms and nk >= 8 and tiles * nk >= 2 * sms
 
 
 def i8_plain(w):

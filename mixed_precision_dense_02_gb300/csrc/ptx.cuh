@@ -186,6 +186,20 @@ __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* map,
       : "memory");
 }
 
+// As tma_load_3d, with an L2 cache policy (createpolicy) for the box.
+__device__ __forceinline__ void tma_load_3d_hint(const CUtensorMap* map,
+                                                 uint64_t* bar, void* dst,
+                                                 int x, int y, int z,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y),
+      "r"(z), "l"(policy)
+      : "memory");
+}
+
 // 3-D tiled store of one box from shared memory (bulk-group completion).
 // Out-of-bounds parts of the box are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map,
@@ -195,6 +209,18 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map,
       "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group "
       "[%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
       "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// As tma_store_3d, with an L2 cache policy for the box.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map,
+                                                  const void* src, int x,
+                                                  int y, int z,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint "
+      "[%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
 }
 

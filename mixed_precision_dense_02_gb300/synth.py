@@ -283,6 +283,11 @@ WORKLOADS = {
                                K=4096, a_signed=False, b_signed=False,
                                clamp=True,
                                c_int_range=(-(1 << 31), (1 << 31) - 1)),
+    # few output tiles (64 of 128 x 128) over a deep K: the tiles' K steps
+    # are split over every SM (stream-K)
+    "gemm_bf16_deepk_1024x1024x32768": dict(kind="gemm", dtype_in="bf16",
+                                            M=1024, N=1024, K=32768,
+                                            dist="normal"),
 }
 
 

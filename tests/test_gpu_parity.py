@@ -424,7 +424,8 @@ FULL_COMPARE = {"gemm_i8_4096", "gemm_bf16_skinny_16384x128x4096"}
 
 @pytest.mark.parametrize("name", ["gemm_f16_256", "gemm_i8_4096", "gemm_bf16_8192",
                                   "gemm_f64_4096_rowB",
-                                  "gemm_bf16_skinny_16384x128x4096"])
+                                  "gemm_bf16_skinny_16384x128x4096",
+                                  "gemm_bf16_deepk_1024x1024x32768"])
 def test_full_size_workload(name):
     """The workloads at full size, D inside guard bands.  The INT8 headline
     (16.8 M outputs, bit-exact) and the skinny BF16 product are compared in
