@@ -72,6 +72,8 @@ NCU_TRAFFIC: dict = {
                                                "bytes": 436228352 + 225458688},
     "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "c0fef1574223789d",
                                                 "bytes": 872517632 + 494047488},
+    "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "5e2d44fac663ee87",
+                                              "bytes": 436244736 + 226981376},
     "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "ee0bc3694a9ab89f",
                                               "bytes": 436278272 + 215408384},
     "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "ee0bc3694a9ab89f",

@@ -28,7 +28,10 @@ constexpr int kTcThreads = 128;
 constexpr int kTcN = 256;
 constexpr int kTcABytes = 128 * 64 * 2;   // 128 rows x 64 K (one swizzle row)
 constexpr int kTcBBytes = kTcN * 64 * 2;  // 256 rows x 64 K
-constexpr int kTcSmem = kTcABytes + kTcBBytes + 64 + 1024;
+// more shared memory than two CTAs could share, so that the grid of one CTA
+// per SM really lands one on every SM (48 KB of it are used)
+constexpr int kTcSmem = 120 * 1024;
+static_assert(kTcABytes + kTcBBytes + 64 + 1024 <= kTcSmem, "probe tiles fit");
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_probe_kernel(long long iters, unsigned* status) {
