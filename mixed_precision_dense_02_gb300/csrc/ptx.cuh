@@ -186,6 +186,20 @@ __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* map,
       : "memory");
 }
 
+// As tma_load_3d_pair, with an L2 cache policy (createpolicy) for the box.
+__device__ __forceinline__ void tma_load_3d_pair_hint(const CUtensorMap* map,
+                                                      uint32_t bar_cluster,
+                                                      void* dst, int x, int y,
+                                                      int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile."
+      "mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], "
+      "[%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y),
+      "r"(z), "l"(policy)
+      : "memory");
+}
+
 // As tma_load_3d, with an L2 cache policy (createpolicy) for the box.
 __device__ __forceinline__ void tma_load_3d_hint(const CUtensorMap* map,
                                                  uint64_t* bar, void* dst,
