@@ -26,10 +26,20 @@
 // from run to run.  Every wait is bounded (MMA_ERR_TIMEOUT on expiry).
 //
 // Roles (320 threads): warp 0 TMA producer (128 x 64 A and B boxes,
-// 128-byte swizzle, STAGES-deep ring), warp 1 tcgen05.mma issuer (M = 128,
-// N = 128, K = 16) into a double-buffered FP32 accumulator in tensor
-// memory, warps 2..9 epilogue (two per tensor-memory lane quarter, 64
-// columns each): each thread owns one row of its warp's columns.
+// 128-byte swizzle, STAGES-deep ring), warp 1 tcgen05.mma issuer into a
+// double-buffered FP32 accumulator in tensor memory, warps 2..9 epilogue
+// (two per tensor-memory lane quarter, one per column half): each thread
+// owns one row of its warp's columns, handled 64 at a time.
+//
+// CL = 1: 128 x 128 tiles, one per CTA (M = 128, N = 128 MMAs).
+// CL = 2: 256 x 256 tiles on CTA pairs (clusters of two SMs): the pair is
+// the unit of the stream-K ranges, each CTA stages 128 rows of A and 128
+// of B per K step, the leader's one thread issues cta_group::2 MMAs
+// (M = 256, N = 256) whose commits release both CTAs, and each CTA's
+// epilogue holds its 128 rows of the tile.  Per SM and K step this moves
+// the same 32 KB of operands as CL = 1 for twice the multiply-adds, which
+// lifts the ceiling that the L2-to-SM operand stream puts on the 128-wide
+// tiles.  A tile's partial sums travel between the CTAs of the same rank.
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
@@ -40,21 +50,24 @@
 namespace mmagb {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBM = 128;  // rows per CTA
 constexpr int kBK = 64;
 constexpr int kUK = 16;
 constexpr int kEpi = 8;                     // epilogue warps
 constexpr int kThreadsSK = 64 + 32 * kEpi;  // 320
-constexpr int kHalf = kBN / 2;              // columns per epilogue warp
-constexpr int kBlk = kHalf / 16;            // 16-column blocks per warp
+constexpr int kPart = 64;                   // columns per epilogue pass
+constexpr int kBlk = kPart / 16;            // 16-column blocks per pass
 constexpr int kStages = 6;
 constexpr int kABytes = kBM * kBK * 2;
-constexpr int kStageBytes = kABytes + kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + 128 * kBK * 2;  // 128 rows of B
 constexpr int kBarOffset = kStages * kStageBytes;
 constexpr int kSmemBytes = kBarOffset + (2 * kStages + 5) * 8 + 16 + 1024;
-// FP32 partial sums of one CTA's piece: 128 x 128
-constexpr int kSlotFloats = kBM * kBN;
+// Tile of CL CTAs: (128 CL) x (128 CL); per CTA 128 x 128 CL accumulators.
+template <int CL>
+constexpr int kTileN = 128 * CL;
+// FP32 partial sums of one CTA's piece: its 128 rows of the tile
+template <int CL>
+constexpr int kSlotFloats = kBM * kTileN<CL>;
 
 // First K step (of the whole sequence) of CTA c's range.
 __host__ __device__ __forceinline__ int64_t range_begin(int64_t c,
@@ -116,7 +129,7 @@ __device__ __forceinline__ Piece piece_at(int64_t s, int64_t end, int nk) {
   return p;
 }
 
-template <bool BF16>
+template <bool BF16, int CL>
 __global__ void __launch_bounds__(kThreadsSK, 1)
     gemm_sk_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
@@ -124,6 +137,11 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
                    int N, int K, float* __restrict__ partials,
                    unsigned* __restrict__ flags, unsigned seq,
                    unsigned* status) {
+  constexpr int TN = kTileN<CL>;    // tile columns
+  constexpr int TM = kBM * CL;      // tile rows
+  constexpr int HALF = TN / 2;      // columns per epilogue warp
+  constexpr int NP = HALF / kPart;  // 64-column passes per warp
+  constexpr uint32_t kTmemCols = 2 * TN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,14 +154,16 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
-  const int num_m = (M + kBM - 1) / kBM;
+  const int num_m = (M + TM - 1) / TM;
   const int nk = (K + kBK - 1) / kBK;
-  const int64_t tiles = int64_t(num_m) * ((N + kBN - 1) / kBN);
+  const int64_t tiles = int64_t(num_m) * ((N + TN - 1) / TN);
   const int64_t total = tiles * nk;
-  const int64_t grid = gridDim.x;
-  const int64_t cta = blockIdx.x;
-  const int64_t beg = range_begin(cta, total, grid);
-  const int64_t end = range_begin(cta + 1, total, grid);
+  // the unit of the ranges: one CTA, or one pair
+  const int64_t grid = gridDim.x / CL;
+  const int64_t unit = blockIdx.x / CL;
+  const int rank = CL > 1 ? int(cluster_ctarank()) : 0;
+  const int64_t beg = range_begin(unit, total, grid);
+  const int64_t end = range_begin(unit + 1, total, grid);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -152,7 +172,7 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpi);
+      mbar_init(&tempty[a], CL * kEpi);  // every epilogue warp of the tile
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -164,11 +184,19 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 2 * kBN);
-    tmem_relinquish();
+    if constexpr (CL == 1) {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL > 1)
+    cluster_sync();  // the peer's barriers exist before anything targets them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -178,6 +206,9 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
+      // the leader CTA's full barriers, which count both CTAs' bytes
+      const uint32_t full_lead =
+          CL > 1 ? mapa_shared(smem_u32(&full[0]), 0) : 0u;
       for (int64_t s = beg; s < end && ok;) {
         const Piece p = piece_at(s, end, nk);
         const int mb = p.t % num_m, nb = p.t / num_m;
@@ -187,9 +218,17 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
             break;
           }
           uint8_t* sa = smem + stage * kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_3d(&tmA, &full[stage], sa, kb * kBK, mb * kBM, 0);
-          tma_load_3d(&tmB, &full[stage], sa + kABytes, kb * kBK, nb * kBN, 0);
+          if constexpr (CL == 1) {
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            tma_load_3d(&tmA, &full[stage], sa, kb * kBK, mb * kBM, 0);
+            tma_load_3d(&tmB, &full[stage], sa + kABytes, kb * kBK, nb * TN, 0);
+          } else {
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], CL * kStageBytes);
+            const uint32_t fb = full_lead + uint32_t(stage) * 8u;
+            tma_load_3d_pair(&tmA, fb, sa, kb * kBK, mb * TM + rank * kBM, 0);
+            tma_load_3d_pair(&tmB, fb, sa + kABytes, kb * kBK,
+                             nb * TN + rank * 128, 0);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -198,24 +237,37 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
         }
         s += p.k1 - p.k0;
       }
-      // on abort, let every load still in flight land before exiting
-      if (!ok) {
-        for (int st = 0; st < kStages; ++st) {
-          const uint32_t fills =
-              issued / kStages + (uint32_t(st) < issued % kStages);
-          if (!fills) continue;
+      for (int st = 0; st < kStages; ++st) {
+        const uint32_t fills =
+            issued / kStages + (uint32_t(st) < issued % kStages);
+        if (!fills) continue;
+        // on abort, let every load still in flight land before exiting (the
+        // leader's full barriers also count the peer's loads)
+        if (!ok && rank == 0) {
           const uint32_t a = smem_u32(&full[st]);
           const unsigned long long t0 = global_timer_ns();
           while (!mbar_try_wait(a, (fills - 1) & 1u))
             if (global_timer_ns() - t0 > kWaitLimitNs) break;
+        }
+        // with a pair, the last release of each stage is the leader's
+        // commit: wait until it has arrived on this CTA
+        if (CL > 1) {
+          const uint32_t a = smem_u32(&empty[st]);
+          const unsigned long long t0 = global_timer_ns();
+          while (!mbar_try_wait(a, (fills - 1) & 1u))
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              atomicOr(status, kStatusTimeout);
+              break;
+            }
         }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (elect_one()) {
-      constexpr uint32_t idesc = idesc_f16_f32(BF16, kBM, kBN);
+    // (with a pair, only the leader CTA issues)
+    if (rank == 0 && elect_one()) {
+      constexpr uint32_t idesc = idesc_f16_f32(BF16, TM, TN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -223,7 +275,7 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
         const Piece p = piece_at(s, end, nk);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(acc * kBN);
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * TN);
         for (int kb = p.k0; kb < p.k1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, status)) {
             ok = false;
@@ -234,22 +286,38 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
           const uint64_t da = sw128_kmajor_desc(sa);
           const uint64_t db = sw128_kmajor_desc(sa + kABytes);
 #pragma unroll
-          for (int k = 0; k < kBK / kUK; ++k)
-            umma_f16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc,
-                     (kb != p.k0 || k != 0) ? 1u : 0u);
-          umma_commit(&empty[stage]);
+          for (int k = 0; k < kBK / kUK; ++k) {
+            const uint32_t accum = (kb != p.k0 || k != 0) ? 1u : 0u;
+            if constexpr (CL == 1)
+              umma_f16(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k),
+                       idesc, accum);
+            else
+              umma_f16_pair(d_tmem, da + uint64_t(2 * k), db + uint64_t(2 * k),
+                            idesc, accum);
+          }
+          if constexpr (CL == 1)
+            umma_commit(&empty[stage]);
+          else
+            umma_commit_pair(&empty[stage], 3u);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (CL == 1)
+          umma_commit(&tfull[acc]);
+        else
+          umma_commit_pair(&tfull[acc], 3u);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
         s += p.k1 - p.k0;
       }
-      umma_commit(done);
+      // every MMA issued above completes before tensor memory is released
+      if constexpr (CL == 1)
+        umma_commit(done);
+      else
+        umma_commit_pair(done, 1u);
       const uint32_t a = smem_u32(done);
       const unsigned long long t0 = global_timer_ns();
       while (!mbar_try_wait(a, 0))
@@ -262,43 +330,48 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
     const int q = warp & 3;    // tensor-memory lane quarter
     const int h = ew >> 2;     // column half
     const int lane = threadIdx.x & 31;
+    // this CTA's partial-sum slot and flags, and those of the CTAs of the
+    // same rank in later units
+    const int64_t me = unit * CL + rank;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    // (lane) 64 values of C's row `row` from column cc0 into v
+    auto load_c = [&](int row, int cc0, float (&v)[kPart]) {
+      const bool live = C != nullptr && row < M;
+      const float* crow = live ? C + int64_t(row) * ldc : nullptr;
+#pragma unroll
+      for (int c = 0; c < kPart / 4; ++c) {
+        const int cc = cc0 + 4 * c;
+        float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && cc + 4 <= N) {
+          w = *reinterpret_cast<const float4*>(crow + cc);
+        } else if (live) {
+          if (cc < N) w.x = crow[cc];
+          if (cc + 1 < N) w.y = crow[cc + 1];
+          if (cc + 2 < N) w.z = crow[cc + 2];
+        }
+        v[4 * c] = w.x;
+        v[4 * c + 1] = w.y;
+        v[4 * c + 2] = w.z;
+        v[4 * c + 3] = w.w;
+      }
+    };
     for (int64_t s = beg; s < end && ok;) {
       const Piece p = piece_at(s, end, nk);
       const int mb = p.t % num_m, nb = p.t / num_m;
-      const int row = mb * kBM + q * 32 + lane;
-      const int col0 = nb * kBN + h * kHalf;
+      const int row = mb * TM + rank * kBM + q * 32 + lane;
+      const int colh = nb * TN + h * HALF;
       const bool head = p.k0 == 0;
       const bool whole = head && p.k1 == nk;
       // The tile's other pieces (only for a first piece that is not the
-      // whole tile): CTAs cta + 1 .. last, each holding it as its first.
-      int64_t last = cta;
+      // whole tile): units unit + 1 .. last, each holding it as its first.
+      int64_t last = unit;
       if (head && !whole) last = owner_of(int64_t(p.t) * nk + nk - 1, total, grid);
-      // A first piece adds C: this thread's 64 values of it are requested
-      // now, while the piece's MMAs run, and held in registers.
-      float v[kHalf];
-      if (head) {
-        const bool live = C != nullptr && row < M;
-        const float* crow = live ? C + int64_t(row) * ldc : nullptr;
-#pragma unroll
-        for (int c = 0; c < kHalf / 4; ++c) {
-          const int cc = col0 + 4 * c;
-          float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (live && cc + 4 <= N) {
-            w = *reinterpret_cast<const float4*>(crow + cc);
-          } else if (live) {
-            if (cc < N) w.x = crow[cc];
-            if (cc + 1 < N) w.y = crow[cc + 1];
-            if (cc + 2 < N) w.z = crow[cc + 2];
-          }
-          v[4 * c] = w.x;
-          v[4 * c + 1] = w.y;
-          v[4 * c + 2] = w.z;
-          v[4 * c + 3] = w.w;
-        }
-      }
+      // A first piece adds C: the first pass's 64 values of it are
+      // requested now, while the piece's MMAs run, and held in registers.
+      float v[kPart];
+      if (head) load_c(row, colh, v);
       ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -306,14 +379,14 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
       }
       tc_fence_after();
       const uint32_t taddr =
-          tmem_base + uint32_t(acc * kBN + h * kHalf) + (uint32_t(q * 32) << 16);
+          tmem_base + uint32_t(acc * TN + h * HALF) + (uint32_t(q * 32) << 16);
       if (!head) {
         // partial sums to this CTA's slot, laid out so that each warp-wide
         // 16-byte store covers 512 contiguous bytes
         float4* slot = reinterpret_cast<float4*>(partials) +
-                       (cta * kEpi + ew) * (kBlk * 4 * 32);
+                       (me * kEpi + ew) * (NP * kBlk * 4 * 32);
 #pragma unroll
-        for (int j = 0; j < kBlk; ++j) {
+        for (int j = 0; j < NP * kBlk; ++j) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
           tmem_ld_wait();
@@ -325,57 +398,71 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
         }
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_u32(&flags[cta * kEpi + ew], seq);
+        if (lane == 0) st_release_u32(&flags[me * kEpi + ew], seq);
       } else {
-        // D = ((acc + C) + partial of cta + 1) + partial of cta + 2 ...: a
-        // fixed order, one FP32 rounding per addition
+        // D = ((acc + C) + partial of unit + 1) + partial of unit + 2 ...:
+        // a fixed order, one FP32 rounding per addition; 64 columns a pass
+        for (int part = 0; part < NP && ok; ++part) {
+          if (part > 0) load_c(row, colh + part * kPart, v);
 #pragma unroll
-        for (int j = 0; j < kBlk; ++j) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
-          tmem_ld_wait();
+          for (int j = 0; j < kBlk; ++j) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(taddr + uint32_t((part * kBlk + j) * 16), r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[16 * j + e] += __uint_as_float(r[e]);
-        }
-        for (int64_t o = cta + 1; o <= last && ok; ++o) {
-          ok = wait_flag(&flags[o * kEpi + ew], seq, abort_flag, status);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
+            for (int e = 0; e < 16; ++e) v[16 * j + e] += __uint_as_float(r[e]);
           }
-          // every 16-byte piece of the partial in flight at once
-          const float4* slot = reinterpret_cast<const float4*>(partials) +
-                               (o * kEpi + ew) * (kBlk * 4 * 32);
-          float4 w[kHalf / 4];
+          for (int64_t o = unit + 1; o <= last && ok; ++o) {
+            const int64_t other = o * CL + rank;
+            if (part == 0) {
+              ok = wait_flag(&flags[other * kEpi + ew], seq, abort_flag, status);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+              }
+            }
+            // every 16-byte piece of the partial in flight at once
+            const float4* slot = reinterpret_cast<const float4*>(partials) +
+                                 (other * kEpi + ew) * (NP * kBlk * 4 * 32) +
+                                 part * (kBlk * 4 * 32);
+            float4 w[kPart / 4];
 #pragma unroll
-          for (int c = 0; c < kHalf / 4; ++c) w[c] = __ldcg(&slot[c * 32 + lane]);
+            for (int c = 0; c < kPart / 4; ++c) w[c] = __ldcg(&slot[c * 32 + lane]);
 #pragma unroll
-          for (int c = 0; c < kHalf / 4; ++c) {
-            v[4 * c] += w[c].x;
-            v[4 * c + 1] += w[c].y;
-            v[4 * c + 2] += w[c].z;
-            v[4 * c + 3] += w[c].w;
+            for (int c = 0; c < kPart / 4; ++c) {
+              v[4 * c] += w[c].x;
+              v[4 * c + 1] += w[c].y;
+              v[4 * c + 2] += w[c].z;
+              v[4 * c + 3] += w[c].w;
+            }
           }
-        }
-        if (!ok) break;
-        if (row < M) {
-          float* drow = D + int64_t(row) * ldd;
+          if (!ok) break;
+          if (row < M) {
+            float* drow = D + int64_t(row) * ldd;
 #pragma unroll
-          for (int c = 0; c < kHalf / 4; ++c) {
-            const int cc = col0 + 4 * c;
-            if (cc + 4 <= N) {
-              *reinterpret_cast<float4*>(drow + cc) =
-                  make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            } else {
-              for (int e = 0; e < 4 && cc + e < N; ++e) drow[cc + e] = v[4 * c + e];
+            for (int c = 0; c < kPart / 4; ++c) {
+              const int cc = colh + part * kPart + 4 * c;
+              if (cc + 4 <= N) {
+                *reinterpret_cast<float4*>(drow + cc) =
+                    make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+              } else {
+                for (int e = 0; e < 4 && cc + e < N; ++e) drow[cc + e] = v[4 * c + e];
+              }
             }
           }
         }
+        if (!ok) break;
       }
-      // this warp's reads of the accumulator are done
+      // this warp's reads of the accumulator are done (to the leader CTA's
+      // barrier for a pair)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if constexpr (CL == 1)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
       s += p.k1 - p.k0;
@@ -383,10 +470,16 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL > 1)
+    cluster_sync();  // neither CTA leaves while the other may still signal it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * kBN);
+    if constexpr (CL == 1)
+      tmem_dealloc(tmem_base, kTmemCols);
+    else
+      tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -403,7 +496,7 @@ bool gemm_sk_fits(int num_sms, int64_t M, int64_t N, int64_t K) {
     return e[0] == '0' ? 0 : 1;
   }();
   if (forced == 0 || M <= 0 || N <= 0 || K <= 0) return false;
-  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
   const int64_t nk = (K + kBK - 1) / kBK;
   if (tiles * nk >= (int64_t(1) << 31)) return false;
   if (forced == 1) return tiles * nk >= 2 && tiles < (int64_t(1) << 31);
@@ -411,40 +504,107 @@ bool gemm_sk_fits(int num_sms, int64_t M, int64_t N, int64_t K) {
 }
 
 size_t gemm_sk_workspace_bytes(int num_sms) {
-  return size_t(num_sms) * kSlotFloats * sizeof(float);
+  // slots for either tile shape
+  return size_t(num_sms) * kSlotFloats<2> * sizeof(float);
 }
 
 size_t gemm_sk_flag_count(int num_sms) { return size_t(num_sms) * kEpi; }
 
-mma_status_t launch_gemm_sk(const Ctx& ctx, bool bf16, int64_t M, int64_t N,
-                            int64_t K, const void* A, int64_t lda,
-                            const void* B, int64_t ldb, const float* C,
-                            int64_t ldc, float* D, int64_t ldd,
-                            float* partials, unsigned* flags, unsigned seq) {
+namespace {
+
+template <bool BF16, int CL>
+mma_status_t launch_sk(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
+                       const void* A, int64_t lda, const void* B, int64_t ldb,
+                       const float* C, int64_t ldc, float* D, int64_t ldd,
+                       float* partials, unsigned* flags, unsigned seq) {
   CUtensorMap ta, tb;
-  if (!make_kmajor_map(&ta, A, K, M, lda, kBM, bf16) ||
-      !make_kmajor_map(&tb, B, K, N, ldb, kBN, bf16))
+  if (!make_kmajor_map(&ta, A, K, M, lda, kBM, BF16) ||
+      !make_kmajor_map(&tb, B, K, N, ldb, 128, BF16))
     return MMA_ERR_LAUNCH;
-  auto kern = bf16 ? gemm_sk_kernel<true> : gemm_sk_kernel<false>;
-  static PerContext<bool> smem_attr[2];
+  auto kern = gemm_sk_kernel<BF16, CL>;
+  static PerContext<bool> smem_attr;
   bool attr_ok = false;
-  if (!smem_attr[bf16 ? 1 : 0].get(ctx, &attr_ok, [&](bool* v) {
+  if (!smem_attr.get(ctx, &attr_ok, [&](bool* v) {
         *v = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kSmemBytes) == cudaSuccess;
         if (!*v) cudaGetLastError();
         return *v;
       }))
     return MMA_ERR_LAUNCH;
-  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  constexpr int TN = kTileN<CL>;
+  const int64_t tiles = ((M + kBM * CL - 1) / (kBM * CL)) * ((N + TN - 1) / TN);
   const int64_t total = tiles * ((K + kBK - 1) / kBK);
-  int64_t grid = ctx.num_sms;
-  if (grid > total) grid = total;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreadsSK, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // units (CTAs or pairs) resident at once: every unit may wait on a later
+  // one, so the grid never exceeds them
+  int64_t units = ctx.num_sms / CL;
+  if (CL > 1) {
+    static PerContext<int> resident;
+    int r = 0;
+    if (!resident.get(ctx, &r, [&](int* v) {
+          cudaLaunchConfig_t probe = cfg;
+          probe.gridDim = dim3(unsigned(CL * (ctx.num_sms / CL)), 1, 1);
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, kern, &probe) != cudaSuccess ||
+              n < 1) {
+            cudaGetLastError();
+            return false;
+          }
+          *v = n;
+          return true;
+        }))
+      return MMA_ERR_LAUNCH;
+    units = r;
+  }
+  if (units > total) units = total;
+  cfg.gridDim = dim3(unsigned(units * CL), 1, 1);
   ctx.mark_start();
-  kern<<<unsigned(grid), kThreadsSK, kSmemBytes, ctx.stream>>>(
-      ta, tb, C, ldc, D, ldd, int(M), int(N), int(K), partials, flags, seq,
-      ctx.status);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, ta, tb, C, ldc, D, ldd, int(M), int(N),
+                         int(K), partials, flags, seq, ctx.status);
   ctx.mark_stop();
-  return cudaGetLastError() == cudaSuccess ? MMA_OK : MMA_ERR_LAUNCH;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MMA_ERR_LAUNCH;
+  }
+  return MMA_OK;
+}
+
+}  // namespace
+
+// CTA pairs on 256 x 256 tiles when the product is at least one such tile
+// in each direction (half-empty pair tiles would waste the pair's operand
+// saving); MMA_GB300_STREAMK_CL (1 or 2) overrides, for tuning.
+mma_status_t launch_gemm_sk(const Ctx& ctx, bool bf16, int64_t M, int64_t N,
+                            int64_t K, const void* A, int64_t lda,
+                            const void* B, int64_t ldb, const float* C,
+                            int64_t ldc, float* D, int64_t ldd,
+                            float* partials, unsigned* flags, unsigned seq) {
+  static const int forced = [] {
+    const char* e = getenv("MMA_GB300_STREAMK_CL");
+    const int v = e ? atoi(e) : 0;
+    return (v == 1 || v == 2) ? v : 0;
+  }();
+  const bool pair = forced ? forced == 2 : (M >= 256 && N >= 256);
+  if (pair)
+    return bf16 ? launch_sk<true, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D,
+                                     ldd, partials, flags, seq)
+                : launch_sk<false, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D,
+                                      ldd, partials, flags, seq);
+  return bf16 ? launch_sk<true, 1>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D,
+                                   ldd, partials, flags, seq)
+              : launch_sk<false, 1>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D,
+                                    ldd, partials, flags, seq);
 }
 
 }  // namespace mmagb

@@ -8,7 +8,10 @@ pieces, C absent and C = D in place, a column count whose rows end off a
 16-byte boundary, run-to-run identical results, and products that the
 automatic choice keeps on the regular kernel but MMA_GB300_STREAMK=1 sends
 here (several whole tiles per CTA between the split ones, and the tall
-16384 x 128 x 4096 shape).  Every output sits inside guard bands.
+16384 x 128 x 4096 shape).  Products at least 256 wide in M and N run on
+CTA pairs with 256 x 256 tiles (their partial sums passed between the
+CTAs of the same rank); MMA_GB300_STREAMK_CL=1 sends them to single CTAs
+instead.  Every output sits inside guard bands.
 """
 from __future__ import annotations
 
@@ -59,8 +62,18 @@ SHAPES = [
 ]
 
 
+# M and N >= 256: CTA pairs on 256 x 256 tiles (ragged in M, N and K)
+PAIR_SHAPES = [
+    (1024, 768, 4096),    # 12 pair tiles over 76 pairs
+    (512, 768, 6000),
+    (300, 520, 9000),     # tiles half outside M, a ragged last column tile
+    (1000, 300, 4000),
+    (256, 256, 16384),    # one pair tile split over every pair
+]
+
+
 @pytest.mark.parametrize("dtype_in", ["bf16", "f16"])
-@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("M,N,K", SHAPES + PAIR_SHAPES)
 def test_stream_k_shapes(dtype_in, M, N, K):
     g = synth.gemm_inputs(f"sk_{M}_{N}_{K}", dtype_in, M, N, K, dist="normal")
     want, ab = oracle.gemm(dtype_in, g.A, g.B, g.C, want_absab=True)
@@ -78,6 +91,18 @@ def test_stream_k_no_c_in_place_and_repeatable():
     check("bf16", run(g, inplace=True), want, ab, "stream-K in place")
     want0, ab0 = oracle.gemm("bf16", g.A, g.B, np.zeros_like(g.C), want_absab=True)
     check("bf16", run(g, use_c=False), want0, ab0, "stream-K, C = NULL")
+
+
+def test_stream_k_pairs_no_c_in_place_and_repeatable():
+    M, N, K = 520, 600, 5000
+    g = synth.gemm_inputs("skp_modes", "bf16", M, N, K, dist="uniform")
+    want, ab = oracle.gemm("bf16", g.A, g.B, g.C, want_absab=True)
+    first = run(g)
+    check("bf16", first, want, ab, "stream-K pairs")
+    assert np.array_equal(first.view(np.uint32), run(g).view(np.uint32))
+    check("bf16", run(g, inplace=True), want, ab, "stream-K pairs in place")
+    want0, ab0 = oracle.gemm("bf16", g.A, g.B, np.zeros_like(g.C), want_absab=True)
+    check("bf16", run(g, use_c=False), want0, ab0, "stream-K pairs, C = NULL")
 
 
 def test_full_size_skinny_repeatable():
@@ -110,6 +135,43 @@ for (M, N, K) in [(2100, 2300, 3000), (512, 640, 192), (256, 256, 64), (16384, 1
 binding.device_status()
 np.savez(sys.argv[2], **out)
 """
+
+
+_SINGLE_SCRIPT = """
+import sys, numpy as np, torch
+sys.path[:0] = [sys.argv[1], sys.argv[1] + '/tests']
+from mixed_precision_dense_02_gb300 import binding, synth
+from helpers import GuardedMatrix, dev_padded
+binding.load()
+M, N, K = 1024, 768, 4096
+g = synth.gemm_inputs(f'sk_{M}_{N}_{K}', 'bf16', M, N, K, dist='normal')
+Gd = GuardedMatrix(M, N, np.float32)
+binding.gemm(dev_padded(g.A, 'bf16'), dev_padded(g.B, 'bf16'), dev_padded(g.C), Gd.view)
+Gd.verify('single-CTA stream-K guard')
+binding.device_status()
+np.save(sys.argv[2], Gd.view.cpu().numpy())
+"""
+
+
+def test_stream_k_pairs_and_single_ctas_agree_with_oracle(tmp_path):
+    """The same product on pairs (automatic) and, in a child process with
+    MMA_GB300_STREAMK_CL=1, on single CTAs: both within the tolerance of
+    the oracle (their sums are split differently, so their bits differ)."""
+    import os
+    import pathlib
+    import subprocess
+    import sys
+    root = str(pathlib.Path(__file__).resolve().parents[1])
+    out = tmp_path / "single.npy"
+    env = dict(os.environ, MMA_GB300_STREAMK_CL="1")
+    r = subprocess.run([sys.executable, "-c", _SINGLE_SCRIPT, root, str(out)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    M, N, K = 1024, 768, 4096
+    g = synth.gemm_inputs(f"sk_{M}_{N}_{K}", "bf16", M, N, K, dist="normal")
+    want, ab = oracle.gemm("bf16", g.A, g.B, g.C, want_absab=True)
+    check("bf16", np.load(out), want, ab, "stream-K single CTAs")
+    check("bf16", run(g), want, ab, "stream-K pairs")
 
 
 def test_stream_k_forced_on_many_tiles(tmp_path):
