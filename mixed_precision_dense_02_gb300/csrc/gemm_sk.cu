@@ -591,7 +591,11 @@ mma_status_t launch_sk(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
 
 // CTA pairs on 256 x 256 tiles when the product is at least one such tile
 // in each direction (half-empty pair tiles would waste the pair's operand
-// saving); MMA_GB300_STREAMK_CL (1 or 2) overrides, for tuning.
+// saving) and has enough of them that a tile is cut into at most about 8
+// ranges: the CTA finishing a tile adds the other ranges' partial tiles one
+// after another (512 x 512 x 65536 on 4 pair tiles, 19 ranges each: 62 us;
+// on 16 single-CTA tiles, 9 ranges each: 51 us).  MMA_GB300_STREAMK_CL (1
+// or 2) overrides, for tuning.
 mma_status_t launch_gemm_sk(const Ctx& ctx, bool bf16, int64_t M, int64_t N,
                             int64_t K, const void* A, int64_t lda,
                             const void* B, int64_t ldb, const float* C,
@@ -602,7 +606,10 @@ mma_status_t launch_gemm_sk(const Ctx& ctx, bool bf16, int64_t M, int64_t N,
     const int v = e ? atoi(e) : 0;
     return (v == 1 || v == 2) ? v : 0;
   }();
-  const bool pair = forced ? forced == 2 : (M >= 256 && N >= 256);
+  const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+  const bool pair = forced ? forced == 2
+                           : (M >= 256 && N >= 256 &&
+                              8 * pair_tiles >= int64_t(ctx.num_sms / 2));
   if (pair)
     return bf16 ? launch_sk<true, 2>(ctx, M, N, K, A, lda, B, ldb, C, ldc, D,
                                      ldd, partials, flags, seq)
