@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
                    const float* C, int64_t ldc, float* D, int64_t ldd, int M,
                    int N, int K, float* __restrict__ partials,
                    unsigned* __restrict__ flags, unsigned seq,
-                   unsigned* status) {
+                   int shared_ranges, unsigned* status) {
   constexpr int TN = kTileN<CL>;    // tile columns
   constexpr int TM = kBM * CL;      // tile rows
   constexpr int HALF = TN / 2;      // columns per epilogue warp
@@ -356,11 +356,111 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
         v[4 * c + 3] = w.w;
       }
     };
+    // this warp's partial sums (its rows and HALF columns) to this CTA's
+    // slot, laid out so that each warp-wide 16-byte store covers 512
+    // contiguous bytes; then its release flag
+    auto write_partial = [&](uint32_t taddr) {
+      float4* slot = reinterpret_cast<float4*>(partials) +
+                     (me * kEpi + ew) * (NP * kBlk * 4 * 32);
+#pragma unroll
+      for (int j = 0; j < NP * kBlk; ++j) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          slot[(j * 4 + c) * 32 + lane] =
+              make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                          __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release_u32(&flags[me * kEpi + ew], seq);
+    };
+    // v += the pass `part` of unit o's partial sums in this warp's region
+    // (after its flag), all of its 16-byte pieces in flight at once
+    auto add_partial = [&](int64_t o, int part, float (&v)[kPart]) -> bool {
+      const int64_t other = o * CL + rank;
+      const bool okf = wait_flag(&flags[other * kEpi + ew], seq, abort_flag, status);
+      if (!__all_sync(0xffffffffu, okf)) return false;
+      const float4* slot = reinterpret_cast<const float4*>(partials) +
+                           (other * kEpi + ew) * (NP * kBlk * 4 * 32) +
+                           part * (kBlk * 4 * 32);
+      float4 w[kPart / 4];
+#pragma unroll
+      for (int c = 0; c < kPart / 4; ++c) w[c] = __ldcg(&slot[c * 32 + lane]);
+#pragma unroll
+      for (int c = 0; c < kPart / 4; ++c) {
+        v[4 * c] += w[c].x;
+        v[4 * c + 1] += w[c].y;
+        v[4 * c + 2] += w[c].z;
+        v[4 * c + 3] += w[c].w;
+      }
+      return true;
+    };
+    // (lane) this row's 64 values from column cc0 to D
+    auto store_d = [&](int row, int cc0, const float (&v)[kPart]) {
+      if (row >= M) return;
+      float* drow = D + int64_t(row) * ldd;
+#pragma unroll
+      for (int c = 0; c < kPart / 4; ++c) {
+        const int cc = cc0 + 4 * c;
+        if (cc + 4 <= N) {
+          *reinterpret_cast<float4*>(drow + cc) =
+              make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        } else {
+          for (int e = 0; e < 4 && cc + e < N; ++e) drow[cc + e] = v[4 * c + e];
+        }
+      }
+    };
+    // This warp's accumulator reads are done (to the leader CTA's barrier
+    // for a pair).
+    auto release_acc = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CL == 1)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    };
     for (int64_t s = beg; s < end && ok;) {
       const Piece p = piece_at(s, end, nk);
       const int mb = p.t % num_m, nb = p.t / num_m;
       const int row = mb * TM + rank * kBM + q * 32 + lane;
       const int colh = nb * TN + h * HALF;
+      if (shared_ranges > 1) {
+        // Every tile is cut into shared_ranges whole ranges, one piece
+        // each: every unit stores its partial sums, then finishes a share
+        // of its tile -- the (warp region, 64-column pass) items whose
+        // index modulo shared_ranges is its position in the tile -- as
+        // (((C + partial_0) + partial_1) + ...) in unit order, the same
+        // order (and bits) as a single finishing unit would add them in.
+        const int P = shared_ranges;
+        ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        write_partial(tmem_base + uint32_t(acc * TN + h * HALF) +
+                      (uint32_t(q * 32) << 16));
+        release_acc();
+        const int64_t first = int64_t(p.t) * P;  // the tile's first unit
+        const int pos = int(unit - first);
+        for (int part = 0; part < NP && ok; ++part) {
+          if ((ew * NP + part) % P != pos) continue;
+          float v[kPart];
+          load_c(row, colh + part * kPart, v);
+          for (int k = 0; k < P && ok; ++k) ok = add_partial(first + k, part, v);
+          if (ok) store_d(row, colh + part * kPart, v);
+        }
+        s += p.k1 - p.k0;
+        continue;
+      }
       const bool head = p.k0 == 0;
       const bool whole = head && p.k1 == nk;
       // The tile's other pieces (only for a first piece that is not the
@@ -380,24 +480,7 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
       const uint32_t taddr =
           tmem_base + uint32_t(acc * TN + h * HALF) + (uint32_t(q * 32) << 16);
       if (!head) {
-        // partial sums to this CTA's slot, laid out so that each warp-wide
-        // 16-byte store covers 512 contiguous bytes
-        float4* slot = reinterpret_cast<float4*>(partials) +
-                       (me * kEpi + ew) * (NP * kBlk * 4 * 32);
-#pragma unroll
-        for (int j = 0; j < NP * kBlk; ++j) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + uint32_t(j * 16), r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            slot[(j * 4 + c) * 32 + lane] =
-                make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                            __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_u32(&flags[me * kEpi + ew], seq);
+        write_partial(taddr);
       } else {
         // D = ((acc + C) + partial of unit + 1) + partial of unit + 2 ...:
         // a fixed order, one FP32 rounding per addition; 64 columns a pass
@@ -411,59 +494,14 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[16 * j + e] += __uint_as_float(r[e]);
           }
-          for (int64_t o = unit + 1; o <= last && ok; ++o) {
-            const int64_t other = o * CL + rank;
-            if (part == 0) {
-              ok = wait_flag(&flags[other * kEpi + ew], seq, abort_flag, status);
-              if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-              }
-            }
-            // every 16-byte piece of the partial in flight at once
-            const float4* slot = reinterpret_cast<const float4*>(partials) +
-                                 (other * kEpi + ew) * (NP * kBlk * 4 * 32) +
-                                 part * (kBlk * 4 * 32);
-            float4 w[kPart / 4];
-#pragma unroll
-            for (int c = 0; c < kPart / 4; ++c) w[c] = __ldcg(&slot[c * 32 + lane]);
-#pragma unroll
-            for (int c = 0; c < kPart / 4; ++c) {
-              v[4 * c] += w[c].x;
-              v[4 * c + 1] += w[c].y;
-              v[4 * c + 2] += w[c].z;
-              v[4 * c + 3] += w[c].w;
-            }
-          }
+          for (int64_t o = unit + 1; o <= last && ok; ++o)
+            ok = add_partial(o, part, v);
           if (!ok) break;
-          if (row < M) {
-            float* drow = D + int64_t(row) * ldd;
-#pragma unroll
-            for (int c = 0; c < kPart / 4; ++c) {
-              const int cc = colh + part * kPart + 4 * c;
-              if (cc + 4 <= N) {
-                *reinterpret_cast<float4*>(drow + cc) =
-                    make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-              } else {
-                for (int e = 0; e < 4 && cc + e < N; ++e) drow[cc + e] = v[4 * c + e];
-              }
-            }
-          }
+          store_d(row, colh + part * kPart, v);
         }
         if (!ok) break;
       }
-      // this warp's reads of the accumulator are done (to the leader CTA's
-      // barrier for a pair)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CL == 1)
-          mbar_arrive(&tempty[acc]);
-        else
-          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      release_acc();
       s += p.k1 - p.k0;
     }
   }
@@ -574,11 +612,22 @@ mma_status_t launch_sk(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   // single CTAs 128 of 152, 68.6 -> 62.0 us).
   const int64_t per_tile = units / tiles;
   if (per_tile >= 1 && 4 * per_tile * tiles >= 3 * units) units = per_tile * tiles;
+  // With whole ranges every unit holds one piece of one tile.  On pairs
+  // the tile's units then finish it together (each adds the partial sums
+  // of a share of the tile) instead of its first unit alone, whose warps
+  // would each add (ranges - 1) partial blocks twice (two 64-column
+  // passes) one after another: 1024 x 768 x 8192 35.7 -> 30.9 us, deep-K
+  // 59.1 -> 57.9 us.  On single CTAs (one pass) sharing only lengthens
+  // each warp's chain of dependent loads (4096 x 128 x 4096 18.1 -> 21.0
+  // us), so their first unit finishes alone.
+  const int shared_ranges =
+      (CL == 2 && units == per_tile * tiles && per_tile > 1) ? int(per_tile) : 0;
   cfg.gridDim = dim3(unsigned(units * CL), 1, 1);
   ctx.mark_start();
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, C, ldc, D, ldd, int(M), int(N),
-                         int(K), partials, flags, seq, ctx.status);
+                         int(K), partials, flags, seq, shared_ranges,
+                         ctx.status);
   ctx.mark_stop();
   if (e != cudaSuccess) {
     cudaGetLastError();

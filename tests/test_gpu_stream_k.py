@@ -10,8 +10,9 @@ automatic choice keeps on the regular kernel but MMA_GB300_STREAMK=1 sends
 here (several whole tiles per CTA between the split ones, and the tall
 16384 x 128 x 4096 shape).  Products at least 256 wide in M and N run on
 CTA pairs with 256 x 256 tiles (their partial sums passed between the
-CTAs of the same rank); MMA_GB300_STREAMK_CL=1 sends them to single CTAs
-instead.  Every output sits inside guard bands.
+CTAs of the same rank, and with whole ranges per tile summed by all of
+the tile's pairs, each a share); MMA_GB300_STREAMK_CL=1 sends them to
+single CTAs instead.  Every output sits inside guard bands.
 """
 from __future__ import annotations
 
@@ -64,7 +65,9 @@ SHAPES = [
 
 # M and N >= 256: CTA pairs on 256 x 256 tiles (ragged in M, N and K)
 PAIR_SHAPES = [
-    (1024, 768, 4096),    # 12 pair tiles over 76 pairs
+    (1024, 768, 4096),    # 12 pair tiles, 6 whole ranges each: the
+                          # tile's pairs finish it together
+    (1200, 700, 6100),    # 15 ragged pair tiles, 5 ranges each
     (512, 768, 6000),
     (300, 520, 9000),     # tiles half outside M, a ragged last column tile
     (1000, 300, 4000),
