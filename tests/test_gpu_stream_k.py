@@ -96,9 +96,11 @@ def test_stream_k_no_c_in_place_and_repeatable():
     check("bf16", run(g, use_c=False), want0, ab0, "stream-K, C = NULL")
 
 
-def test_stream_k_pairs_no_c_in_place_and_repeatable():
-    M, N, K = 520, 600, 5000
-    g = synth.gemm_inputs("skp_modes", "bf16", M, N, K, dist="uniform")
+@pytest.mark.parametrize("M,N,K", [(520, 600, 5000), (1200, 700, 6100)])
+def test_stream_k_pairs_no_c_in_place_and_repeatable(M, N, K):
+    """Single CTAs (9 pair tiles would be too few for pairs) and pairs whose
+    tiles are finished by all of their units, each a share."""
+    g = synth.gemm_inputs(f"skp_modes_{M}", "bf16", M, N, K, dist="uniform")
     want, ab = oracle.gemm("bf16", g.A, g.B, g.C, want_absab=True)
     first = run(g)
     check("bf16", first, want, ab, "stream-K pairs")
