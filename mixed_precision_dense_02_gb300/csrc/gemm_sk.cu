@@ -24,6 +24,12 @@
 // their partials before waiting on anything, so no cycle of waits exists;
 // the sum order depends only on M, N, K and G, so results are identical
 // from run to run.  Every wait is bounded (MMA_ERR_TIMEOUT on expiry).
+// When G is a whole number of ranges per tile (the host picks such a G
+// when it idles at most a quarter of the units), every range lies in one
+// tile and all tiles' ranges start at the same K offsets; on pairs every
+// unit then stores its partial sums and the tile's units share the final
+// additions (same order, same bits), each waiting only for flags that are
+// written before any wait.
 //
 // Roles (320 threads): warp 0 TMA producer (128 x 64 A and B boxes,
 // 128-byte swizzle, STAGES-deep ring), warp 1 tcgen05.mma issuer into a
