@@ -179,6 +179,46 @@ def test_stream_k_pairs_and_single_ctas_agree_with_oracle(tmp_path):
     check("bf16", run(g), want, ab, "stream-K pairs")
 
 
+_PAIRS_SCRIPT = """
+import sys, numpy as np, torch
+sys.path[:0] = [sys.argv[1], sys.argv[1] + '/tests']
+from mixed_precision_dense_02_gb300 import binding, synth
+from helpers import GuardedMatrix, dev_padded
+binding.load()
+out = {}
+for (M, N, K) in [(256, 512, 16384), (300, 260, 5000), (512, 256, 3000)]:
+    g = synth.gemm_inputs(f'skq_{M}_{N}_{K}', 'bf16', M, N, K, dist='uniform')
+    Gd = GuardedMatrix(M, N, np.float32)
+    binding.gemm(dev_padded(g.A, 'bf16'), dev_padded(g.B, 'bf16'), dev_padded(g.C), Gd.view)
+    Gd.verify('forced pairs guard')
+    out[f'{M}_{N}_{K}'] = Gd.view.cpu().numpy()
+binding.device_status()
+np.savez(sys.argv[2], **out)
+"""
+
+
+def test_stream_k_forced_pairs_many_ranges(tmp_path):
+    """MMA_GB300_STREAMK_CL=2 (child process) on products with one to two
+    pair tiles, so each tile is cut into 25 to 76 whole ranges and has more
+    ranges than finishing items (some units add nothing), ragged in M, N
+    and K; against the oracle."""
+    import os
+    import pathlib
+    import subprocess
+    import sys
+    root = str(pathlib.Path(__file__).resolve().parents[1])
+    out = tmp_path / "forced_pairs.npz"
+    env = dict(os.environ, MMA_GB300_STREAMK_CL="2")
+    r = subprocess.run([sys.executable, "-c", _PAIRS_SCRIPT, root, str(out)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    got = np.load(out)
+    for (M, N, K) in [(256, 512, 16384), (300, 260, 5000), (512, 256, 3000)]:
+        g = synth.gemm_inputs(f"skq_{M}_{N}_{K}", "bf16", M, N, K, dist="uniform")
+        want, ab = oracle.gemm("bf16", g.A, g.B, g.C, want_absab=True)
+        check("bf16", got[f"{M}_{N}_{K}"], want, ab, f"forced pairs {M}x{N}x{K}")
+
+
 def test_stream_k_forced_on_many_tiles(tmp_path):
     """MMA_GB300_STREAMK=1 (read once per process, so in a child process):
     products with more tiles than SMs (whole tiles between each CTA's split
