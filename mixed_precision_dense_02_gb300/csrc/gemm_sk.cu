@@ -529,9 +529,14 @@ __global__ void __launch_bounds__(kThreadsSK, 1)
 }  // namespace
 
 // Stream-K applies to FP32-result products whose 128 x 128 tiles are fewer
-// than the SMs, with at least two K steps per CTA on average and at least
-// eight per tile (MMA_GB300_STREAMK=0 turns it off, =1 on wherever the
-// sizes allow it, for tuning).
+// than half the SMs, with at least two K steps per CTA on average and at
+// least eight per tile, and either at most a quarter of the SMs busy on the
+// regular kernel or at least 128 K steps per tile: the split only pays when
+// the MMAs outweigh the fixed cost of a call and the partial-sum hand-off
+// (3000 x 256 x 2048: 23.2 us split, 13.5 us regular; 1024 x 1024 x 4096:
+// 25.1 against 21.5 us; 4096 x 128 x 4096: 19.0 against 22.9 us).
+// MMA_GB300_STREAMK=0 turns it off, =1 on wherever the sizes allow it, for
+// tuning.
 bool gemm_sk_fits(int num_sms, int64_t M, int64_t N, int64_t K) {
   static const int forced = [] {
     const char* e = getenv("MMA_GB300_STREAMK");
@@ -543,7 +548,8 @@ bool gemm_sk_fits(int num_sms, int64_t M, int64_t N, int64_t K) {
   const int64_t nk = (K + kBK - 1) / kBK;
   if (tiles * nk >= (int64_t(1) << 31)) return false;
   if (forced == 1) return tiles * nk >= 2 && tiles < (int64_t(1) << 31);
-  return 2 * tiles < num_sms && nk >= 8 && tiles * nk >= 2 * int64_t(num_sms);
+  return 2 * tiles < num_sms && nk >= 8 && tiles * nk >= 2 * int64_t(num_sms) &&
+         (4 * tiles <= num_sms || nk >= 128);
 }
 
 size_t gemm_sk_workspace_bytes(int num_sms) {

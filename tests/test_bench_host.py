@@ -170,7 +170,9 @@ def test_bench_kernel_attribution_follows_the_library_routing():
     assert bench.kernel_source(big).endswith("gemm_tc.cu")
     # stream-K: the rule of gemm_sk_fits (few tiles, deep K)
     with open(os.path.join(ROOT, csrc + "gemm_sk.cu"), encoding="utf-8") as f:
-        assert "2 * tiles < num_sms && nk >= 8 && tiles * nk >= 2 * int64_t(num_sms)" in f.read()
+        src = f.read()
+    assert "2 * tiles < num_sms && nk >= 8 && tiles * nk >= 2 * int64_t(num_sms)" in src
+    assert "(4 * tiles <= num_sms || nk >= 128)" in src
     deep = {"kind": "gemm", "dtype_in": "bf16", "M": 1024, "N": 1024, "K": 32768}
     assert bench.kernel_source(deep).endswith("gemm_sk.cu")
     skinny = dict(deep, M=16384, N=128, K=4096)           # 128 tiles >= 76

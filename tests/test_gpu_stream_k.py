@@ -65,9 +65,9 @@ SHAPES = [
 
 # M and N >= 256: CTA pairs on 256 x 256 tiles (ragged in M, N and K)
 PAIR_SHAPES = [
-    (1024, 768, 4096),    # 12 pair tiles, 6 whole ranges each: the
+    (1024, 768, 8192),    # 12 pair tiles, 6 whole ranges each: the
                           # tile's pairs finish it together
-    (1200, 700, 6100),    # 15 ragged pair tiles, 5 ranges each
+    (1200, 700, 8200),    # 15 ragged pair tiles, 5 ranges each
     (512, 768, 6000),
     (300, 520, 9000),     # tiles half outside M, a ragged last column tile
     (1000, 300, 4000),
@@ -96,7 +96,7 @@ def test_stream_k_no_c_in_place_and_repeatable():
     check("bf16", run(g, use_c=False), want0, ab0, "stream-K, C = NULL")
 
 
-@pytest.mark.parametrize("M,N,K", [(520, 600, 5000), (1200, 700, 6100)])
+@pytest.mark.parametrize("M,N,K", [(520, 600, 5000), (1200, 700, 8200)])
 def test_stream_k_pairs_no_c_in_place_and_repeatable(M, N, K):
     """Single CTAs (9 pair tiles would be too few for pairs) and pairs whose
     tiles are finished by all of their units, each a share."""
@@ -148,7 +148,7 @@ sys.path[:0] = [sys.argv[1], sys.argv[1] + '/tests']
 from mixed_precision_dense_02_gb300 import binding, synth
 from helpers import GuardedMatrix, dev_padded
 binding.load()
-M, N, K = 1024, 768, 4096
+M, N, K = 1024, 768, 8192
 g = synth.gemm_inputs(f'sk_{M}_{N}_{K}', 'bf16', M, N, K, dist='normal')
 Gd = GuardedMatrix(M, N, np.float32)
 binding.gemm(dev_padded(g.A, 'bf16'), dev_padded(g.B, 'bf16'), dev_padded(g.C), Gd.view)
@@ -172,7 +172,7 @@ def test_stream_k_pairs_and_single_ctas_agree_with_oracle(tmp_path):
     r = subprocess.run([sys.executable, "-c", _SINGLE_SCRIPT, root, str(out)],
                        env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
-    M, N, K = 1024, 768, 4096
+    M, N, K = 1024, 768, 8192
     g = synth.gemm_inputs(f"sk_{M}_{N}_{K}", "bf16", M, N, K, dist="normal")
     want, ab = oracle.gemm("bf16", g.A, g.B, g.C, want_absab=True)
     check("bf16", np.load(out), want, ab, "stream-K single CTAs")
