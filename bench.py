@@ -81,8 +81,8 @@ NCU_TRAFFIC: dict = {
     "gemm_f64_4096_rowB": {"sha": "b947734a2fa7d71b", "bytes": 3657537000 + 130594048},
     "gemm_bf16_acc16_8192": {"sha": "22df8f61666701a6", "bytes": 1485881344 + 129445888},
     "gemm_f16_256": {"sha": "22df8f61666701a6", "bytes": 580096 + 0},
-    "gemm_bf16_deepk_1024x1024x32768": {"sha": "7102bae14e0ea19a",
-                                        "bytes": 138483200 + 3309312},
+    "gemm_bf16_deepk_1024x1024x32768": {"sha": "b39718a8ce94b2da",
+                                        "bytes": 138511104 + 3083008},
 }
 
 
