@@ -50,10 +50,11 @@
  * terms; batched INT8 products widen every tile, batch * (M + N) *
  * roundup(K, 8) * 2 bytes; FP16/BF16 products with row-major B transpose
  * B, N * roundup(K, 8) * 2 bytes; FP16/BF16 -> FP32 products with
- * column-major B and fewer 128 x 128 output tiles than SMs (and at least
- * eight 64-deep K steps per tile) split K over every SM and meet in it,
- * SMs * 64 KiB, plus a hand-off flag buffer of SMs * 32 bytes allocated
- * (and zeroed) once per device.  That buffer is allocated once
+ * column-major B, fewer than half as many 128 x 128 output tiles as SMs
+ * and deep enough K (at least eight 64-deep K steps per tile, and either at
+ * most a quarter as many tiles as SMs or at least 128 steps) split K over
+ * the SMs and meet in it, SMs * 128 KiB, plus a hand-off flag buffer of
+ * SMs * 32 bytes allocated (and zeroed) once per device.  That buffer is allocated once
  * per device by the first such call, grown (cudaMalloc, after the previous
  * user finishes) only when a larger problem arrives, and kept until the
  * process exits; calls on different streams are ordered on it by an event.
