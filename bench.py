@@ -74,10 +74,10 @@ NCU_TRAFFIC: dict = {
                                                 "bytes": 901588224 + 490481664},
     "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "5e2d44fac663ee87",
                                               "bytes": 436244736 + 226981376},
-    "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "ee0bc3694a9ab89f",
-                                              "bytes": 436278272 + 215408384},
-    "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "ee0bc3694a9ab89f",
-                                            "bytes": 352372736 + 211523072},
+    "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "7c13c61cea575839",
+                                              "bytes": 436254208 + 214824960},
+    "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "7c13c61cea575839",
+                                            "bytes": 352359168 + 213289472},
     "gemm_f64_4096_rowB": {"sha": "b947734a2fa7d71b", "bytes": 3657537000 + 130594048},
     "gemm_bf16_acc16_8192": {"sha": "22df8f61666701a6", "bytes": 1485881344 + 129445888},
     "gemm_f16_256": {"sha": "22df8f61666701a6", "bytes": 580096 + 0},

@@ -210,14 +210,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 // row (one 8-byte load): the low word takes the fragment's k = 4t .. 4t+3,
 // the high word k = 16+4t .. 16+4t+3, identically in A and B.  K beyond the
 // block (K a multiple of 8) reads as zero.
-template <int MT, int NT>
+template <int MT, int NT, int KS>
 __global__ void __launch_bounds__(kThreads, 2)
     batched_i8_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B,
                       const int32_t* __restrict__ C, int32_t* __restrict__ D,
                       int M, int N, int K, int64_t batch, int group, int abid,
                       int blgp) {
+  // KS: k32 steps per chunk, all their loads in flight
   constexpr int WM = 16 * MT, WN = 8 * NT;
-  constexpr int KS = 2;  // k32 steps per chunk: all their loads in flight
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int tiles_n = N / WN;
@@ -313,7 +313,10 @@ mma_status_t run_i8(const Ctx& ctx, int64_t M, int64_t N, int64_t K,
   const int64_t cap = int64_t(ctx.num_sms) * 8;
   if (blocks > cap) blocks = cap;
   ctx.mark_start();
-  batched_i8_kernel<MT, NT><<<int(blocks), kThreads, 0, ctx.stream>>>(
+  // one 32-deep step per chunk when K fits it (no predicated-off second
+  // step): 65536 x 32^3 105.6 -> 98.2 us
+  auto kern = K <= 32 ? batched_i8_kernel<MT, NT, 1> : batched_i8_kernel<MT, NT, 2>;
+  kern<<<int(blocks), kThreads, 0, ctx.stream>>>(
       static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
       static_cast<const int32_t*>(C), static_cast<int32_t*>(D), int(M),
       int(N), int(K), batch, group, abid, blgp);
