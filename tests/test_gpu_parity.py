@@ -485,3 +485,22 @@ def test_ragged_shapes_on_cta_pairs(dtype_in):
         want, ab = oracle.gemm(dtype_in, A, g.B, C, want_absab=True)
         check(dtype_in, got, want, ab, f"{dtype_in} ragged pairs")
 
+
+
+# One row of tiles (M at most one pair row, or one 128-row tile) or one
+# column (N at most one tile): the producer loads both operands with an
+# evict-first L2 policy, on CTA pairs (256 x 20480 x 1000: 80 pair tiles)
+# and on single CTAs (128 x 8192 x 2040; 1000 x 128 x 1000), ragged in K.
+@pytest.mark.parametrize("dtype_in", ["bf16", "i8"])
+@pytest.mark.parametrize("M,N,K", [(256, 20480, 1000), (128, 8192, 2040),
+                                   (1000, 128, 1000)])
+def test_single_row_or_column_of_tiles(dtype_in, M, N, K):
+    g = synth.gemm_inputs(f"stream_ops_{M}_{N}_{K}_{dtype_in}", dtype_in, M, N, K,
+                          dist="uniform")
+    got = run_gemm(g, pad=1)
+    if dtype_in == "i8":
+        check("i8", got, oracle.gemm("i8", g.A, g.B, g.C), None,
+              f"i8 {M}x{N}x{K} single row/column of tiles")
+    else:
+        want, ab = oracle.gemm(dtype_in, g.A, g.B, g.C, want_absab=True)
+        check(dtype_in, got, want, ab, f"{dtype_in} {M}x{N}x{K} single row/column of tiles")
