@@ -14,7 +14,7 @@ import pytest
 import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import (GuardedBatch, GuardedMatrix, check, check16, dev_padded,
+from helpers import (TOL, GuardedBatch, GuardedMatrix, check, check16, dev_padded,
                      oracle_ref, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -504,3 +504,49 @@ def test_single_row_or_column_of_tiles(dtype_in, M, N, K):
     else:
         want, ab = oracle.gemm(dtype_in, g.A, g.B, g.C, want_absab=True)
         check(dtype_in, got, want, ab, f"{dtype_in} {M}x{N}x{K} single row/column of tiles")
+
+
+# IEEE special values through the tensor pipe: a NaN in A, an infinity in A
+# whose K column of B holds zeros, positives and negatives (NaN, +inf and
+# -inf results), an infinity in B met by a zero column of A, and a NaN and
+# an infinity in C.  NaN positions and infinity signs must match the
+# oracle's double arithmetic exactly; the finite outputs keep the usual
+# tolerance.  64 x 96 x 128 runs on the regular kernel, 256 x 320 x 9000 on
+# the stream-K kernel (the specials meet inside split tiles).
+_SPECIAL = {"f16": (0x7E00, 0x7C00, 0xFC00), "bf16": (0x7FC0, 0x7F80, 0xFF80)}
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(64, 96, 128), (256, 320, 9000)])
+def test_special_values_propagate(dtype_in, M, N, K):
+    nan, pinf, ninf = _SPECIAL[dtype_in]
+    g = synth.gemm_inputs(f"special_{M}_{N}_{K}_{dtype_in}", dtype_in, M, N, K,
+                          dist="uniform")
+    A, B, C = g.A.copy(), g.B.copy(), g.C.copy()   # B is column-major: N x K
+    A[3, 5] = nan                                  # row 3 all NaN
+    A[7, 0] = pinf                                 # row 7: inf * B[:, 0]
+    B[0:N:3, 0] = 0                                # ... NaN where B is 0
+    B[1:N:3, 0] = 0x3C00 if dtype_in == "f16" else 0x3F80   # +1: +inf
+    B[2:N:3, 0] = 0xBC00 if dtype_in == "f16" else 0xBF80   # -1: -inf
+    B[10, K - 1] = ninf                            # column 10: -inf * A[:, K-1]
+    A[0:M:2, K - 1] = 0                            # ... NaN in even rows
+    C[20, 30] = np.nan
+    C[21, 31] = np.inf
+    gs = synth.GemmInputs(dtype_in, M, N, K, A, B, C)
+    want, ab = oracle.gemm(dtype_in, A, B, C, want_absab=True)
+    got = run_gemm(gs)
+    assert np.array_equal(np.isnan(got), np.isnan(want)), "NaN positions differ"
+    inf_w = np.isinf(want)
+    assert np.array_equal(np.isinf(got), inf_w), "infinity positions differ"
+    assert np.array_equal(np.sign(got[inf_w]), np.sign(want[inf_w])), "infinity signs differ"
+    # the cases the inputs were built for (column 10 of row 7 also meets
+    # the -inf of B, so it is left out)
+    cols = np.arange(N) != 10
+    assert np.isnan(want[3]).all() and np.isnan(want[7, 0::3]).all()
+    assert (want[7, 1::3][cols[1::3]] == np.inf).all()
+    assert (want[7, 2::3][cols[2::3]] == -np.inf).all()
+    assert np.isnan(want[0:M:2, 10]).all()
+    fin = np.isfinite(want) & np.isfinite(ab)
+    rel, ab0 = TOL[dtype_in]
+    err = np.abs(got[fin].astype(np.float64) - want[fin])
+    assert (err <= rel * ab[fin] + ab0).all(), f"finite outputs off by up to {err.max()}"
