@@ -32,7 +32,11 @@
  *     complement.
  *   - FP64: Ogita-Rump-Oishi compensated dot product "Dot2" (TwoProduct by
  *     fma, TwoSum by Knuth), with C as one more term, so the oracle's error
- *     is about eps^2 relative to sum |a*b| plus one final rounding.
+ *     is about eps^2 relative to sum |a*b| plus one final rounding.  When a
+ *     term (a product or C) is infinite or NaN the compensation terms are
+ *     meaningless (inf - inf), and the result is the IEEE value of the
+ *     plain sum instead: NaN if a term is NaN or infinities of both signs
+ *     meet, else the infinity.
  *
  * Build: plain C11, -O2 -fopenmp -ffp-contract=off (no contraction, no
  * reassociation, no fast-math); only the loop over output rows is parallel.
@@ -309,6 +313,8 @@ static void f64_row(int64_t i, int64_t N, int64_t K, const double *A,
                     double *absab, int64_t ldabs) {
   for (int64_t j = 0; j < N; ++j) {
     double p = 0.0, s = 0.0, sa = 0.0;
+    double plain = 0.0;   /* IEEE sum of the terms, for non-finite ones */
+    int special = 0;
     for (int64_t k = 0; k < K; ++k) {
       const double a = A[i * lda + k];
       const double b = B[b_index(b_layout, k, j, ldb)];
@@ -316,14 +322,19 @@ static void f64_row(int64_t i, int64_t N, int64_t K, const double *A,
       two_prod(a, b, &h, &r);
       two_sum(p, h, &p, &q);
       s += q + r;
+      plain += h;
+      if (!isfinite(h)) special = 1;
       if (absab) sa += fabs(a) * fabs(b);
     }
     if (C) {
+      const double c = C[i * ldc + j];
       double q;
-      two_sum(p, C[i * ldc + j], &p, &q);
+      two_sum(p, c, &p, &q);
       s += q;
+      plain += c;
+      if (!isfinite(c)) special = 1;
     }
-    D[i * ldd + j] = p + s;
+    D[i * ldd + j] = special ? plain : p + s;
     if (absab) absab[i * ldabs + j] = sa;
   }
 }

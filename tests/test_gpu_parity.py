@@ -550,3 +550,31 @@ def test_special_values_propagate(dtype_in, M, N, K):
     rel, ab0 = TOL[dtype_in]
     err = np.abs(got[fin].astype(np.float64) - want[fin])
     assert (err <= rel * ab[fin] + ab0).all(), f"finite outputs off by up to {err.max()}"
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 96, 128), (200, 136, 520)])
+def test_special_values_propagate_f64(M, N, K):
+    """The same specials through the FP64 (DMMA) kernel."""
+    g = synth.gemm_inputs(f"special64_{M}_{N}_{K}", "f64", M, N, K, dist="uniform")
+    A, B, C = g.A.copy(), g.B.copy(), g.C.copy()
+    A[3, 5] = np.nan
+    A[7, 0] = np.inf
+    B[0:N:3, 0] = 0.0
+    B[1:N:3, 0] = 1.0
+    B[2:N:3, 0] = -1.0
+    B[10, K - 1] = -np.inf
+    A[0:M:2, K - 1] = 0.0
+    C[20, 30] = np.nan
+    C[21, 31] = np.inf
+    gs = synth.GemmInputs("f64", M, N, K, A, B, C)
+    want, ab = oracle.gemm("f64", A, B, C, want_absab=True)
+    got = run_gemm(gs)
+    assert np.array_equal(np.isnan(got), np.isnan(want)), "NaN positions differ"
+    inf_w = np.isinf(want)
+    assert np.array_equal(np.isinf(got), inf_w), "infinity positions differ"
+    assert np.array_equal(np.sign(got[inf_w]), np.sign(want[inf_w])), "infinity signs differ"
+    assert np.isnan(want[3]).all() and np.isnan(want[0:M:2, 10]).all()
+    fin = np.isfinite(want) & np.isfinite(ab)
+    rel, ab0 = TOL["f64"]
+    err = np.abs(got[fin] - want[fin])
+    assert (err <= rel * ab[fin] + ab0 + np.abs(want[fin]) * 2.0 ** -52).all()

@@ -286,6 +286,44 @@ def test_f64_compensation_recovers_cancelled_terms(oracle_mod):
     assert oracle_mod.gemm("f64", A, B, None)[0, 0] == 2.0 ** -60
 
 
+def test_f64_special_values_extended_reals(oracle_mod):
+    """IEEE semantics of D = A*B + C with non-finite terms (arithmetic over
+    the extended reals): an infinity plus finite terms is that infinity,
+    infinities of both signs or a NaN give NaN, 0 * inf is NaN; the same
+    for the batched branch (which shares the row kernel)."""
+    inf, nan = np.inf, np.nan
+    A = np.array([[inf, 1.0, 2.0],        # +inf + 3 + 8        -> +inf
+                  [inf, -inf, 0.5],       # +inf - inf          -> NaN
+                  [nan, 1.0, 1.0],        # NaN                 -> NaN
+                  [0.0, 1.0, 1.0],        # 0 * (-inf) in col 1 -> NaN
+                  [-inf, 1.0, 1.0],       # -inf * 3 = -inf     -> -inf
+                  [1.0, 1.0, 1.0]])       # finite; C decides
+    B = np.array([[1.0, 3.0, 4.0],        # column 0 (N x K layout)
+                  [-inf, 1.0, 1.0],       # column 1: starts with -inf
+                  [3.0, 0.0, 0.0]])       # column 2
+    C = np.zeros((6, 3))
+    C[5, 0] = inf
+    C[5, 1] = -inf
+    C[5, 2] = nan
+    D = oracle_mod.gemm("f64", A, B, C)
+    assert D[0, 0] == inf and np.isnan(D[1, 0]) and np.isnan(D[2, 0])
+    assert D[4, 0] == -inf and D[3, 0] == 7.0
+    # column 1 starts with -inf: inf * -inf = -inf, -inf * -inf = +inf
+    assert np.isnan(D[3, 1]) and D[4, 1] == inf and D[0, 1] == -inf
+    assert D[1, 1] == -inf
+    # column 2 is (3, 0, 0): -inf * 0 in row 1 gives NaN
+    assert D[0, 2] == inf and D[4, 2] == -inf and np.isnan(D[2, 2])
+    assert np.isnan(D[1, 2])
+    assert D[5, 0] == inf and D[5, 1] == -inf and np.isnan(D[5, 2])
+    # finite entries keep the compensated (exact here) value
+    assert D[3, 2] == 0.0 and D[5, 0] == inf
+    # the batched branch on the same tile (batch of 1)
+    Db = oracle_mod.gemm_batched("f64", A[None], B[None], C[None], group=1, abid=0)
+    assert np.array_equal(np.isnan(Db[0]), np.isnan(D))
+    assert np.array_equal(Db[0][np.isfinite(D)], D[np.isfinite(D)])
+    assert np.array_equal(Db[0][np.isinf(D)], D[np.isinf(D)])
+
+
 def test_f64_closed_forms(oracle_mod):
     n = 32
     rng = np.random.default_rng(5)
