@@ -14,7 +14,7 @@ import pytest
 import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import (TOL, GuardedBatch, GuardedMatrix, check, check16, dev_padded,
+from helpers import (TOL, GuardedBatch, GuardedMatrix, check, check16, decode16, dev_padded,
                      oracle_ref, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -578,3 +578,41 @@ def test_special_values_propagate_f64(M, N, K):
     rel, ab0 = TOL["f64"]
     err = np.abs(got[fin] - want[fin])
     assert (err <= rel * ab[fin] + ab0 + np.abs(want[fin]) * 2.0 ** -52).all()
+
+
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+def test_special_values_propagate_acc16(dtype_in):
+    """The same specials with a 16-bit addend and result (the kernel rounds
+    its FP32 sum once to 16 bits, the oracle its double sum), plus a finite
+    row whose sum overflows the 16-bit range (+inf in both)."""
+    M, N, K = 64, 96, 128
+    nan, pinf, ninf = _SPECIAL[dtype_in]
+    big = 0x7BFF if dtype_in == "f16" else 0x7F7F        # the largest finite
+    one = 0x3C00 if dtype_in == "f16" else 0x3F80
+    g = acc16_inputs(f"special16_{dtype_in}", dtype_in, M, N, K)
+    A, B, C = g.A.copy(), g.B.copy(), g.C.copy()
+    A[3, 5] = nan
+    A[7, 0] = pinf
+    B[0:N:3, 0] = 0
+    B[1:N:3, 0] = one
+    B[2:N:3, 0] = one | 0x8000
+    B[10, K - 1] = ninf
+    A[0:M:2, K - 1] = 0
+    C[20, 30] = nan
+    C[21, 31] = pinf
+    A[9, :] = 0                                          # row 9: 4 * big
+    A[9, 4:8] = big
+    B[:, 4:8] = one
+    gs = synth.GemmInputs(dtype_in, M, N, K, A, B, C)
+    want_bits, ab = oracle16(gs)
+    got = decode16(run_gemm16(gs), dtype_in)
+    want = decode16(want_bits, dtype_in)
+    assert np.array_equal(np.isnan(got), np.isnan(want)), "NaN positions differ"
+    inf_w = np.isinf(want)
+    assert np.array_equal(np.isinf(got), inf_w), "infinity positions differ"
+    assert np.array_equal(np.sign(got[inf_w]), np.sign(want[inf_w])), "infinity signs differ"
+    assert (want[9, np.arange(N) != 10] == np.inf).all()   # overflowed
+    fin = np.isfinite(want) & np.isfinite(ab)
+    ulp = 2.0 ** -10 if dtype_in == "f16" else 2.0 ** -7
+    err = np.abs(got[fin] - want[fin])
+    assert (err <= 1e-3 * ab[fin] + 1e-6 + ulp * np.abs(want[fin])).all()
