@@ -17,7 +17,7 @@ import pytest
 import oracle
 from mixed_precision_dense_02_gb300 import binding, synth
 
-from helpers import GuardedBatch, check, check16, to_dev
+from helpers import TOL, GuardedBatch, check, check16, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -439,3 +439,54 @@ def test_batched_padded_ld_guard(dtype_in, M, N, K, batch, pad):
     Gc.verify(f"batched {dtype_in} {M}x{N}x{K} padded ldc (input) guard")
     check(dtype_in, Gd.result(), want(bi), absab(bi) if dtype_in != "i8" else None,
           f"batched {dtype_in} {M}x{N}x{K} padded ld")
+
+
+# IEEE special values through each batched kernel: a NaN in the broadcast A
+# tile of the first group, an infinity in one entry's B met by zeros,
+# positives and negatives of its A column (NaN, +inf, -inf outputs), and a
+# NaN and an infinity in another entry's C.  NaN positions and infinity
+# signs must match the oracle; finite outputs keep the tolerance.
+_SPECIAL_BITS = {"f16": (0x7E00, 0x7C00, 0x3C00), "bf16": (0x7FC0, 0x7F80, 0x3F80)}
+
+
+@pytest.mark.parametrize("dtype_in,M,N,K,batch", [
+    ("bf16", 16, 16, 16, 64),      # streaming 16^3 kernel
+    ("bf16", 32, 32, 32, 64),      # warp-level kernel
+    ("f16", 64, 64, 64, 48),       # CTA-cooperative kernel
+    ("bf16", 128, 128, 128, 16),   # tensor-memory kernel
+    ("f64", 32, 32, 32, 32),       # FP64 batched
+])
+def test_batched_special_values(dtype_in, M, N, K, batch):
+    bi = synth.batched_inputs(f"bsv_{dtype_in}_{M}", dtype_in, batch, M=M, N=N, K=K,
+                              group=4, abid=1)
+    A, B, C = bi.A.copy(), bi.B.copy(), bi.C.copy()
+    if dtype_in == "f64":
+        nan, inf, one = np.nan, np.inf, 1.0
+        neg = lambda v: -v
+    else:
+        nan, inf, one = _SPECIAL_BITS[dtype_in]
+        neg = lambda v: v | 0x8000
+    A[1, 3, 5] = nan                 # group 0 reads A tile 1: row 3 NaN in entries 0..3
+    B[6, 2, 0] = inf                 # entry 6, column 2, k = 0
+    A[5, 0:M:3, 0] = 0               # entry 6 reads A tile 5: NaN rows
+    A[5, 1:M:3, 0] = one             # +inf rows
+    A[5, 2:M:3, 0] = neg(one)        # -inf rows
+    C[9, 4, 7] = np.nan
+    C[9, 5, 8] = np.inf
+    bs = synth.BatchedInputs(dtype_in, batch, M, N, K, 4, 1, A, B, C, 0)
+    w = want(bs)
+    got = run(bs)
+    assert np.array_equal(np.isnan(got), np.isnan(w)), "NaN positions differ"
+    inf_w = np.isinf(w)
+    assert np.array_equal(np.isinf(got), inf_w), "infinity positions differ"
+    assert np.array_equal(np.sign(got[inf_w]), np.sign(w[inf_w])), "infinity signs differ"
+    assert np.isnan(w[0:4, 3]).all() and np.isnan(w[6, 0:M:3, 2]).all()
+    assert (w[6, 1:M:3, 2] == np.inf).all() and (w[6, 2:M:3, 2] == -np.inf).all()
+    ab = absab(bs)
+    fin = np.isfinite(w) & np.isfinite(ab)
+    rel, ab0 = TOL[dtype_in]
+    err = np.abs(got[fin].astype(np.float64) - w[fin].astype(np.float64))
+    bound = rel * ab[fin] + ab0
+    if dtype_in == "f64":
+        bound = bound + np.abs(w[fin]) * 2.0 ** -52
+    assert (err <= bound).all(), f"finite outputs off by up to {err.max()}"
