@@ -71,10 +71,20 @@ constexpr int kGroupM = 16;
 //            the host; K up to about 32000): the INT32 sums start from the
 //            terms like I32EXACT's, never wrap, and each output is widened
 //            to 64 bits only to add C and clamp; no TMEM folds.
-enum class Epi { F32, I32EXACT, H16, I32SAT, I32SATW };
+//   I32SATE  as I32SATW, with C added to the INT32 sums while the chunks
+//            run (I32EXACT's early C), for problems whose exact product S
+//            lies in [-2^30, 2^30) (checked on the host from K and the
+//            operands' signedness).  The register sum then holds S + C
+//            modulo 2^32, and with the sign of C (one bit per output, kept
+//            as C is added) it fixes the saturated value: for C >= 0,
+//            S + C overflowed exactly when the wrapped sum is below -2^30;
+//            for C < 0, exactly when it is at least 2^30.  Both ranges are
+//            disjoint from the values the sum takes without overflow.
+enum class Epi { F32, I32EXACT, H16, I32SAT, I32SATW, I32SATE };
 
 constexpr bool int_mode(Epi e) {
-  return e == Epi::I32EXACT || e == Epi::I32SAT || e == Epi::I32SATW;
+  return e == Epi::I32EXACT || e == Epi::I32SAT || e == Epi::I32SATW ||
+         e == Epi::I32SATE;
 }
 
 // Chunk depth of the exact 8-bit integer modes: every partial sum must stay
@@ -108,6 +118,19 @@ struct Layout {
   static constexpr uint32_t TMEM_COLS =
       2 * BN <= 256 ? 256u : 512u;
 };
+
+// I32SATE: per epilogue warp, one 32-bit word per lane and 32 columns of
+// its half tile holding the sign bits of the C elements it added (word w of
+// lane l at index w * 32 + l), placed after the barriers.
+template <int BN>
+constexpr int sign_words() { return (BN / 2 + 31) / 32; }
+template <int BN>
+constexpr int sign_bytes() { return kEpiWarps * 32 * sign_words<BN>() * 4; }
+template <int BN, int STAGES, int CL, int NSTG, Epi EPI>
+constexpr int smem_alloc() {
+  return Layout<BN, STAGES, CL, NSTG>::ALLOC +
+         (EPI == Epi::I32SATE ? sign_bytes<BN>() : 0);
+}
 
 // Batched problems: `batch` entries of the same M x N x K shape, each tile
 // of A, B, C and D contiguous (the batch entry is the third tensor-map
@@ -454,12 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and one column half, emitted as 16-column blocks through a ring of
     // NSTG staging blocks: D leaves by TMA store, and C arrives by TMA PF
     // blocks ahead of its use -- across tile boundaries, so the next tile's
-    // first C blocks are in flight while this tile finishes.  In the exact
-    // INT8 mode the chunks' INT32 sums are kept in registers (starting from
-    // zero) and C is added only as each block is emitted, so no chunk drain
-    // ever waits on memory.  (Accumulating the chunks into D with TMA
-    // reduce-add instead was measured slower: the L2 atomics cost more than
-    // the registers.)
+    // first C blocks are in flight while this tile finishes.  In the
+    // integer modes the chunks' INT32 sums are kept in registers; C joins
+    // them either as each block is emitted or, with two staging blocks per
+    // warp, while the chunks run (early C, below).  (Accumulating the
+    // chunks into D with TMA reduce-add instead was measured slower: the L2
+    // atomics cost more than the registers.)
     // Integer modes: C is read once and D written once, while the widened
     // operands (64 MB at 4096^3) are re-read from L2 by every wave of
     // tiles; C and D take an evict-first L2 policy so they do not push
@@ -475,6 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     uint8_t* stg = smem + L::STG_OFFSET + ew * NSTG * kStgBytes;
     uint64_t* wbar = &cbar[NSTG * ew];
+    [[maybe_unused]] uint32_t* sgn =
+        reinterpret_cast<uint32_t*>(smem + L::TOTAL) + ew * sign_words<BN>() * 32;
     const bool has_c = Cv != nullptr;
     // columns per 64-byte staging row: 16 of 4 bytes, or 32 of 2 bytes
     constexpr int COLS = EPI == Epi::H16 ? 32 : 16;
@@ -498,8 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (Instances with two staging blocks per warp; with one or two chunks
     // per tile the host picks the four-block ring, whose C loads run ahead
     // in the emission instead.)
-    constexpr bool kEarlyC = EPI == Epi::I32EXACT && NSTG == 2;
+    // I32SATE takes the same early C and also keeps the sign bit of each
+    // C element it adds.
+    constexpr bool kEarlyC =
+        (EPI == Epi::I32EXACT || EPI == Epi::I32SATE) && NSTG == 2;
     static_assert(!kEarlyC || NSTG >= 2, "early C uses staging slots 0 and 1");
+    static_assert(EPI != Epi::I32SATE || kEarlyC,
+                  "I32SATE adds C while the chunks run");
     constexpr int NMP = (NBLK + 1) / 2;  // early-C steps per unit
     uint32_t cpar = 0;                   // phase parity of slots 0 and 1
     uint32_t g = 0;  // blocks emitted so far by this warp
@@ -687,8 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       [[maybe_unused]] int64_t rt = 0;
       [[maybe_unused]] int64_t ct[TG];
       if constexpr (int_mode(EPI)) {
-        // I32EXACT starts from the correction terms modulo 2^32 and
-        // I32SATW from their exact value (in range by the host's check);
+        // I32EXACT and I32SATE start from the correction terms modulo
+        // 2^32 and I32SATW from their exact value (in range by the host's
+        // check);
         // I32SAT adds them in 64 bits at its first fold.
         if (has_terms) load_terms(row0, colh, rt, ct);
         if (EPI != Epi::I32SAT && has_terms) {
@@ -711,6 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int m = 0; m < NMP; ++m) {
             if (m != mp_done) continue;
+            // I32SATE: step m's two blocks are columns [32 m, 32 m + 32)
+            // of the warp's half, one sign word per lane
+            [[maybe_unused]] uint32_t neg = 0u;
 #pragma unroll
             for (int sl = 0; sl < 2; ++sl) {
               const int jj = 2 * m + sl;
@@ -722,8 +756,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 iacc[jj * 16 + 4 * c + 1] += w.y;
                 iacc[jj * 16 + 4 * c + 2] += w.z;
                 iacc[jj * 16 + 4 * c + 3] += w.w;
+                if constexpr (EPI == Epi::I32SATE) {
+                  const int b0 = sl * 16 + 4 * c;
+                  neg |= ((w.x >> 31) << b0) | ((w.y >> 31) << (b0 + 1)) |
+                         ((w.z >> 31) << (b0 + 2)) | ((w.w >> 31) << (b0 + 3));
+                }
               }
             }
+            if constexpr (EPI == Epi::I32SATE) sgn[m * 32 + lane] = neg;
           }
           __syncwarp();  // every lane has read both slots
           cpar ^= 1u;
@@ -828,6 +868,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
+        // I32SATE: the sign bits of this block's C (none without C)
+        [[maybe_unused]] uint32_t negw = 0u;
+        if constexpr (EPI == Epi::I32SATE)
+          negw = has_c ? sgn[(j / 2) * 32 + lane] : 0u;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint4* p = chunk(buf, c);
@@ -857,6 +901,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             o.y = w.y + iacc[j * 16 + 4 * c + 1];
             o.z = w.z + iacc[j * 16 + 4 * c + 2];
             o.w = w.w + iacc[j * 16 + 4 * c + 3];
+          } else if constexpr (EPI == Epi::I32SATE) {
+            // iacc holds S + C modulo 2^32 with S in [-2^30, 2^30): the
+            // sign of C tells an overflow from a wrapped value
+            auto sat = [&](int e) {
+              const int32_t v = int32_t(iacc[j * 16 + 4 * c + e]);
+              const bool neg = (negw >> ((j & 1) * 16 + 4 * c + e)) & 1u;
+              const int32_t out = !neg && v < -(1 << 30) ? INT32_MAX
+                                  : neg && v >= (1 << 30) ? INT32_MIN
+                                                          : v;
+              return uint32_t(out);
+            };
+            o.x = sat(0);
+            o.y = sat(1);
+            o.z = sat(2);
+            o.w = sat(3);
           } else {
             // exact 64-bit sum, saturated once to the INT32 range
             auto sat = [&](uint32_t cw, int e) {
@@ -1192,8 +1251,8 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
                  int kb_per_chunk, BatchArgs bat, const int64_t* row_term,
                  const int64_t* col_term,
                  TestHook hook = TestHook{kWaitLimitNs, 0}) {
-  using L = Layout<BN, STAGES, CL, NSTG>;
-  static_assert(L::ALLOC <= 232448, "shared memory per CTA");
+  constexpr int kSmem = smem_alloc<BN, STAGES, CL, NSTG, EPI>();
+  static_assert(kSmem <= 232448, "shared memory per CTA");
   const CUtensorMapDataType cd_type =
       int_mode(EPI)        ? CU_TENSOR_MAP_DATA_TYPE_INT32
       : EPI == Epi::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -1222,7 +1281,7 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   bool attr_ok = false;
   if (!smem_attr.get(ctx, &attr_ok, [&](bool* v) {
         *v = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  L::ALLOC) == cudaSuccess;
+                                  kSmem) == cudaSuccess;
         if (!*v) cudaGetLastError();
         return *v;
       }))
@@ -1232,7 +1291,7 @@ mma_status_t run(const Ctx& ctx, bool pdl, int64_t M, int64_t N, int64_t K,
   if (units > int64_t(INT32_MAX)) return MMA_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = ctx.stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1360,7 +1419,13 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
   // emitted, within one chunk's MMA time, which needs 4 staging blocks per
   // warp (2 C loads ahead), so they keep five stages.  Single-CTA wide
   // tiles (48 KB stages) take four stages and 2 staging blocks.
-  if constexpr (EPI != Epi::I32SAT) {
+  if constexpr (EPI == Epi::I32SATE) {
+    // early C only: 224-wide pair tiles with two staging blocks per warp
+    // (256-wide ones leave no room for the sign words); the host picks
+    // this mode for those tiles and three or more chunks
+    if (cl == 2 && bn == 224)
+      return run<224, 6, BF16, EPI, 2, 2>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+  } else if constexpr (EPI != Epi::I32SAT) {
     // 224-wide pair tiles (FP32 and exact-INT32 results: 112 columns per
     // epilogue warp, seven 16-column blocks)
     if constexpr (EPI == Epi::F32 || EPI == Epi::I32EXACT ||
@@ -1400,8 +1465,12 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
     if (cl == 1 && (K + BK - 1) / BK <= 4)
       return run<128, 4, BF16, EPI, 1, 6>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
   }
-  return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
-                 : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+  if constexpr (EPI == Epi::I32SATE) {
+    return MMA_ERR_UNSUPPORTED;
+  } else {
+    return cl == 2 ? run<128, 6, BF16, EPI, 2, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term)
+                   : run<128, 5, BF16, EPI, 1, 4>(ctx, pdl, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, kpc, bat, row_term, col_term);
+  }
 }
 
 // Row-major B (K x N, N contiguous) -> K-major copy W (N rows of K, leading
@@ -1645,6 +1714,17 @@ mma_status_t launch_gemm_i8_tc(const Ctx& ctx, int64_t M, int64_t N,
   if (cudaGetLastError() != cudaSuccess) return MMA_ERR_LAUNCH;
   const int cl = cluster_size(ctx, M, N, K);
   if (clamp) {
+    // C joins the INT32 sums while the chunks run (as in the exact mode)
+    // when the exact product's magnitude stays below 2^30, on 224-wide
+    // pair tiles, from three chunks per tile up.
+    const int bn = tile_n(ctx, M, N, 1, cl, true);
+    const double amax = a_signed ? 128.0 : 255.0;
+    const double bmax = b_signed ? 128.0 : 255.0;
+    if (cl == 2 && bn == 224 && K > 2 * kI8ChunkK &&
+        double(K) * amax * bmax < 1073741824.0)
+      return dispatch<true, Epi::I32SATE>(ctx, true, bn, cl, M, N, K, W, ldw,
+                                          Bw, ldw, C, ldc, D, ldd, row_term,
+                                          col_term);
     // Largest magnitude of any partial INT32 sum when the sums start from
     // the correction terms: each chunk adds at most 2^24, and
     // |row term| + |column term| <= K * (128 ob + 128 oa + oa ob).

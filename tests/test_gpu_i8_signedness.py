@@ -210,3 +210,91 @@ def test_saturating_modes_either_side_of_the_int32_reach(K):
         want, _ = oracle.gemm_i8_ex(A, B, C, clamp=clamp)
         got = run_i8x(A, B, C, clamp=clamp)
         check("i8", got, want, None, f"uu K={K} clamp={clamp}")
+
+
+def _routes_to_early_c_saturation(M, N, K, sa, sb, num_sms):
+    """Whether a saturating product runs with C added during the chunk
+    phase: 224-wide CTA-pair tiles (the library's tile-width choice: at
+    least one 256-wide tile per SM, and fewer columns of waves with 224),
+    three or more 1024-deep chunks, and K * max|a| * max|b| < 2^30."""
+    wide = -(-M // 128) * -(-N // 256)
+    if not (N > 128 and wide >= num_sms):
+        return False
+    pairs, m_units = num_sms // 2, -(-M // 256)
+    cost = lambda bn: -(-(m_units * -(-N // bn)) // pairs) * bn
+    amax, bmax = (128 if sa else 255), (128 if sb else 255)
+    return cost(224) < cost(256) and K > 2048 and K * amax * bmax < (1 << 30)
+
+
+def _aimed_c(S, seed):
+    """C for which S + C lands on the edges of the INT32 range and on the
+    values +-2^30 where the wrapped sum changes meaning: each output draws a
+    target from the list and takes C = target - S when that C is itself an
+    INT32, otherwise a uniform C."""
+    targets = np.array([I32_MAX, I32_MAX + 1, I32_MAX + 7, I32_MIN, I32_MIN - 1,
+                        I32_MIN - 9, (1 << 30) - 1, 1 << 30, -(1 << 30),
+                        -(1 << 30) - 1, I32_MAX + (1 << 30) - 3,
+                        I32_MIN - (1 << 30) + 3, 0], np.int64)
+    rng = np.random.default_rng(seed)
+    t = targets[rng.integers(0, len(targets), S.shape)]
+    c = t - S.astype(np.int64)
+    fallback = rng.integers(I32_MIN, I32_MAX, S.shape, endpoint=True)
+    ok = (c >= I32_MIN) & (c <= I32_MAX)
+    return np.where(ok, c, fallback).astype(np.int32)
+
+
+@pytest.mark.parametrize("sa,sb", SIGNS, ids=[_tag(*s) for s in SIGNS])
+@pytest.mark.parametrize("b_layout", ["col", "row"])
+def test_saturation_with_c_added_during_the_chunks(sa, sb, b_layout):
+    """Saturating products on 224-wide pair tiles: C is added to the INT32
+    sums while the chunks run, so the sums hold S + C modulo 2^32 and the
+    sign of C decides, at emission, whether the result crossed an end of the
+    range.  Outputs are aimed at both ends (in range by one, out of range by
+    one), at the values +-2^30 and at the farthest reachable overflows, on a
+    ragged shape (edge tiles cut in M and N, three chunks and a tail in K),
+    with and without C."""
+    import torch
+    M, N, K = 2000, 3900, 3000 + 40
+    assert _routes_to_early_c_saturation(
+        M, N, K, sa, sb, torch.cuda.get_device_properties(0).multi_processor_count)
+    g = synth.gemm_inputs("i8x_sate", "i8", M, N, K, a_signed=sa, b_signed=sb,
+                          b_layout=b_layout)
+    S, ov = oracle.gemm_i8_ex(g.A, g.B, None, clamp=False, b_layout=b_layout)
+    assert ov == 0 and int(np.abs(S.astype(np.int64)).max()) < (1 << 30)
+    C = _aimed_c(S, 41 + 2 * sa + sb)
+    want, n_over = oracle.gemm_i8_ex(g.A, g.B, C, clamp=True, b_layout=b_layout)
+    got = run_i8x(g.A, g.B, C, clamp=True, b_layout=b_layout)
+    check("i8", got, want, None, f"{_tag(sa, sb)} early-C saturation {b_layout}-B")
+    assert n_over > 0 and np.any(got == I32_MAX)
+    if sa or sb:
+        # products of either sign: the low end is crossed too (with both
+        # operands unsigned S >= 0, so S + C never falls below INT32_MIN)
+        assert np.any(got == I32_MIN)
+    # in-range results on either side of +-2^30 are present too
+    assert np.any(got == (1 << 30)) and np.any(got == -(1 << 30))
+    got0 = run_i8x(g.A, g.B, None, clamp=True, b_layout=b_layout)
+    check("i8", got0, S, None, f"{_tag(sa, sb)} early-C saturation C=None")
+
+
+@pytest.mark.parametrize("K", [16512, 16513])
+def test_early_c_saturation_bound_on_k(K):
+    """Unsigned x unsigned: K * 255^2 stays below 2^30 up to K = 16512,
+    where C joins the sums during the chunks; from K = 16513 the sums
+    keep S exact and C is added at emission.  Rows and columns of 255 give
+    the largest S; C is aimed at the range's edges."""
+    import torch
+    M, N = 2048, 2432
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert _routes_to_early_c_saturation(M, N, K, False, False, sms) == (K == 16512)
+    rng = np.random.default_rng(K)
+    A = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    B = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    A[::3] = 255
+    B[::4] = 255
+    S, _ = oracle.gemm_i8_ex(A, B, None, clamp=False)
+    C = _aimed_c(S, K)
+    want, n_over = oracle.gemm_i8_ex(A, B, C, clamp=True)
+    got = run_i8x(A, B, C, clamp=True)
+    check("i8", got, want, None, f"uu K={K} saturation")
+    # S >= 0 here, so only the top of the range can be crossed
+    assert n_over > 0 and np.any(got == I32_MAX)
