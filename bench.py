@@ -63,15 +63,15 @@ BF16_FLOP_PER_SM_CLK = 8192.0
 NCU_TRAFFIC: dict = {
     # one ncu capture per workload (dram__bytes_read.sum and
     # dram__bytes_write.sum of one launch after the warm-up launches)
-    "gemm_i8_4096": {"sha": "22df8f61666701a6", "bytes": 156990720 + 36182784},
-    "gemm_u8_4096_clamp": {"sha": "22df8f61666701a6", "bytes": 163757824 + 36275968},
-    "gemm_bf16_8192": {"sha": "22df8f61666701a6", "bytes": 1629129472 + 259018240},
-    "gemm_bf16_skinny_16384x128x4096": {"sha": "22df8f61666701a6",
-                                        "bytes": 143720448 + 3141888},
+    "gemm_i8_4096": {"sha": "2b87d5f638b5e79f", "bytes": 157382144 + 36154880},
+    "gemm_u8_4096_clamp": {"sha": "2b87d5f638b5e79f", "bytes": 156731904 + 36141568},
+    "gemm_bf16_8192": {"sha": "2b87d5f638b5e79f", "bytes": 1632362496 + 258151424},
+    "gemm_bf16_skinny_16384x128x4096": {"sha": "2b87d5f638b5e79f",
+                                        "bytes": 143721472 + 2897408},
     "batched_bf16_16x16x16_b262144_g4_abid1": {"sha": "e9a765212730005e",
                                                "bytes": 436228352 + 225458688},
-    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "22df8f61666701a6",
-                                                "bytes": 901588224 + 490481664},
+    "batched_bf16_128x128x128_b8192_g4_abid1": {"sha": "2b87d5f638b5e79f",
+                                                "bytes": 904013824 + 490111488},
     "batched_bf16_64x64x64_b16384_g4_abid1": {"sha": "5e2d44fac663ee87",
                                               "bytes": 436244736 + 226981376},
     "batched_bf16_32x32x32_b65536_g4_abid1": {"sha": "7c13c61cea575839",
@@ -79,8 +79,8 @@ NCU_TRAFFIC: dict = {
     "batched_i8_32x32x32_b65536_g4_abid1": {"sha": "7c13c61cea575839",
                                             "bytes": 352359168 + 213289472},
     "gemm_f64_4096_rowB": {"sha": "b947734a2fa7d71b", "bytes": 3657537000 + 130594048},
-    "gemm_bf16_acc16_8192": {"sha": "22df8f61666701a6", "bytes": 1485881344 + 129445888},
-    "gemm_f16_256": {"sha": "22df8f61666701a6", "bytes": 580096 + 0},
+    "gemm_bf16_acc16_8192": {"sha": "2b87d5f638b5e79f", "bytes": 1482969600 + 128653824},
+    "gemm_f16_256": {"sha": "2b87d5f638b5e79f", "bytes": 580096 + 0},
     "gemm_bf16_deepk_1024x1024x32768": {"sha": "b39718a8ce94b2da",
                                         "bytes": 138511104 + 3083008},
 }
