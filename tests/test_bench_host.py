@@ -178,3 +178,26 @@ def test_bench_kernel_attribution_follows_the_library_routing():
     skinny = dict(deep, M=16384, N=128, K=4096)           # 128 tiles >= 76
     assert bench.kernel_source(skinny).endswith("gemm_tc.cu")
     assert bench.kernel_source(dict(deep, acc16=True)).endswith("gemm_tc.cu")
+
+
+def test_saturating_early_c_rule_in_the_library():
+    """The saturating 8-bit path adds C during the chunk phase only on
+    224-wide CTA-pair tiles with three or more 1024-deep chunks and
+    K * max|a| * max|b| < 2^30; the GPU tests aim their shapes with a mirror
+    of this rule, so it is pinned here against the library source."""
+    path = os.path.join(ROOT, "mixed_precision_dense_02_gb300", "csrc", "gemm_tc.cu")
+    with open(path, encoding="utf-8") as f:
+        src = f.read()
+    assert "const double amax = a_signed ? 128.0 : 255.0;" in src
+    assert "const double bmax = b_signed ? 128.0 : 255.0;" in src
+    assert "if (cl == 2 && bn == 224 && K > 2 * kI8ChunkK &&" in src
+    assert "double(K) * amax * bmax < 1073741824.0)" in src
+    assert "constexpr int kI8ChunkK = 1024;" in src
+    # the mode's shared-memory sign words fit beside the 224-wide pair
+    # layout (six stages, two staging blocks per warp) but not the 256-wide
+    stage224 = 128 * 64 * 2 + 112 * 64 * 2
+    stage256 = 128 * 64 * 2 + 128 * 64 * 2
+    staging, bars, slack = 8 * 2 * 32 * 16 * 4, (2 * 6 + 5 + 2 * 8) * 8 + 16, 1024
+    sign = 8 * 32 * 4 * 4
+    assert 6 * stage224 + staging + bars + slack + sign <= 232448
+    assert 6 * stage256 + staging + bars + slack + sign > 232448
