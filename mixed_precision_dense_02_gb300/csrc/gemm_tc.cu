@@ -1414,10 +1414,11 @@ mma_status_t dispatch(const Ctx& ctx, bool pdl, int bn, int cl, int64_t M,
   // exact-INT32 results take six stages and 2 staging blocks per warp
   // (FP32 and 16-bit drain one accumulator per tile, with a whole tile of
   // MMA work to hide it; exact INT32 adds C to its register sums while the
-  // chunks run, from three 1024-deep chunks per tile up).  The saturating
-  // mode, and exact INT32 with one or two chunks, add C as each block is
-  // emitted, within one chunk's MMA time, which needs 4 staging blocks per
-  // warp (2 C loads ahead), so they keep five stages.  Single-CTA wide
+  // chunks run, from three 1024-deep chunks per tile up; so do saturated
+  // INT32 results whose products stay below 2^30, I32SATE).  The other
+  // saturating modes, and exact INT32 with one or two chunks, add C as
+  // each block is emitted, within one chunk's MMA time, which needs 4
+  // staging blocks per warp (2 C loads ahead), so they keep five stages.  Single-CTA wide
   // tiles (48 KB stages) take four stages and 2 staging blocks.
   if constexpr (EPI == Epi::I32SATE) {
     // early C only: 224-wide pair tiles with two staging blocks per warp
